@@ -1,0 +1,238 @@
+"""Python binding of libtcg, the GB300 (sm_103a) mixed-precision tensor-core GEMM.
+
+D = alpha * op(A) * op(B) + beta * C with FP16/BF16 (or TF32-rounded FP32)
+inputs, exact products, FP32 accumulation and an FP32 or round-to-nearest-even
+FP16/BF16 output.  The C ABI is declared in ``include/tcg.h``; this module only
+marshals arguments into it (ctypes).  PyTorch is used for device memory and
+streams.  Every step of the GEMM runs in the library's CUDA kernels: if the
+in-tree ``_lib/libtcg.so`` is missing, calls raise -- there is no fallback.
+
+Names mirror the C ABI: ``tcg_create``, ``tcg_destroy``, ``tcg_set_stream``,
+``tcg_set_workspace``, ``tcg_gemm_workspace_size``, ``tcg_gemm_ex``,
+``tcg_gemm_strided_batched``, ``tcg_get_device_error``, ``tcg_status_string``,
+``tcg_set_debug``, ``tcg_launch_count``.  ``Handle`` and ``gemm_rowmajor`` are
+conveniences on top of them.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libtcg.so")
+
+# enums (include/tcg.h)
+TCG_STATUS_SUCCESS = 0
+TCG_STATUS_NOT_INITIALIZED = 1
+TCG_STATUS_INVALID_VALUE = 2
+TCG_STATUS_NOT_SUPPORTED = 3
+TCG_STATUS_ARCH_MISMATCH = 4
+TCG_STATUS_EXECUTION_FAILED = 5
+TCG_STATUS_TIMEOUT = 6
+TCG_STATUS_ALLOC_FAILED = 7
+TCG_OP_N, TCG_OP_T = 0, 1
+TCG_R_16F, TCG_R_16BF, TCG_R_32F = 0, 1, 2
+TCG_COMPUTE_32F, TCG_COMPUTE_32F_FAST_TF32 = 0, 1
+
+EXPORTS = ("tcg_create", "tcg_destroy", "tcg_set_stream", "tcg_set_workspace",
+           "tcg_gemm_workspace_size", "tcg_gemm_ex", "tcg_gemm_strided_batched",
+           "tcg_get_device_error", "tcg_last_device_error_bits", "tcg_status_string",
+           "tcg_set_debug", "tcg_launch_count")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class TcgError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {tcg_status_string(status)}" if what else
+                         tcg_status_string(status))
+
+
+def load_library(path: str | None = None) -> ctypes.CDLL:
+    """Load the in-tree libtcg.so (built by ``__graft_entry__.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"libtcg.so not found at {p}; build it first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(p)
+        i64, vp, ci, f32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        st = ctypes.c_int
+        lib.tcg_create.restype = st
+        lib.tcg_create.argtypes = [ctypes.POINTER(vp)]
+        lib.tcg_destroy.restype = st
+        lib.tcg_destroy.argtypes = [vp]
+        lib.tcg_set_stream.restype = st
+        lib.tcg_set_stream.argtypes = [vp, vp]
+        lib.tcg_set_workspace.restype = st
+        lib.tcg_set_workspace.argtypes = [vp, vp, ctypes.c_size_t]
+        lib.tcg_gemm_workspace_size.restype = st
+        lib.tcg_gemm_workspace_size.argtypes = [ci, ci, i64, i64, i64, ci, ci, i64,
+                                                ctypes.POINTER(ctypes.c_size_t)]
+        lib.tcg_gemm_ex.restype = st
+        lib.tcg_gemm_ex.argtypes = [vp, ci, ci, i64, i64, i64, f32, vp, ci, i64, vp, ci, i64,
+                                    f32, vp, ci, i64, ci]
+        lib.tcg_gemm_strided_batched.restype = st
+        lib.tcg_gemm_strided_batched.argtypes = [vp, ci, ci, i64, i64, i64, f32, vp, ci, i64,
+                                                 i64, vp, ci, i64, i64, f32, vp, ci, i64, i64,
+                                                 i64, ci]
+        lib.tcg_get_device_error.restype = st
+        lib.tcg_get_device_error.argtypes = [vp]
+        lib.tcg_last_device_error_bits.restype = ctypes.c_uint32
+        lib.tcg_last_device_error_bits.argtypes = [vp]
+        lib.tcg_status_string.restype = ctypes.c_char_p
+        lib.tcg_status_string.argtypes = [ci]
+        lib.tcg_set_debug.restype = st
+        lib.tcg_set_debug.argtypes = [vp, ctypes.c_uint64, ci]
+        lib.tcg_launch_count.restype = ctypes.c_uint64
+        lib.tcg_launch_count.argtypes = [vp]
+        _lib = lib
+        return lib
+
+
+def _ptr(x) -> int | None:
+    """Device pointer of a torch tensor, or an int/None passed through."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+# ---------------------------------------------------------------- raw C ABI
+def tcg_create() -> int:
+    h = ctypes.c_void_p()
+    s = load_library().tcg_create(ctypes.byref(h))
+    if s != TCG_STATUS_SUCCESS:
+        raise TcgError(s, "tcg_create")
+    return h.value
+
+
+def tcg_destroy(h: int) -> int:
+    return load_library().tcg_destroy(h)
+
+
+def tcg_set_stream(h: int, stream: int | None) -> int:
+    return load_library().tcg_set_stream(h, stream)
+
+
+def tcg_set_workspace(h: int, ptr, nbytes: int) -> int:
+    return load_library().tcg_set_workspace(h, _ptr(ptr), nbytes)
+
+
+def tcg_gemm_workspace_size(transa, transb, m, n, k, Atype, compute, batch_count=1) -> int:
+    out = ctypes.c_size_t(0)
+    s = load_library().tcg_gemm_workspace_size(transa, transb, m, n, k, Atype, compute,
+                                               batch_count, ctypes.byref(out))
+    if s != TCG_STATUS_SUCCESS:
+        raise TcgError(s, "tcg_gemm_workspace_size")
+    return out.value
+
+
+def tcg_gemm_ex(h, transa, transb, m, n, k, alpha, A, Atype, lda, B, Btype, ldb, beta, C,
+                Ctype, ldc, compute) -> int:
+    """Status of the C call; A, B, C are torch tensors or raw device pointers."""
+    return load_library().tcg_gemm_ex(h, transa, transb, m, n, k, float(alpha), _ptr(A), Atype,
+                                      lda, _ptr(B), Btype, ldb, float(beta), _ptr(C), Ctype,
+                                      ldc, compute)
+
+
+def tcg_gemm_strided_batched(h, transa, transb, m, n, k, alpha, A, Atype, lda, strideA, B,
+                             Btype, ldb, strideB, beta, C, Ctype, ldc, strideC, batch_count,
+                             compute) -> int:
+    return load_library().tcg_gemm_strided_batched(
+        h, transa, transb, m, n, k, float(alpha), _ptr(A), Atype, lda, strideA, _ptr(B), Btype,
+        ldb, strideB, float(beta), _ptr(C), Ctype, ldc, strideC, batch_count, compute)
+
+
+def tcg_get_device_error(h: int) -> int:
+    return load_library().tcg_get_device_error(h)
+
+
+def tcg_last_device_error_bits(h: int) -> int:
+    return load_library().tcg_last_device_error_bits(h)
+
+
+def tcg_status_string(s: int) -> str:
+    return load_library().tcg_status_string(s).decode()
+
+
+def tcg_set_debug(h: int, wait_limit_ns: int = 0, fault_inject: int = 0) -> int:
+    return load_library().tcg_set_debug(h, wait_limit_ns, fault_inject)
+
+
+def tcg_launch_count(h: int) -> int:
+    return load_library().tcg_launch_count(h)
+
+
+# ------------------------------------------------------------ conveniences
+_TORCH_TYPE = {}
+
+
+def dtype_code(t) -> int:
+    import torch
+    if not _TORCH_TYPE:
+        _TORCH_TYPE.update({torch.float16: TCG_R_16F, torch.bfloat16: TCG_R_16BF,
+                            torch.float32: TCG_R_32F})
+    return _TORCH_TYPE[t]
+
+
+class Handle:
+    """Owns a tcgHandle_t bound to a torch CUDA stream."""
+
+    def __init__(self, stream=None):
+        self.h = tcg_create()
+        self.set_stream(stream)
+
+    def set_stream(self, stream=None):
+        import torch
+        if stream is None and torch.cuda.is_available():
+            stream = torch.cuda.current_stream()
+        self.stream = stream
+        check(tcg_set_stream(self.h, stream.cuda_stream if stream is not None else None),
+              "tcg_set_stream")
+
+    def close(self):
+        if self.h:
+            tcg_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def check(status: int, what: str = "") -> None:
+    if status != TCG_STATUS_SUCCESS:
+        raise TcgError(status, what)
+
+
+def gemm_rowmajor(handle: Handle, A, B, C, alpha=1.0, beta=0.0, tf32=False) -> None:
+    """Row-major D = alpha*A@B + beta*C in place in C (torch CUDA tensors).
+
+    A: (m, k) or (batch, m, k); B: (k, n) or (batch, k, n); C: (m, n) or
+    (batch, m, n), all contiguous row-major.  Issued as the column-major call
+    gemm(N, N, n, m, k, alpha, B, n, A, k, beta, C, n) (C^T = B^T A^T).
+    """
+    batched = A.dim() == 3
+    m, k = A.shape[-2:]
+    n = B.shape[-1]
+    at, ct = dtype_code(A.dtype), dtype_code(C.dtype)
+    comp = TCG_COMPUTE_32F_FAST_TF32 if (tf32 or A.dtype.is_floating_point and
+                                         at == TCG_R_32F) else TCG_COMPUTE_32F
+    if not batched:
+        s = tcg_gemm_ex(handle.h, TCG_OP_N, TCG_OP_N, n, m, k, alpha, B, at, n, A, at, k, beta,
+                        C, ct, n, comp)
+    else:
+        batch = A.shape[0]
+        s = tcg_gemm_strided_batched(handle.h, TCG_OP_N, TCG_OP_N, n, m, k, alpha, B, at, n,
+                                     k * n, A, at, k, m * k, beta, C, ct, n, m * n, batch, comp)
+    check(s, "gemm_rowmajor")

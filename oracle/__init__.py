@@ -1,0 +1,155 @@
+"""CPU oracle for the mixed-precision tensor-core GEMM -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py`` (its CPU-baseline
+leg and its ``--impl reference`` arm) may import this package.  The product
+library never calls it, and it shares no code with the CUDA path.
+
+The arithmetic lives in ``tcg_oracle.c`` (plain C, FP64 accumulation, its own
+FP16/BF16/TF32 rounding); this module compiles it with gcc and marshals numpy
+arrays into it.  What it computes, and which passage each step follows, is
+written at the top of ``tcg_oracle.c``.
+
+Parity pins (all in ``tests/test_oracle_*.py``): closed forms (all-ones,
+identity), small-integer inputs against int64 matmul, a 16x16x16 brute force in
+exact rational arithmetic, the accumulation and subnormal examples of "NVIDIA
+Tensor Core混合精度计算原理与应用解析" sections 2.2.1 and 2.2.3, rounding routines
+against numpy/torch conversions, TF32 rounding exhaustively against a second
+formulation, and numpy float64 matmul on random inputs.  Non-integer GPU results
+are held to the error bound of section 2.3 of that page, not to exact bits.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "tcg_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
+
+F16, BF16, F32 = 0, 1, 2
+OP_N, OP_T = 0, 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile tcg_oracle.c into oracle/_build/liboracle.so with gcc."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+           "-shared", "-pthread", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        i64, dbl, vp, ci = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int
+        lib.orc_gemm.restype = ci
+        lib.orc_gemm.argtypes = [ci, ci, i64, i64, i64, dbl, vp, ci, i64, vp, ci, i64,
+                                 dbl, vp, ci, i64, ci, i64, i64, i64, i64, vp, i64,
+                                 vp, vp, ci]
+        for name in ("orc_f16_to_f64_array", "orc_bf16_to_f64_array",
+                     "orc_tf32_round_bits_array", "orc_f64_to_f16_array",
+                     "orc_f64_to_bf16_array", "orc_f64_to_f32_array"):
+            fn = getattr(lib, name)
+            fn.restype = None
+            fn.argtypes = [vp, vp, i64]
+        lib.orc_tf32_round_bits.restype = ctypes.c_uint32
+        lib.orc_tf32_round_bits.argtypes = [ctypes.c_uint32]
+        _lib = lib
+        return lib
+
+
+def tf32_round_fn_address() -> int:
+    """Address of the scalar ``uint32_t orc_tf32_round_bits(uint32_t)``."""
+    lib = _load()
+    return ctypes.cast(lib.orc_tf32_round_bits, ctypes.c_void_p).value
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _array_call(name, a, out_dtype):
+    a = np.ascontiguousarray(a)
+    out = np.empty(a.shape, dtype=out_dtype)
+    getattr(_load(), name)(_ptr(a), _ptr(out), a.size)
+    return out
+
+
+def f16_to_f64(bits):
+    return _array_call("orc_f16_to_f64_array", np.asarray(bits, dtype=np.uint16), np.float64)
+
+
+def bf16_to_f64(bits):
+    return _array_call("orc_bf16_to_f64_array", np.asarray(bits, dtype=np.uint16), np.float64)
+
+
+def tf32_round_bits(bits):
+    return _array_call("orc_tf32_round_bits_array", np.asarray(bits, dtype=np.uint32), np.uint32)
+
+
+def f64_to_f16_bits(x):
+    return _array_call("orc_f64_to_f16_array", np.asarray(x, dtype=np.float64), np.uint16)
+
+
+def f64_to_bf16_bits(x):
+    return _array_call("orc_f64_to_bf16_array", np.asarray(x, dtype=np.float64), np.uint16)
+
+
+def f64_to_f32(x):
+    return _array_call("orc_f64_to_f32_array", np.asarray(x, dtype=np.float64), np.float32)
+
+
+_ELEM_DTYPE = {F16: np.uint16, BF16: np.uint16, F32: np.float32}
+
+
+def gemm(transa, transb, m, n, k, alpha, A, atype, lda, B, btype, ldb, beta, C, ctype,
+         ldc, tf32=False, rows=None, cols=None, nthreads=None, want_r=True,
+         want_abs=True):
+    """Block of D = alpha*op(A)*op(B) + beta*C (column-major, BLAS arguments).
+
+    ``A``, ``B``, ``C`` are flat numpy arrays holding the raw storage (FP16/BF16
+    as uint16 bit patterns, FP32 as float32); ``C`` may be None when beta == 0.
+    ``rows=(i0, i1)``, ``cols=(j0, j1)`` select the block of D to compute.
+    Returns ``(D, R, absAB)``: D as a (i1-i0, j1-j0) array in the output storage
+    type, R = alpha*S + beta*C in FP64 and absAB = sum_p |a_ip||b_pj|, or None
+    for those not requested.
+    """
+    i0, i1 = rows if rows is not None else (0, m)
+    j0, j1 = cols if cols is not None else (0, n)
+    nr, nc = i1 - i0, j1 - j0
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    A = np.ascontiguousarray(A) if A is not None else None
+    B = np.ascontiguousarray(B) if B is not None else None
+    C = np.ascontiguousarray(C) if C is not None else None
+    D = np.zeros(max(nr * nc, 1), dtype=_ELEM_DTYPE[ctype])
+    R = np.zeros(max(nr * nc, 1), dtype=np.float64) if want_r else None
+    AB = np.zeros(max(nr * nc, 1), dtype=np.float64) if want_abs else None
+    rc = _load().orc_gemm(int(transa), int(transb), int(m), int(n), int(k), float(alpha),
+                          _ptr(A), int(atype), int(lda), _ptr(B), int(btype), int(ldb),
+                          float(beta), _ptr(C), int(ctype), int(ldc), int(bool(tf32)),
+                          int(i0), int(i1), int(j0), int(j1), _ptr(D), int(max(nr, 1)),
+                          _ptr(R), _ptr(AB), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"orc_gemm failed with code {rc}")
+
+    def shape(x):
+        return None if x is None else x[: nr * nc].reshape(nc, nr).T
+    return shape(D), shape(R), shape(AB)
