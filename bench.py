@@ -1,0 +1,432 @@
+#!/usr/bin/env python3
+"""Benchmark of the mixed-precision tensor-core GEMM on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+A step is one call of the library's GEMM (the whole hot path) on one batch of
+synthetic input already resident in HBM.  Default workload: the 8192^3 FP16 ->
+FP32 GEMM (A, B uniform[-1,1] rounded to FP16, beta = 0, seed 1).  Prints one
+JSON line (rank 0).  Under torchrun (--gpus N > 1) every rank runs an
+independent replica ("replicas only": the GEMM has no exchange step), timing is
+bracketed by a barrier and a device synchronisation and the max over ranks is
+taken; value = all ranks' FLOPs / that time.
+
+--impl reference times the CPU oracle (the plain FP64 C implementation under
+oracle/), as it stands, on this host's cores, on bounded samples of the same
+workload, and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s and % of dense tensor peak (FP16→FP32, 8192³) on 1 GB300"
+UNIT = "TFLOP/s"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def traffic_record(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel source (its source digest must match), else None."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mixed_precision_tensor_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    digest = h.hexdigest()[:16]
+    with open(p) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            kv = dict(x.split("=", 1) for x in line.split())
+            if kv.get("kernel") == kernel and kv.get("workload") == workload and \
+                    kv.get("source_sha") == digest:
+                return float(kv["dram_bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def mark_begin(self):
+        self.t0 = _dt.datetime.now()
+
+    def mark_end(self):
+        self.t1 = _dt.datetime.now()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                sm, smax = float(parts[2]), float(parts[3])
+            except ValueError:
+                continue
+            rows.append((ts, sm, smax, parts))
+        during = [r for r in rows if self.t0 and self.t1 and self.t0 <= r[0] <= self.t1]
+        use = during if during else rows[-3:]
+        if not use:
+            return None
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in use:
+            for nm, v in zip(names, r[3][6:10]):
+                if v.strip().lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(r[1] for r in use),
+                "sm_max_mhz": max(r[2] for r in use),
+                "samples": len(use), "samples_in_timed_region": len(during),
+                "reasons": sorted(reasons)}
+
+
+def dist_setup(n_gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl"
+        try:
+            import torch
+            if not torch.cuda.is_available():
+                backend = "gloo"
+        except Exception:
+            backend = "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() and \
+        dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------- CPU oracle
+def oracle_blocks(w, A, B, rows_per_block, count, seed):
+    """Sampled output blocks (rows_per_block x 128, full k) of the row-major D."""
+    from mixed_precision_tensor_gb300 import workloads as wl
+    tiles = wl.sample_tiles(w.m, w.n, count=count, tile=128, seed=seed)
+    return [(i0, min(i0 + rows_per_block, i1), j0, j1) for (i0, i1, j0, j1) in tiles]
+
+
+def time_oracle(w, A, B, C, blocks, nthreads):
+    import numpy as np
+
+    import oracle
+    codes = {"f16": oracle.F16, "bf16": oracle.BF16, "f32": oracle.F32}
+
+    def rawv(x):
+        return x.view(np.uint16) if x.dtype == np.float16 else x
+    flops = 0.0
+    t0 = time.perf_counter()
+    for (i0, i1, j0, j1) in blocks:
+        # the column-major call the library gets: gemm(N, N, n, m, k, B, n, A, k, C, n)
+        oracle.gemm(oracle.OP_N, oracle.OP_N, w.n, w.m, w.k, w.alpha,
+                    rawv(B[0]).reshape(-1), codes[w.in_type], w.n,
+                    rawv(A[0]).reshape(-1), codes[w.in_type], w.k,
+                    w.beta, None if C is None else rawv(C[0]).reshape(-1), codes[w.out_type],
+                    w.n, tf32=(w.in_type == "f32"), rows=(j0, j1), cols=(i0, i1),
+                    nthreads=nthreads, want_r=False, want_abs=False)
+        flops += 2.0 * (i1 - i0) * (j1 - j0) * w.k
+    return time.perf_counter() - t0, flops
+
+
+def cpu_baseline(w, A, B, C, budget_s=12.0):
+    """The oracle timed on this host's cores on a bounded sample of the workload."""
+    nthreads = os.cpu_count() or 1
+    blk = oracle_blocks(w, A, B, 128, 1, seed=w.seed)
+    dt1, fl1 = time_oracle(w, A, B, C, blk, nthreads)
+    count = max(1, min(256, int(budget_s / max(dt1, 1e-6))))
+    blocks = oracle_blocks(w, A, B, 128, count, seed=w.seed)
+    dt, fl = time_oracle(w, A, B, C, blocks, nthreads)
+    return {"value": fl / dt / 1e12, "unit": UNIT, "cores": nthreads, "kind": "oracle",
+            "sample": f"{len(blocks)} seeded 128x128 output tiles of the {w.m}x{w.n}x{w.k} "
+                      f"GEMM, full k each ({fl:.3e} FLOP in {dt:.2f} s)"}
+
+
+# ------------------------------------------------------------------ main arms
+def run_reference(args, w):
+    world, rank, _ = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")), 0
+    if rank != 0:
+        return 0
+    from mixed_precision_tensor_gb300 import workloads as wl
+    import oracle
+    oracle.build()
+    A, B, C = wl.draw(w)
+    nthreads = os.cpu_count() or 1
+    # Size one step so the whole run stays within about two minutes.
+    probe = oracle_blocks(w, A, B, 16, 1, seed=w.seed)
+    dtp, _ = time_oracle(w, A, B, C, probe, nthreads)
+    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
+    rows = 128
+    while rows > 8 and dtp * rows / 16 > per_step_budget:
+        rows //= 2
+    blocks = oracle_blocks(w, A, B, rows, 1, seed=w.seed)
+    for _ in range(args.warmup):
+        time_oracle(w, A, B, C, blocks, nthreads)
+    tot_t, tot_f = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, fl = time_oracle(w, A, B, C, blocks, nthreads)
+        tot_t += dt
+        tot_f += fl
+    value = tot_f / tot_t / 1e12
+    sample = (f"each step: one {rows}x128 output block of the {w.m}x{w.n}x{w.k} GEMM, "
+              f"full k ({tot_f / args.steps:.3e} FLOP)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "m": w.m, "n": w.n, "k": w.k,
+                       "in": w.in_type, "out": w.out_type, "batch": w.batch},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": nthreads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, w):
+    import numpy as np
+    import torch
+
+    import mixed_precision_tensor_gb300 as tcg
+    from mixed_precision_tensor_gb300 import workloads as wl
+
+    world, rank, local = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    tcg.load_library()
+    peaks, peak_src = load_peaks()
+
+    A, B, C = wl.draw(w)
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+    squeeze = w.batch == 1
+
+    def host(x):
+        a = np.ascontiguousarray(x[0] if squeeze else x)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+
+    def to_dev(x, t):
+        tt = host(x).to(dev)
+        return tt.view(torch.bfloat16) if t == "bf16" else tt
+    dA, dB = to_dev(A, w.in_type), to_dev(B, w.in_type)
+    oshape = (w.m, w.n) if squeeze else (w.batch, w.m, w.n)
+    dC0 = to_dev(C, w.out_type) if C is not None else None
+    dC = dC0.clone() if dC0 is not None else torch.empty(oshape, dtype=tdt[w.out_type],
+                                                         device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    h = tcg.Handle(stream)
+    tf32 = w.in_type == "f32"
+    in_bytes = A.nbytes + B.nbytes + (C.nbytes if C is not None else 0)
+    flush = None
+    if in_bytes < 2 * L2_BYTES:
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def step():
+        tcg.gemm_rowmajor(h, dA, dB, dC, alpha=w.alpha, beta=w.beta, tf32=tf32)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    tcg.check(tcg.tcg_get_device_error(h.h), "warm-up")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    launches0 = tcg.tcg_launch_count(h.h)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.mark_begin()
+    with torch.cuda.stream(stream):
+        g0.record(stream)
+        for i in range(args.steps):
+            if flush is not None:
+                flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        g1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    sampler.mark_end()
+    launches = tcg.tcg_launch_count(h.h) - launches0
+    tcg.check(tcg.tcg_get_device_error(h.h), "timed region")
+    clocks = sampler.stop()
+    kernel_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps
+    region_ms = g0.elapsed_time(g1)
+    step_ms = kernel_ms if flush is not None else region_ms / args.steps
+    step_ms_max = max_over_ranks(step_ms, world)
+    value = w.flops * world / (step_ms_max * 1e-3) / 1e12
+
+    # End to end through the C ABI: pinned host inputs -> device -> GEMM -> host result.
+    hA = host(A).pin_memory()
+    hB = host(B).pin_memory()
+    hC = host(C).pin_memory() if C is not None else None
+    hD = torch.empty(oshape, dtype=tdt[w.out_type] if w.out_type != "bf16" else torch.int16
+                     ).pin_memory()
+    e2e_steps = max(3, min(20, args.steps // 10))
+    h2d = hA.nbytes + hB.nbytes + (hC.nbytes if hC is not None else 0)
+    d2h = hD.nbytes
+
+    def e2e_step():
+        dA.copy_(hA.view(torch.bfloat16) if w.in_type == "bf16" else hA, non_blocking=True)
+        dB.copy_(hB.view(torch.bfloat16) if w.in_type == "bf16" else hB, non_blocking=True)
+        if hC is not None:
+            dC.copy_(hC.view(torch.bfloat16) if w.out_type == "bf16" else hC, non_blocking=True)
+        step()
+        hD.copy_(dC.view(torch.int16) if w.out_type == "bf16" else dC, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    e2e_value = w.flops * world / (e2e_ms * 1e-3) / 1e12
+    tcg.check(tcg.tcg_get_device_error(h.h), "e2e")
+
+    bound = "hbm" if w.flops / max(1, w.algorithmic_bytes()) < 284 else "tensor"
+    if bound == "tensor":
+        peak = float(peaks["bf16_tflops"])        # FP16 and BF16 share the dense rate
+        if w.in_type == "f32":
+            peak = peak / 2.0                     # TF32 dense rate: half of FP16/BF16
+        achieved = w.flops / (kernel_ms * 1e-3) / 1e12
+        unit = "TFLOP/s"
+    else:
+        peak = float(peaks["hbm_gbs"])
+        achieved = w.algorithmic_bytes() / (kernel_ms * 1e-3) / 1e9
+        unit = "GB/s"
+    traffic = traffic_record("tcg_gemm_kernel", w.name)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": step_ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": {"f16": "f16", "bf16": "bf16", "f32": "tf32"}[w.in_type],
+        "data": "synthetic",
+        "config": {"workload": w.name, "m": w.m, "n": w.n, "k": w.k, "batch": w.batch,
+                   "in": w.in_type, "accumulate": "f32", "out": w.out_type,
+                   "alpha": w.alpha, "beta": w.beta, "seed": w.seed,
+                   "l2": ("inputs larger than L2" if flush is None else
+                          "L2 flushed between steps (write of a 258 MiB buffer)"),
+                   "parallelism": f"replicas x{world}"},
+        "pct_of_peak": 100.0 * value / world / (peak if bound == "tensor" else float(
+            peaks["bf16_tflops"])),
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{peak_src} ({'bf16_tflops' if bound == 'tensor' else 'hbm_gbs'})"},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, A, B, C)
+    h.close()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    from mixed_precision_tensor_gb300 import workloads as wl
+    w = wl.WORKLOADS[args.workload or wl.HEADLINE]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,190 @@
+/*
+ * tcg.h -- C ABI of libtcg, a mixed-precision tensor-core GEMM for GB300
+ * (sm_103a).
+ *
+ * The one operation (every entry point below serves it):
+ *
+ *     D = alpha * op(A) * op(B) + beta * C
+ *
+ *   - "Programming Tensor Cores in CUDA 9", section "什么是张量核?" and Figure 2:
+ *     16-bit floating-point inputs, full-precision products, FP32 accumulation;
+ *     C and D may be FP16 or FP32.
+ *   - same page, section "如何在 cuBLAS 中使用张量核": the GemmEx argument list
+ *     (transa, transb, m, n, k, alpha, A, Atype, lda, B, Btype, ldb, beta, C,
+ *     Ctype, ldc, compute type); C is overwritten by D.  Its dimension rules
+ *     (k, lda, ldb, ldc multiples of 8, m a multiple of 4) become the 16-byte
+ *     rule below, and ragged m, n, k are supported.  Its silent fallback to a
+ *     non-tensor-core routine is replaced by an explicit status.
+ *   - same page, section "CUDA 9.0 中张量核的编程访问" (the wmma_example
+ *     kernel): column-major storage with leading dimensions; alpha and beta
+ *     applied elementwise to the accumulated product.
+ *   - "CUDA Handbook, 17.5 Tensor Cores": TF32 mode, FP32 inputs rounded to
+ *     TF32 (8-bit exponent, 10-bit mantissa) before the product, FP32
+ *     accumulation.  libtcg rounds to nearest, ties to even.
+ *   - "NVIDIA Tensor Core混合精度计算原理与应用解析", section 2.3: the final
+ *     output is rounded to nearest even.
+ *
+ * Storage is column-major (BLAS).  op(A) is m x k, op(B) is k x n, C and D are
+ * m x n and share the buffer C (D overwrites C; Ctype is both the C input type
+ * and the D output type).  op(X) = X for TCG_OP_N and X^T for TCG_OP_T.  A
+ * row-major problem D = A*B + C (A m x k, B k x n, all row-major) is the
+ * column-major call gemm(N, N, n, m, k, alpha, B, n, A, k, beta, C, n).
+ *
+ * Supported (Atype = Btype, compute, Ctype) combinations; everything else
+ * returns TCG_STATUS_NOT_SUPPORTED (no fallback of any kind):
+ *     16F  / 32F            / 32F or 16F
+ *     16BF / 32F            / 32F or 16BF
+ *     32F  / 32F_FAST_TF32  / 32F
+ *
+ * Ownership and threading.  The caller owns every device buffer; libtcg never
+ * frees or keeps them.  All calls are asynchronous on the handle's stream and
+ * return without a device synchronisation (except tcg_get_device_error).  A
+ * handle is not thread-safe: use one per host thread.  C must not overlap A or
+ * B.  The first GEMM call on a handle binds it to the current device and
+ * allocates a 4-byte device error word; make that call before any stream
+ * capture.  The TF32 path needs a workspace (see tcg_set_workspace).
+ *
+ * Pointers are device pointers (or memory the device can access, e.g. managed
+ * memory) unless stated otherwise.
+ */
+#ifndef TCG_H_
+#define TCG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TCG_STATUS_SUCCESS = 0,
+    TCG_STATUS_NOT_INITIALIZED = 1,  /* no usable CUDA device / runtime */
+    TCG_STATUS_INVALID_VALUE = 2,    /* argument check failed; nothing launched */
+    TCG_STATUS_NOT_SUPPORTED = 3,    /* type combination not offered */
+    TCG_STATUS_ARCH_MISMATCH = 4,    /* device is not compute capability 10.3 */
+    TCG_STATUS_EXECUTION_FAILED = 5, /* a launch or CUDA call failed */
+    TCG_STATUS_TIMEOUT = 6,          /* a bounded device wait gave up (sticky word) */
+    TCG_STATUS_ALLOC_FAILED = 7      /* workspace / error word allocation failed */
+} tcgStatus_t;
+
+typedef enum { TCG_OP_N = 0, TCG_OP_T = 1 } tcgOp_t;
+
+typedef enum {
+    TCG_R_16F = 0,   /* IEEE binary16 */
+    TCG_R_16BF = 1,  /* bfloat16: upper 16 bits of an IEEE binary32 */
+    TCG_R_32F = 2    /* IEEE binary32 */
+} tcgDataType_t;
+
+typedef enum {
+    TCG_COMPUTE_32F = 0,            /* exact products, FP32 accumulation */
+    TCG_COMPUTE_32F_FAST_TF32 = 1   /* FP32 inputs rounded (RNE) to TF32 first */
+} tcgComputeType_t;
+
+typedef struct tcgContext *tcgHandle_t;
+
+/* Create a handle.  Makes no CUDA call (device binding happens on first use).
+ * Errors: INVALID_VALUE if h is NULL, ALLOC_FAILED if host memory runs out. */
+tcgStatus_t tcg_create(tcgHandle_t *h);
+
+/* Destroy a handle: synchronises its stream if it was used, frees the error
+ * word and any workspace that libtcg allocated itself (never the caller's).
+ * Errors: INVALID_VALUE if h is NULL. */
+tcgStatus_t tcg_destroy(tcgHandle_t h);
+
+/* Set the stream (a cudaStream_t passed as void*) for later calls; NULL is the
+ * legacy default stream.  Errors: INVALID_VALUE if h is NULL. */
+tcgStatus_t tcg_set_stream(tcgHandle_t h, void *stream);
+
+/* Give the handle caller-owned device scratch memory for the TF32 path (which
+ * writes TF32-rounded, K-major copies of op(A) and op(B) before the product).
+ * ptr must be 256-byte aligned; bytes may be 0 to detach.  Without a caller
+ * workspace the handle grows one of its own with cudaMalloc on the first TF32
+ * call that needs more (not capture-safe).  Errors: INVALID_VALUE. */
+tcgStatus_t tcg_set_workspace(tcgHandle_t h, void *ptr, size_t bytes);
+
+/* Bytes of workspace a tcg_gemm_strided_batched call with these arguments
+ * needs (0 for the 16-bit paths).  Errors: INVALID_VALUE (NULL bytes). */
+tcgStatus_t tcg_gemm_workspace_size(tcgOp_t transa, tcgOp_t transb, int64_t m, int64_t n,
+                                    int64_t k, tcgDataType_t Atype,
+                                    tcgComputeType_t compute, int64_t batch_count,
+                                    size_t *bytes);
+
+/*
+ * D = alpha*op(A)*op(B) + beta*C, column-major.
+ *
+ *   m, n, k      >= 0.  m == 0 or n == 0: no-op.  k == 0 or alpha == 0:
+ *                D = beta*C and A, B are not read.  beta == 0: C is not read
+ *                (NaN in C does not propagate).
+ *   A, lda       op(A) data; lda >= m (OP_N) or >= k (OP_T), lda >= 1.
+ *   B, ldb       op(B) data; ldb >= k (OP_N) or >= n (OP_T), ldb >= 1.
+ *   C, ldc       in: C (read only if beta != 0); out: D.  ldc >= max(1, m).
+ *   alpha, beta  FP32 scalars passed by value.
+ *
+ * Alignment (the TMA 16-byte rule): A, B, C 16-byte aligned; lda, ldb, ldc
+ * times the element size a multiple of 16 bytes.
+ *
+ * Accuracy: FP32 accumulation of exact products; per element
+ * |D - exact| <= k*2^-23*(|alpha|*(|A||B|)_ij + |beta|*|C_ij|), plus one output
+ * ulp for 16-bit outputs (the error model of "NVIDIA Tensor Core混合精度计算原理
+ * 与应用解析", section 2.3, with p = 23).  Integer-valued inputs whose sums stay
+ * exact in FP32 give bit-exact results.
+ *
+ * Returns SUCCESS once the work is queued.  INVALID_VALUE: NULL handle or
+ * needed pointer, negative sizes, ld too small, misaligned pointer or ld.
+ * NOT_SUPPORTED: type/compute combination.  ARCH_MISMATCH: not sm_103.
+ * EXECUTION_FAILED: launch error.  ALLOC_FAILED: first-use allocations.
+ */
+tcgStatus_t tcg_gemm_ex(tcgHandle_t h, tcgOp_t transa, tcgOp_t transb, int64_t m, int64_t n,
+                        int64_t k, float alpha, const void *A, tcgDataType_t Atype,
+                        int64_t lda, const void *B, tcgDataType_t Btype, int64_t ldb,
+                        float beta, void *C, tcgDataType_t Ctype, int64_t ldc,
+                        tcgComputeType_t compute);
+
+/*
+ * batch_count independent GEMMs; matrix i uses A + i*strideA, B + i*strideB,
+ * C + i*strideC (strides in elements).  This is the strided-batched form of
+ * tcg_gemm_ex, for many small problems in one launch ("NVIDIA Tensor Core混合
+ * 精度计算原理与应用解析", section 6.2 item 3: merge small matrices into larger
+ * units of work).  Same rules as tcg_gemm_ex, plus: batch_count >= 0 (0 is a
+ * no-op); strides >= 0 and times the element size a multiple of 16 bytes;
+ * strideC == 0 with batch_count > 1 is INVALID_VALUE (outputs would alias).
+ */
+tcgStatus_t tcg_gemm_strided_batched(tcgHandle_t h, tcgOp_t transa, tcgOp_t transb,
+                                     int64_t m, int64_t n, int64_t k, float alpha,
+                                     const void *A, tcgDataType_t Atype, int64_t lda,
+                                     int64_t strideA, const void *B, tcgDataType_t Btype,
+                                     int64_t ldb, int64_t strideB, float beta, void *C,
+                                     tcgDataType_t Ctype, int64_t ldc, int64_t strideC,
+                                     int64_t batch_count, tcgComputeType_t compute);
+
+/* Synchronise the handle's stream, then return and clear the sticky device
+ * error word: SUCCESS, or TIMEOUT if a bounded wait inside a kernel gave up
+ * (the kernel then stopped early and its output is undefined), or
+ * EXECUTION_FAILED if the synchronisation itself reported an error.  Returns
+ * SUCCESS for a handle that has launched nothing.  INVALID_VALUE: NULL h. */
+tcgStatus_t tcg_get_device_error(tcgHandle_t h);
+
+/* Raw value of the last device error word read by tcg_get_device_error (bit
+ * flags saying which wait gave up); 0 if none.  For diagnostics. */
+uint32_t tcg_last_device_error_bits(tcgHandle_t h);
+
+/* Static string naming a status. */
+const char *tcg_status_string(tcgStatus_t s);
+
+/* Test hooks.  wait_limit_ns bounds every device-side wait (0 restores the
+ * default of 2 s).  fault_inject = 1 makes the next GEMM launches skip the
+ * first operand load of the first tile, so the consumer's bounded wait runs
+ * out and the kernel reports TIMEOUT through the error word (no fault, no
+ * trap); 0 turns it off.  INVALID_VALUE: NULL h. */
+tcgStatus_t tcg_set_debug(tcgHandle_t h, uint64_t wait_limit_ns, int fault_inject);
+
+/* Number of GEMM-path kernel launches this handle has made (for the
+ * benchmark's launch count).  Returns 0 for NULL. */
+uint64_t tcg_launch_count(tcgHandle_t h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TCG_H_ */

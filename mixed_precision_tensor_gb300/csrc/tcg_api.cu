@@ -1,0 +1,535 @@
+// tcg_api.cu -- host runtime and C ABI of libtcg (declared in include/tcg.h).
+//
+// Order of work in a GEMM call:
+//   1. argument checks (pure host code, no CUDA call): the GemmEx argument rules of
+//      "Programming Tensor Cores in CUDA 9", section "如何在 cuBLAS 中使用张量核",
+//      restated for TMA (16-byte aligned pointers and leading dimensions);
+//   2. device binding on first use (compute capability 10.3, SM count, error word);
+//   3. dispatch: k == 0 or alpha == 0 -> D = beta*C kernel; TF32 -> round-and-pack
+//      kernels into the workspace, then the GEMM kernel on the packed copies;
+//      FP16/BF16 -> the GEMM kernel straight on the caller's operands;
+//   4. tensor maps (cached per pointer/shape/stride/type) and a persistent grid of
+//      min(tiles, SMs) CTAs on the handle's stream.
+
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "tcg.h"
+#include "tcg_internal.h"
+
+using namespace tcg;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+constexpr int kMapCacheSize = 32;
+
+struct MapKey {
+    const void *ptr;
+    int dtype;
+    uint64_t dims[3];
+    uint64_t strides[2];
+    uint32_t box[3];
+    bool operator==(const MapKey &o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
+};
+
+struct MapEntry {
+    MapKey key;
+    CUtensorMap map;
+    bool valid;
+};
+
+}  // namespace
+
+struct tcgContext {
+    int device = -1;
+    int num_sms = 0;
+    cudaStream_t stream = nullptr;
+    uint32_t *d_err = nullptr;
+    void *ws_user = nullptr;
+    size_t ws_user_bytes = 0;
+    void *ws_own = nullptr;
+    size_t ws_own_bytes = 0;
+    unsigned long long wait_limit_ns = kDefaultWaitNs;
+    int fault_inject = 0;
+    uint64_t launches = 0;
+    uint32_t last_err_bits = 0;
+    bool used = false;
+    EncodeTiledFn encode = nullptr;
+    MapEntry cache[kMapCacheSize];
+    int cache_next = 0;
+};
+
+namespace {
+
+int elem_size(tcgDataType_t t) { return t == TCG_R_32F ? 4 : 2; }
+
+bool valid_type(int t) { return t == TCG_R_16F || t == TCG_R_16BF || t == TCG_R_32F; }
+
+int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Problem {
+    tcgOp_t transa, transb;
+    int64_t m, n, k;
+    float alpha, beta;
+    const void *A; tcgDataType_t Atype; int64_t lda; int64_t strideA;
+    const void *B; tcgDataType_t Btype; int64_t ldb; int64_t strideB;
+    void *C; tcgDataType_t Ctype; int64_t ldc; int64_t strideC;
+    int64_t batch;
+    tcgComputeType_t compute;
+    bool batched;
+};
+
+// Pure host argument checks: no CUDA call is made before they pass.
+tcgStatus_t check_args(const Problem &p)
+{
+    if ((p.transa != TCG_OP_N && p.transa != TCG_OP_T) ||
+        (p.transb != TCG_OP_N && p.transb != TCG_OP_T))
+        return TCG_STATUS_INVALID_VALUE;
+    if (!valid_type(p.Atype) || !valid_type(p.Btype) || !valid_type(p.Ctype))
+        return TCG_STATUS_INVALID_VALUE;
+    if (p.compute != TCG_COMPUTE_32F && p.compute != TCG_COMPUTE_32F_FAST_TF32)
+        return TCG_STATUS_INVALID_VALUE;
+    if (p.m < 0 || p.n < 0 || p.k < 0 || p.batch < 0)
+        return TCG_STATUS_INVALID_VALUE;
+    // Supported (A/B, compute, C) combinations.
+    if (p.Atype != p.Btype)
+        return TCG_STATUS_NOT_SUPPORTED;
+    if (p.Atype == TCG_R_32F) {
+        if (p.compute != TCG_COMPUTE_32F_FAST_TF32 || p.Ctype != TCG_R_32F)
+            return TCG_STATUS_NOT_SUPPORTED;
+    } else {
+        if (p.compute != TCG_COMPUTE_32F)
+            return TCG_STATUS_NOT_SUPPORTED;
+        if (p.Ctype != TCG_R_32F && p.Ctype != p.Atype)
+            return TCG_STATUS_NOT_SUPPORTED;
+    }
+    // Leading dimensions (BLAS rules), then the 16-byte TMA rule.
+    const int64_t a_rows = p.transa == TCG_OP_N ? p.m : p.k;
+    const int64_t b_rows = p.transb == TCG_OP_N ? p.k : p.n;
+    if (p.lda < max64(1, a_rows) || p.ldb < max64(1, b_rows) || p.ldc < max64(1, p.m))
+        return TCG_STATUS_INVALID_VALUE;
+    const int ea = elem_size(p.Atype), ec = elem_size(p.Ctype);
+    if ((p.lda * ea) % 16 || (p.ldb * ea) % 16 || (p.ldc * ec) % 16)
+        return TCG_STATUS_INVALID_VALUE;
+    if (p.batched) {
+        if (p.strideA < 0 || p.strideB < 0 || p.strideC < 0)
+            return TCG_STATUS_INVALID_VALUE;
+        if ((p.strideA * ea) % 16 || (p.strideB * ea) % 16 || (p.strideC * ec) % 16)
+            return TCG_STATUS_INVALID_VALUE;
+        if (p.strideC == 0 && p.batch > 1)
+            return TCG_STATUS_INVALID_VALUE;
+    }
+    // Limits of the kernels' 32-bit tile and TMA coordinates.
+    const int64_t lim = (int64_t(1) << 31) - 1;
+    if (p.m > lim || p.n > lim || p.k > lim || p.batch > lim)
+        return TCG_STATUS_NOT_SUPPORTED;
+    if (p.m == 0 || p.n == 0 || p.batch == 0)
+        return TCG_STATUS_SUCCESS;
+    const bool reads_ab = p.k > 0 && p.alpha != 0.0f;
+    if (!p.C || !aligned16(p.C))
+        return TCG_STATUS_INVALID_VALUE;
+    if (reads_ab && (!p.A || !p.B || !aligned16(p.A) || !aligned16(p.B)))
+        return TCG_STATUS_INVALID_VALUE;
+    const int64_t tiles_m = (p.m + kBM - 1) / kBM, tiles_n = (p.n + kBN - 1) / kBN;
+    if (tiles_m * tiles_n * p.batch > lim)
+        return TCG_STATUS_NOT_SUPPORTED;
+    return TCG_STATUS_SUCCESS;
+}
+
+tcgStatus_t bind_device(tcgContext *h)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return TCG_STATUS_NOT_INITIALIZED;
+    }
+    if (h->device >= 0) {
+        return dev == h->device ? TCG_STATUS_SUCCESS : TCG_STATUS_INVALID_VALUE;
+    }
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return TCG_STATUS_NOT_INITIALIZED;
+    }
+    if (major != 10 || minor != 3)
+        return TCG_STATUS_ARCH_MISMATCH;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+        cudaGetLastError();
+        return TCG_STATUS_NOT_INITIALIZED;
+    }
+    uint32_t *err = nullptr;
+    if (cudaMalloc(&err, sizeof(uint32_t)) != cudaSuccess) {
+        cudaGetLastError();
+        return TCG_STATUS_ALLOC_FAILED;
+    }
+    if (cudaMemset(err, 0, sizeof(uint32_t)) != cudaSuccess) {
+        cudaFree(err);
+        cudaGetLastError();
+        return TCG_STATUS_EXECUTION_FAILED;
+    }
+    h->encode = reinterpret_cast<EncodeTiledFn>(fn);
+    h->d_err = err;
+    h->num_sms = sms;
+    h->device = dev;
+    return TCG_STATUS_SUCCESS;
+}
+
+CUtensorMapDataType map_type(tcgDataType_t t)
+{
+    switch (t) {
+    case TCG_R_16F: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    case TCG_R_16BF: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    default: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    }
+}
+
+// Rank-3 tiled map {inner, outer, batch} with 128-byte swizzle, zero fill out of range.
+tcgStatus_t get_map(tcgContext *h, const void *ptr, tcgDataType_t t, uint64_t inner,
+                    uint64_t outer, uint64_t batch, uint64_t ld_bytes, uint64_t bstride_bytes,
+                    uint32_t box_inner, uint32_t box_outer, CUtensorMap *out)
+{
+    MapKey key;
+    std::memset(&key, 0, sizeof key);
+    key.ptr = ptr;
+    key.dtype = static_cast<int>(t);
+    key.dims[0] = inner; key.dims[1] = outer; key.dims[2] = batch;
+    key.strides[0] = ld_bytes; key.strides[1] = bstride_bytes;
+    key.box[0] = box_inner; key.box[1] = box_outer; key.box[2] = 1;
+    for (int i = 0; i < kMapCacheSize; ++i) {
+        if (h->cache[i].valid && h->cache[i].key == key) {
+            *out = h->cache[i].map;
+            return TCG_STATUS_SUCCESS;
+        }
+    }
+    alignas(64) CUtensorMap map;
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = h->encode(&map, map_type(t), 3, const_cast<void *>(ptr), key.dims, key.strides,
+                           key.box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return TCG_STATUS_EXECUTION_FAILED;
+    MapEntry &e = h->cache[h->cache_next];
+    h->cache_next = (h->cache_next + 1) % kMapCacheSize;
+    e.key = key;
+    e.map = map;
+    e.valid = true;
+    *out = map;
+    return TCG_STATUS_SUCCESS;
+}
+
+// Map for one operand as the kernel loads it.  rows = M (for A) or N (for B); box_rows
+// = 128 (A) or 256 (B).  K-major: {K, rows, batch}, box {k_per_block, box_rows}.
+// M/N-major: {rows, K, batch}, box {mn_box, k_per_block}.
+tcgStatus_t operand_map(tcgContext *h, const void *ptr, tcgDataType_t t, bool kmajor,
+                        int64_t rows, int64_t k, int64_t ld, int64_t stride, int64_t batch,
+                        int box_rows, int k_per_block, int mn_box, bool *bcast, CUtensorMap *out)
+{
+    const int es = elem_size(t);
+    const bool bc = (batch > 1 && stride == 0);
+    *bcast = bc;
+    const uint64_t nb = bc ? 1 : static_cast<uint64_t>(batch);
+    const uint64_t ldb = static_cast<uint64_t>(ld) * es;
+    const uint64_t inner = kmajor ? k : rows, outer = kmajor ? rows : k;
+    uint64_t bstride = static_cast<uint64_t>(stride) * es;
+    if (nb == 1)
+        bstride = ldb * outer;                  // unused; any legal value
+    if (bstride == 0)
+        bstride = 16;
+    if (kmajor)
+        return get_map(h, ptr, t, inner, outer, nb, ldb, bstride, k_per_block, box_rows, out);
+    return get_map(h, ptr, t, inner, outer, nb, ldb, bstride, mn_box, k_per_block, out);
+}
+
+int out_kind(tcgDataType_t c)
+{
+    return c == TCG_R_32F ? kOutF32 : (c == TCG_R_16F ? kOutF16 : kOutBF16);
+}
+
+size_t tf32_ws_bytes(int64_t m, int64_t n, int64_t k, int64_t batch)
+{
+    const int64_t kp = (k + 3) / 4 * 4;
+    const size_t a = ((size_t)(batch * m * kp) * 4 + 255) / 256 * 256;
+    const size_t b = ((size_t)(batch * n * kp) * 4 + 255) / 256 * 256;
+    return a + b;
+}
+
+tcgStatus_t run(tcgContext *h, const Problem &p)
+{
+    tcgStatus_t st = check_args(p);
+    if (st != TCG_STATUS_SUCCESS)
+        return st;
+    if (p.m == 0 || p.n == 0 || p.batch == 0)
+        return TCG_STATUS_SUCCESS;
+    st = bind_device(h);
+    if (st != TCG_STATUS_SUCCESS)
+        return st;
+    h->used = true;
+    const int ok = out_kind(p.Ctype);
+    const int m = static_cast<int>(p.m), n = static_cast<int>(p.n), k = static_cast<int>(p.k);
+    const int batch = static_cast<int>(p.batch);
+    const int64_t strideC = p.batched ? p.strideC : 0;
+
+    if (p.k == 0 || p.alpha == 0.0f) {
+        const int64_t total = p.m * p.n * p.batch;
+        int64_t blocks = (total + 255) / 256;
+        const int64_t cap = static_cast<int64_t>(h->num_sms) * 8;
+        if (blocks > cap) blocks = cap;
+        cudaError_t e = launch_scale(p.C, p.C, m, n, p.ldc, strideC, batch, p.beta, ok,
+                                     static_cast<int>(blocks), h->stream);
+        h->launches += 1;
+        return e == cudaSuccess ? TCG_STATUS_SUCCESS : TCG_STATUS_EXECUTION_FAILED;
+    }
+
+    const bool tf32 = p.compute == TCG_COMPUTE_32F_FAST_TF32;
+    const void *Aop = p.A, *Bop = p.B;
+    bool a_kmajor = p.transa == TCG_OP_T;   // op(A) = A^T: K is A's contiguous dim
+    bool b_kmajor = p.transb == TCG_OP_N;   // op(B) = B:   K is B's contiguous dim
+    int64_t lda = p.lda, ldb = p.ldb;
+    int64_t sA = p.batched ? p.strideA : 0, sB = p.batched ? p.strideB : 0;
+
+    if (tf32) {
+        // Round to TF32 (nearest even) into K-major packed copies in the workspace.
+        const size_t need = tf32_ws_bytes(p.m, p.n, p.k, p.batch);
+        void *ws = nullptr;
+        if (h->ws_user) {
+            if (h->ws_user_bytes < need)
+                return TCG_STATUS_INVALID_VALUE;
+            ws = h->ws_user;
+        } else {
+            if (h->ws_own_bytes < need) {
+                if (h->ws_own) {
+                    cudaStreamSynchronize(h->stream);
+                    cudaFree(h->ws_own);
+                    h->ws_own = nullptr;
+                    h->ws_own_bytes = 0;
+                }
+                if (cudaMalloc(&h->ws_own, need) != cudaSuccess) {
+                    cudaGetLastError();
+                    h->ws_own = nullptr;
+                    return TCG_STATUS_ALLOC_FAILED;
+                }
+                h->ws_own_bytes = need;
+            }
+            ws = h->ws_own;
+        }
+        const int64_t kp = (p.k + 3) / 4 * 4;
+        uint8_t *Ak = static_cast<uint8_t *>(ws);
+        uint8_t *Bk = Ak + ((size_t)(p.batch * p.m * kp) * 4 + 255) / 256 * 256;
+        const int grid = h->num_sms * 8;
+        // op(A) element (i, p): A[p + i*lda] if A^T else A[i + p*lda]
+        cudaError_t e = launch_tf32_pack(p.A, p.lda, sA, a_kmajor ? 1 : 0, m, k, batch, Ak, kp,
+                                         p.m * kp, grid, h->stream);
+        if (e == cudaSuccess)
+            e = launch_tf32_pack(p.B, p.ldb, sB, b_kmajor ? 1 : 0, n, k, batch, Bk, kp,
+                                 p.n * kp, grid, h->stream);
+        h->launches += 2;
+        if (e != cudaSuccess)
+            return TCG_STATUS_EXECUTION_FAILED;
+        Aop = Ak;
+        Bop = Bk;
+        a_kmajor = b_kmajor = true;
+        lda = ldb = kp;
+        sA = p.m * kp;
+        sB = p.n * kp;
+    }
+
+    GemmArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.m = m; a.n = n; a.k = k; a.batch = batch;
+    a.num_m_tiles = (m + kBM - 1) / kBM;
+    a.num_n_tiles = (n + kBN - 1) / kBN;
+    a.k_per_block = tf32 ? 32 : 64;
+    a.num_k_blocks = (k + a.k_per_block - 1) / a.k_per_block;
+    a.total_tiles = a.num_m_tiles * a.num_n_tiles * batch;
+    a.group_m = 16;
+    a.a_kmajor = a_kmajor ? 1 : 0;
+    a.b_kmajor = b_kmajor ? 1 : 0;
+    a.is_tf32 = tf32 ? 1 : 0;
+    a.mn_box = tf32 ? 32 : 64;
+    const uint32_t fmt = tf32 ? 2u : (p.Atype == TCG_R_16BF ? 1u : 0u);
+    a.idesc = (1u << 4)                               // D: FP32
+              | (fmt << 7) | (fmt << 10)              // A, B formats
+              | ((a_kmajor ? 0u : 1u) << 15)          // A: 0 = K-major, 1 = M-major
+              | ((b_kmajor ? 0u : 1u) << 16)          // B: 0 = K-major, 1 = N-major
+              | (static_cast<uint32_t>(kBN >> 3) << 17)
+              | (static_cast<uint32_t>(kBM >> 4) << 24);
+    a.alpha = p.alpha;
+    a.beta = p.beta;
+    a.C = p.C;
+    a.D = p.C;
+    a.ldc = p.ldc;
+    a.strideC = strideC;
+    a.err = h->d_err;
+    a.wait_limit_ns = h->wait_limit_ns;
+    a.fault_inject = h->fault_inject;
+
+    const tcgDataType_t at = tf32 ? TCG_R_32F : p.Atype;
+    CUtensorMap tmA, tmB;
+    bool abc = false, bbc = false;
+    st = operand_map(h, Aop, at, a_kmajor, p.m, p.k, lda, sA, p.batch, kBM, a.k_per_block,
+                     a.mn_box, &abc, &tmA);
+    if (st != TCG_STATUS_SUCCESS)
+        return st;
+    st = operand_map(h, Bop, at, b_kmajor, p.n, p.k, ldb, sB, p.batch, kBN, a.k_per_block,
+                     a.mn_box, &bbc, &tmB);
+    if (st != TCG_STATUS_SUCCESS)
+        return st;
+    a.a_bcast = abc ? 1 : 0;
+    a.b_bcast = bbc ? 1 : 0;
+
+    const int grid = a.total_tiles < h->num_sms ? a.total_tiles : h->num_sms;
+    cudaError_t e = launch_gemm(tmA, tmB, a, ok, grid, h->stream);
+    h->launches += 1;
+    return e == cudaSuccess ? TCG_STATUS_SUCCESS : TCG_STATUS_EXECUTION_FAILED;
+}
+
+}  // namespace
+
+extern "C" {
+
+tcgStatus_t tcg_create(tcgHandle_t *h)
+{
+    if (!h)
+        return TCG_STATUS_INVALID_VALUE;
+    tcgContext *c = new (std::nothrow) tcgContext();
+    if (!c)
+        return TCG_STATUS_ALLOC_FAILED;
+    *h = c;
+    return TCG_STATUS_SUCCESS;
+}
+
+tcgStatus_t tcg_destroy(tcgHandle_t h)
+{
+    if (!h)
+        return TCG_STATUS_INVALID_VALUE;
+    if (h->used)
+        cudaStreamSynchronize(h->stream);
+    if (h->d_err)
+        cudaFree(h->d_err);
+    if (h->ws_own)
+        cudaFree(h->ws_own);
+    delete h;
+    return TCG_STATUS_SUCCESS;
+}
+
+tcgStatus_t tcg_set_stream(tcgHandle_t h, void *stream)
+{
+    if (!h)
+        return TCG_STATUS_INVALID_VALUE;
+    h->stream = static_cast<cudaStream_t>(stream);
+    return TCG_STATUS_SUCCESS;
+}
+
+tcgStatus_t tcg_set_workspace(tcgHandle_t h, void *ptr, size_t bytes)
+{
+    if (!h || (bytes > 0 && !ptr) || (reinterpret_cast<uintptr_t>(ptr) & 255u))
+        return TCG_STATUS_INVALID_VALUE;
+    h->ws_user = bytes ? ptr : nullptr;
+    h->ws_user_bytes = bytes;
+    return TCG_STATUS_SUCCESS;
+}
+
+tcgStatus_t tcg_gemm_workspace_size(tcgOp_t transa, tcgOp_t transb, int64_t m, int64_t n,
+                                    int64_t k, tcgDataType_t Atype, tcgComputeType_t compute,
+                                    int64_t batch_count, size_t *bytes)
+{
+    (void)transa;
+    (void)transb;
+    if (!bytes || m < 0 || n < 0 || k < 0 || batch_count < 0 || !valid_type(Atype))
+        return TCG_STATUS_INVALID_VALUE;
+    *bytes = (compute == TCG_COMPUTE_32F_FAST_TF32 && Atype == TCG_R_32F && k > 0)
+                 ? tf32_ws_bytes(m, n, k, batch_count)
+                 : 0;
+    return TCG_STATUS_SUCCESS;
+}
+
+tcgStatus_t tcg_gemm_ex(tcgHandle_t h, tcgOp_t transa, tcgOp_t transb, int64_t m, int64_t n,
+                        int64_t k, float alpha, const void *A, tcgDataType_t Atype,
+                        int64_t lda, const void *B, tcgDataType_t Btype, int64_t ldb,
+                        float beta, void *C, tcgDataType_t Ctype, int64_t ldc,
+                        tcgComputeType_t compute)
+{
+    if (!h)
+        return TCG_STATUS_INVALID_VALUE;
+    Problem p{transa, transb, m, n, k, alpha, beta, A, Atype, lda, 0, B, Btype, ldb, 0,
+              C, Ctype, ldc, 0, 1, compute, false};
+    return run(h, p);
+}
+
+tcgStatus_t tcg_gemm_strided_batched(tcgHandle_t h, tcgOp_t transa, tcgOp_t transb,
+                                     int64_t m, int64_t n, int64_t k, float alpha,
+                                     const void *A, tcgDataType_t Atype, int64_t lda,
+                                     int64_t strideA, const void *B, tcgDataType_t Btype,
+                                     int64_t ldb, int64_t strideB, float beta, void *C,
+                                     tcgDataType_t Ctype, int64_t ldc, int64_t strideC,
+                                     int64_t batch_count, tcgComputeType_t compute)
+{
+    if (!h)
+        return TCG_STATUS_INVALID_VALUE;
+    Problem p{transa, transb, m, n, k, alpha, beta, A, Atype, lda, strideA, B, Btype, ldb,
+              strideB, C, Ctype, ldc, strideC, batch_count, compute, true};
+    return run(h, p);
+}
+
+tcgStatus_t tcg_get_device_error(tcgHandle_t h)
+{
+    if (!h)
+        return TCG_STATUS_INVALID_VALUE;
+    if (!h->d_err)
+        return TCG_STATUS_SUCCESS;
+    uint32_t bits = 0;
+    if (cudaStreamSynchronize(h->stream) != cudaSuccess ||
+        cudaMemcpy(&bits, h->d_err, sizeof bits, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(h->d_err, 0, sizeof(uint32_t)) != cudaSuccess) {
+        cudaGetLastError();
+        return TCG_STATUS_EXECUTION_FAILED;
+    }
+    h->last_err_bits = bits;
+    return bits ? TCG_STATUS_TIMEOUT : TCG_STATUS_SUCCESS;
+}
+
+uint32_t tcg_last_device_error_bits(tcgHandle_t h) { return h ? h->last_err_bits : 0u; }
+
+const char *tcg_status_string(tcgStatus_t s)
+{
+    switch (s) {
+    case TCG_STATUS_SUCCESS: return "TCG_STATUS_SUCCESS";
+    case TCG_STATUS_NOT_INITIALIZED: return "TCG_STATUS_NOT_INITIALIZED";
+    case TCG_STATUS_INVALID_VALUE: return "TCG_STATUS_INVALID_VALUE";
+    case TCG_STATUS_NOT_SUPPORTED: return "TCG_STATUS_NOT_SUPPORTED";
+    case TCG_STATUS_ARCH_MISMATCH: return "TCG_STATUS_ARCH_MISMATCH";
+    case TCG_STATUS_EXECUTION_FAILED: return "TCG_STATUS_EXECUTION_FAILED";
+    case TCG_STATUS_TIMEOUT: return "TCG_STATUS_TIMEOUT";
+    case TCG_STATUS_ALLOC_FAILED: return "TCG_STATUS_ALLOC_FAILED";
+    }
+    return "TCG_STATUS_UNKNOWN";
+}
+
+tcgStatus_t tcg_set_debug(tcgHandle_t h, uint64_t wait_limit_ns, int fault_inject)
+{
+    if (!h)
+        return TCG_STATUS_INVALID_VALUE;
+    h->wait_limit_ns = wait_limit_ns ? wait_limit_ns : kDefaultWaitNs;
+    h->fault_inject = fault_inject ? 1 : 0;
+    return TCG_STATUS_SUCCESS;
+}
+
+uint64_t tcg_launch_count(tcgHandle_t h) { return h ? h->launches : 0; }
+
+}  // extern "C"

@@ -1,0 +1,151 @@
+"""C-ABI tests that need no GPU: the library loads, exports every symbol that
+include/tcg.h declares, and rejects bad arguments before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mixed_precision_tensor_gb300 as tcg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mixed_precision_tensor_gb300 import _build
+    _build.build()
+    return tcg.load_library()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "tcg.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(tcg_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_abi():
+    names = declared_symbols()
+    for required in ("tcg_create", "tcg_destroy", "tcg_set_stream", "tcg_gemm_ex",
+                     "tcg_gemm_strided_batched", "tcg_get_device_error", "tcg_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    assert set(declared_symbols()) <= set(tcg.EXPORTS)
+
+
+def test_status_strings(lib):
+    assert tcg.tcg_status_string(0) == "TCG_STATUS_SUCCESS"
+    assert tcg.tcg_status_string(6) == "TCG_STATUS_TIMEOUT"
+    assert tcg.tcg_status_string(99) == "TCG_STATUS_UNKNOWN"
+
+
+@pytest.fixture
+def handle(lib):
+    h = tcg.tcg_create()
+    yield h
+    assert tcg.tcg_destroy(h) == tcg.TCG_STATUS_SUCCESS
+
+
+# Fake, 16-byte aligned "device" addresses: the checks must reject the call before
+# anything dereferences them.
+PA, PB, PC = 0x10000, 0x20000, 0x30000
+F16, BF16, F32 = tcg.TCG_R_16F, tcg.TCG_R_16BF, tcg.TCG_R_32F
+N, T = tcg.TCG_OP_N, tcg.TCG_OP_T
+C32, TF32 = tcg.TCG_COMPUTE_32F, tcg.TCG_COMPUTE_32F_FAST_TF32
+INV, NSUP = tcg.TCG_STATUS_INVALID_VALUE, tcg.TCG_STATUS_NOT_SUPPORTED
+
+
+def gemm(h, transa=N, transb=N, m=64, n=64, k=64, alpha=1.0, A=PA, at=F16, lda=64, B=PB,
+         bt=F16, ldb=64, beta=0.0, C=PC, ct=F32, ldc=64, comp=C32):
+    return tcg.tcg_gemm_ex(h, transa, transb, m, n, k, alpha, A, at, lda, B, bt, ldb, beta, C,
+                           ct, ldc, comp)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(m=-1), INV), (dict(n=-1), INV), (dict(k=-1), INV),
+    (dict(transa=2), INV), (dict(transb=-1), INV),
+    (dict(at=7), INV), (dict(ct=9), INV), (dict(comp=5), INV),
+    (dict(lda=63), INV),                      # lda < m for OP_N
+    (dict(transa=T, m=128, k=64, lda=56, ldc=128), INV),  # OP_T: lda < k
+    (dict(transb=T, n=128, ldb=64), INV),                 # OP_T: ldb < n
+    (dict(ldb=60), INV),                      # ldb < k
+    (dict(ldc=32), INV),                      # ldc < m
+    (dict(m=60, lda=68, ldc=68), INV),        # 68*2 bytes = 136, not a multiple of 16
+    (dict(ldc=66), INV),                      # 66*4 bytes: multiple of 8 only
+    (dict(A=PA + 8), INV),                    # misaligned pointer
+    (dict(B=PB + 2), INV),
+    (dict(C=PC + 4), INV),
+    (dict(A=None), INV), (dict(B=None), INV), (dict(C=None), INV),
+    (dict(at=F16, bt=BF16), NSUP),            # mixed input types
+    (dict(at=F32, bt=F32, comp=C32), NSUP),   # FP32 inputs need the TF32 compute type
+    (dict(at=F32, bt=F32, comp=TF32, ct=F16, ldc=64), NSUP),
+    (dict(at=F16, bt=F16, comp=TF32), NSUP),
+    (dict(at=F16, bt=F16, ct=BF16), NSUP),    # 16-bit output must match the input type
+])
+def test_argument_checks(handle, kw, status):
+    assert gemm(handle, **kw) == status
+
+
+def test_null_handle_is_invalid(lib):
+    assert tcg.tcg_gemm_ex(None, N, N, 1, 1, 1, 1.0, PA, F16, 8, PB, F16, 8, 0.0, PC, F32, 4,
+                           C32) == INV
+    assert tcg.tcg_get_device_error(None) == INV
+    assert tcg.tcg_set_stream(None, None) == INV
+    assert tcg.tcg_destroy(None) == INV
+    assert lib.tcg_create(None) == INV
+
+
+def test_empty_problems_are_noops_without_cuda(handle):
+    # m == 0 / n == 0 / batch == 0 succeed before any device work (no GPU here)
+    assert gemm(handle, m=0, lda=8, ldc=4) == tcg.TCG_STATUS_SUCCESS
+    assert gemm(handle, n=0) == tcg.TCG_STATUS_SUCCESS
+    s = tcg.tcg_gemm_strided_batched(handle, N, N, 64, 64, 64, 1.0, PA, F16, 64, 4096, PB, F16,
+                                     64, 4096, 0.0, PC, F32, 64, 4096, 0, C32)
+    assert s == tcg.TCG_STATUS_SUCCESS
+    # k == 0 / alpha == 0: A and B are not read, so NULL is fine there
+    assert gemm(handle, m=0, k=0, A=None, B=None, lda=8, ldc=4) == tcg.TCG_STATUS_SUCCESS
+
+
+def test_batched_stride_checks(handle):
+    def b(**kw):
+        args = dict(sA=4096, sB=4096, sC=4096, batch=4)
+        args.update(kw)
+        return tcg.tcg_gemm_strided_batched(handle, N, N, 64, 64, 64, 1.0, PA, F16, 64,
+                                            args["sA"], PB, F16, 64, args["sB"], 0.0, PC, F32,
+                                            64, args["sC"], args["batch"], C32)
+    assert b(sA=-8) == INV
+    assert b(sA=4100) == INV                   # 4100*2 bytes not a multiple of 16
+    assert b(sC=4098) == INV                   # 4098*4 bytes not a multiple of 16
+    assert b(sC=0) == INV                      # outputs would alias
+    assert b(batch=-1) == INV
+
+
+def test_workspace_size_query(lib):
+    assert tcg.tcg_gemm_workspace_size(N, N, 64, 64, 64, F16, C32) == 0
+    ws = tcg.tcg_gemm_workspace_size(N, N, 100, 50, 30, F32, TF32)
+    kp = 32
+    assert ws >= (100 + 50) * kp * 4
+    assert tcg.tcg_set_workspace(tcg.tcg_create(), 0x1000 + 16, 1024) == INV   # not 256-aligned
+
+
+def test_debug_hook_and_launch_count(handle):
+    assert tcg.tcg_set_debug(handle, 1000, 1) == tcg.TCG_STATUS_SUCCESS
+    assert tcg.tcg_set_debug(handle, 0, 0) == tcg.TCG_STATUS_SUCCESS
+    assert tcg.tcg_launch_count(handle) == 0
+    # a handle that never launched reports no device error, with no CUDA call
+    assert tcg.tcg_get_device_error(handle) == tcg.TCG_STATUS_SUCCESS
+
+
+def test_product_path_has_no_oracle_dependency():
+    """The package and the CUDA sources never import or link the oracle."""
+    pkg = os.path.join(ROOT, "mixed_precision_tensor_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "tcg_oracle" not in text and "liboracle" not in text, f

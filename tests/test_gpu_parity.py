@@ -1,0 +1,364 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Bar (element by element): bit-exact (by value class) on integer-valued inputs
+whose sums stay exact in FP32; on random inputs
+    |D - ref| <= k*2^-23*(|alpha|*(|A||B|) + |beta|*|C|)  (+ one output ulp for 16-bit out)
+the error model of "NVIDIA Tensor Core混合精度计算原理与应用解析" section 2.3 with
+p = 23 (FP32 accumulation).  Small cases are checked in full; the 8192^3,
+16384x4096x4096 and 4096x4096x16384 workloads are checked on 64 seeded 128x128
+output tiles (corners always included), in the launch configuration the
+benchmark times.  Output buffers carry canary guard bands (before, after, and in
+the ldc padding) that must stay untouched.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mixed_precision_tensor_gb300 as tcg
+import oracle
+from helpers import TYPE_CODE, check_bound, decode_out, oracle_rowmajor, raw, values_equal
+from mixed_precision_tensor_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+N, T = tcg.TCG_OP_N, tcg.TCG_OP_T
+CODE = {"f16": tcg.TCG_R_16F, "bf16": tcg.TCG_R_16BF, "f32": tcg.TCG_R_32F}
+ESIZE = {"f16": 2, "bf16": 2, "f32": 4}
+
+
+@pytest.fixture(scope="module")
+def handle(cuda_device):
+    h = tcg.Handle()
+    yield h
+    h.close()
+
+
+def _to_storage(x64, t):
+    if t == "f16":
+        return x64.astype(np.float32).astype(np.float16).view(np.uint16)
+    if t == "bf16":
+        return torch.from_numpy(x64.astype(np.float32)).to(torch.bfloat16).view(
+            torch.int16).numpy().view(np.uint16)
+    return x64.astype(np.float32)
+
+
+def _t(a):
+    """numpy -> torch without uint16 (limited in torch): raw 16-bit data as int16."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a)
+
+
+def _decode(raw_arr, t):
+    if t == "f16":
+        return raw_arr.view(np.float16).astype(np.float64)
+    if t == "bf16":
+        return oracle.bf16_to_f64(raw_arr)
+    return raw_arr.astype(np.float64)
+
+
+def _draw_values(rng, shape, dist):
+    if dist == "integer":
+        return rng.integers(-2, 3, shape).astype(np.float64)
+    return rng.uniform(-1, 1, shape)
+
+
+def _roundup(x, a):
+    return max(a, (x + a - 1) // a * a)
+
+
+CANARY = {"f32": np.array([0x7FC0DEAD], dtype=np.uint32).view(np.float32)[0],
+          "f16": np.uint16(0x7E5A), "bf16": np.uint16(0x7FDA)}
+
+
+def run_colmajor(h, transa, transb, m, n, k, alpha, beta, in_t, out_t, seed, dist,
+                 extra_ld=0, batch=1):
+    """One column-major call through the C ABI on padded buffers with guard bands;
+    returns (got, ref, R, absAB, Cdecoded) as column-major (m, n) blocks per batch,
+    plus a flag saying whether the guard bands survived."""
+    rng = np.random.default_rng(seed)
+    ain = 16 // ESIZE[in_t]
+    aout = 16 // ESIZE[out_t]
+    a_rows, a_cols = (m, k) if transa == N else (k, m)
+    b_rows, b_cols = (k, n) if transb == N else (n, k)
+    lda = _roundup(a_rows, ain) + extra_ld * ain
+    ldb = _roundup(b_rows, ain) + extra_ld * ain
+    ldc = _roundup(m, aout) + extra_ld * aout
+    sA, sB, sC = lda * a_cols, ldb * b_cols, ldc * n
+    sA, sB, sC = _roundup(sA, ain), _roundup(sB, ain), _roundup(sC, aout)
+    Araw = _to_storage(_draw_values(rng, batch * sA, dist), in_t)
+    Braw = _to_storage(_draw_values(rng, batch * sB, dist), in_t)
+    if dist == "integer":
+        Cv = rng.integers(-8, 9, batch * sC).astype(np.float64)
+        if out_t != "f32":
+            Cv = Cv / 2.0
+    else:
+        Cv = rng.standard_normal(batch * sC)
+    Craw = _to_storage(Cv, out_t)
+    guard = 64
+    canary = CANARY[out_t]
+    Cbuf = np.full(batch * sC + 2 * guard, canary, dtype=Craw.dtype)
+    Cbuf[guard:guard + batch * sC] = Craw
+    # ldc padding rows hold canaries too (they must survive)
+    view = Cbuf[guard:guard + batch * sC].reshape(batch, sC)[:, : ldc * n].reshape(batch, n, ldc)
+    view[:, :, m:] = canary
+    Cin = Cbuf[guard:guard + batch * sC].copy()
+    dev = torch.device("cuda:0")
+    dA = _t(Araw).to(dev)
+    dB = _t(Braw).to(dev)
+    dC = _t(Cbuf).to(dev)
+    cptr = dC.data_ptr() + guard * Cbuf.itemsize
+    comp = tcg.TCG_COMPUTE_32F_FAST_TF32 if in_t == "f32" else tcg.TCG_COMPUTE_32F
+    if batch == 1:
+        s = tcg.tcg_gemm_ex(h.h, transa, transb, m, n, k, alpha, dA, CODE[in_t], lda, dB,
+                            CODE[in_t], ldb, beta, cptr, CODE[out_t], ldc, comp)
+    else:
+        s = tcg.tcg_gemm_strided_batched(h.h, transa, transb, m, n, k, alpha, dA, CODE[in_t],
+                                         lda, sA, dB, CODE[in_t], ldb, sB, beta, cptr,
+                                         CODE[out_t], ldc, sC, batch, comp)
+    tcg.check(s, "gemm")
+    tcg.check(tcg.tcg_get_device_error(h.h), "device error")
+    out = dC.cpu().numpy().view(Cbuf.dtype)
+    guards_ok = (np.array_equal(out[:guard].view(np.uint8), Cbuf[:guard].view(np.uint8)) and
+                 np.array_equal(out[-guard:].view(np.uint8), Cbuf[-guard:].view(np.uint8)))
+    body = out[guard:guard + batch * sC].reshape(batch, sC)
+    pad = body[:, : ldc * n].reshape(batch, n, ldc)[:, :, m:]
+    guards_ok = guards_ok and np.array_equal(pad.view(np.uint8),
+                                             np.full_like(pad, canary).view(np.uint8))
+    results = []
+    for b in range(batch):
+        D, R, AB = oracle.gemm(transa, transb, m, n, k, alpha, Araw[b * sA:(b + 1) * sA],
+                               TYPE_CODE[in_t], lda, Braw[b * sB:(b + 1) * sB], TYPE_CODE[in_t],
+                               ldb, beta, Cin[b * sC:(b + 1) * sC], TYPE_CODE[out_t], ldc,
+                               tf32=(in_t == "f32"))
+        got = body[b, : ldc * n].reshape(n, ldc)[:, :m].T
+        cdec = _decode(Cin[b * sC:(b + 1) * sC][: ldc * n].reshape(n, ldc)[:, :m].T, out_t)
+        results.append((got, D, R, AB, cdec))
+    return results, guards_ok
+
+
+def _assert_results(results, k, alpha, beta, out_t, exact):
+    for got, D, R, AB, cdec in results:
+        g = _decode(np.ascontiguousarray(got), out_t)
+        ref = _decode(np.ascontiguousarray(D), out_t)
+        if exact:
+            assert values_equal(g, ref), f"max |diff| {np.nanmax(np.abs(g - ref))}"
+        else:
+            ok, worst, idx = check_bound(g, ref, AB, cdec, k, alpha, beta, out_t)
+            assert ok, f"bound exceeded: worst normalised error {worst} at {np.unravel_index(idx, g.shape)}"
+
+
+RAGGED = [(1, 1, 1), (7, 17, 15), (129, 255, 257), (200, 127, 1000), (257, 513, 64),
+          (1000, 300, 129), (128, 256, 64), (33, 1, 300), (1, 260, 8)]
+
+
+@pytest.mark.parametrize("m,n,k", RAGGED)
+@pytest.mark.parametrize("in_t,out_t", [("f16", "f32"), ("f16", "f16"), ("bf16", "f32"),
+                                        ("bf16", "bf16"), ("f32", "f32")])
+def test_ragged_integer_bitexact(handle, m, n, k, in_t, out_t):
+    res, guards = run_colmajor(handle, N, N, m, n, k, 1.0, 1.0, in_t, out_t, seed=m * 7 + n + k,
+                               dist="integer")
+    assert guards, "guard band or ldc padding overwritten"
+    _assert_results(res, k, 1.0, 1.0, out_t, exact=True)
+
+
+@pytest.mark.parametrize("m,n,k", RAGGED)
+@pytest.mark.parametrize("in_t,out_t", [("f16", "f32"), ("f16", "f16"), ("bf16", "f32"),
+                                        ("f32", "f32")])
+def test_ragged_random_within_bound(handle, m, n, k, in_t, out_t):
+    res, guards = run_colmajor(handle, N, N, m, n, k, 0.75, -0.5, in_t, out_t,
+                               seed=1000 + m + n * 3 + k, dist="uniform", extra_ld=1)
+    assert guards
+    _assert_results(res, k, 0.75, -0.5, out_t, exact=False)
+
+
+@pytest.mark.parametrize("transa", [N, T])
+@pytest.mark.parametrize("transb", [N, T])
+@pytest.mark.parametrize("in_t", ["f16", "bf16", "f32"])
+def test_all_op_combinations(handle, transa, transb, in_t):
+    m, n, k = 300, 520, 200
+    res, guards = run_colmajor(handle, transa, transb, m, n, k, 1.0, 1.0, in_t, "f32",
+                               seed=5 + transa * 2 + transb, dist="integer", extra_ld=2)
+    assert guards
+    _assert_results(res, k, 1.0, 1.0, "f32", exact=True)
+    res, guards = run_colmajor(handle, transa, transb, m, n, k, 1.5, 0.25, in_t, "f32",
+                               seed=50 + transa * 2 + transb, dist="uniform")
+    assert guards
+    _assert_results(res, k, 1.5, 0.25, "f32", exact=False)
+
+
+@pytest.mark.parametrize("in_t,out_t", [("f16", "f16"), ("f16", "f32"), ("f32", "f32")])
+def test_strided_batched_ragged(handle, in_t, out_t):
+    res, guards = run_colmajor(handle, N, T, 100, 72, 40, 1.0, 0.5, in_t, out_t, seed=77,
+                               dist="integer", batch=5)
+    assert guards
+    _assert_results(res, 40, 1.0, 0.5, out_t, exact=True)
+
+
+def test_degenerate_cases(handle):
+    # k == 0 and alpha == 0: D = beta*C, A/B not read (NULL)
+    for k, alpha in ((0, 1.0), (64, 0.0)):
+        m, n = 70, 40
+        C = torch.randn(n, 72, device="cuda")        # column-major m x n, ldc = 72
+        want = (-1.5 * C.double()).float()
+        s = tcg.tcg_gemm_ex(handle.h, N, N, m, n, k, alpha, None, tcg.TCG_R_16F, 72, None,
+                            tcg.TCG_R_16F, 64, -1.5, C, tcg.TCG_R_32F, 72, tcg.TCG_COMPUTE_32F)
+        tcg.check(s)
+        torch.cuda.synchronize()
+        assert torch.equal(C[:, :m], want[:, :m])
+    # beta == 0: NaN in C does not propagate
+    A = torch.ones(64, 64, dtype=torch.float16, device="cuda")
+    B = torch.ones(64, 64, dtype=torch.float16, device="cuda")
+    C = torch.full((64, 64), float("nan"), device="cuda")
+    tcg.gemm_rowmajor(handle, A, B, C, alpha=1.0, beta=0.0)
+    torch.cuda.synchronize()
+    assert torch.all(C == 64.0)
+
+
+def test_page_vectors_on_gpu(handle):
+    """The accumulation vector of section 2.2.1 and the subnormal vector of section
+    2.2.3 ("NVIDIA Tensor Core混合精度计算原理与应用解析"), padded to 16x16x16.  The
+    oracle value is pinned on CPU; the hardware value is recorded and must lie
+    within the bound (either truncating or rounding accumulation is acceptable)."""
+    A = torch.zeros(16, 16, dtype=torch.float16)
+    B = torch.zeros(16, 16, dtype=torch.float16)
+    A[0, :3] = torch.tensor([1.5, 2.0 ** -23, 2.0 ** -24], dtype=torch.float16)
+    B[:3, 0] = torch.tensor([1.5, 1.0, 1.0], dtype=torch.float16)
+    C = torch.zeros(16, 16, device="cuda")
+    tcg.gemm_rowmajor(handle, A.cuda(), B.cuda(), C)
+    torch.cuda.synchronize()
+    v = float(C[0, 0])
+    assert v in (2.25, 2.25 + 2.0 ** -22, 2.25 + 2.0 ** -23)
+    print(f"accumulation vector: GPU {v!r} (oracle 2.25 + 2^-22 = {2.25 + 2.0 ** -22!r})")
+    A = torch.zeros(16, 16, dtype=torch.bfloat16)
+    B = torch.zeros(16, 16, dtype=torch.bfloat16)
+    A[0, :2] = torch.tensor([127 * 2.0 ** -78, 2.0 ** -78], dtype=torch.float64).to(torch.bfloat16)
+    B[:2, 0] = torch.tensor([2.0 ** -78, 2.0 ** -79], dtype=torch.float64).to(torch.bfloat16)
+    C = torch.zeros(16, 16, device="cuda")
+    tcg.gemm_rowmajor(handle, A.cuda(), B.cuda(), C)
+    torch.cuda.synchronize()
+    v = float(C[0, 0])
+    print(f"subnormal vector: GPU {v!r} (oracle 2^-149 = {2.0 ** -149!r})")
+    assert 0.0 <= v <= 2.0 ** -148
+
+
+# ------------------------------------------------------------ the five workloads
+def _device_inputs(w, A, B, C):
+    dev = torch.device("cuda:0")
+    dA = _t(A if w.batch > 1 else A[0]).to(dev)
+    dB = _t(B if w.batch > 1 else B[0]).to(dev)
+    if w.in_type == "bf16":
+        dA, dB = dA.view(torch.bfloat16), dB.view(torch.bfloat16)
+    shape = (w.batch, w.m, w.n) if w.batch > 1 else (w.m, w.n)
+    odt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.out_type]
+    if C is not None:
+        dC = _t(C if w.batch > 1 else C[0]).to(dev)
+        if w.out_type == "bf16":
+            dC = dC.view(torch.bfloat16)
+    else:
+        dC = torch.empty(shape, dtype=odt, device=dev)
+    return dA, dB, dC
+
+
+def _run_workload(handle, w, A, B, C):
+    dA, dB, dC = _device_inputs(w, A, B, C)
+    tcg.gemm_rowmajor(handle, dA, dB, dC, alpha=w.alpha, beta=w.beta, tf32=w.in_type == "f32")
+    tcg.check(tcg.tcg_get_device_error(handle.h), "device error")
+    out = dC.cpu()
+    if w.out_type == "bf16":
+        out = out.view(torch.int16).numpy().view(np.uint16)
+    else:
+        out = out.numpy()
+    return out if w.batch > 1 else out[None]
+
+
+def _check_full(w, A, B, C, out, exact):
+    for b in range(w.batch):
+        D, R, AB = oracle_rowmajor(w, A, B, C, b=b)
+        g = decode_out(raw(out[b]), w.out_type)
+        ref = decode_out(raw(D), w.out_type)
+        cdec = decode_out(raw(C[b]), w.out_type) if C is not None else None
+        if exact:
+            assert values_equal(g, ref), f"batch {b}: not bit-exact"
+        else:
+            ok, worst, idx = check_bound(g, ref, AB, cdec, w.k, w.alpha, w.beta, w.out_type)
+            assert ok, f"batch {b}: worst normalised error {worst}"
+
+
+def _check_sampled(w, A, B, C, out, exact, count=64):
+    tiles = wl.sample_tiles(w.m, w.n, count=count, tile=128, seed=w.seed)
+    assert len(tiles) == min(count, (-(-w.m // 128)) * (-(-w.n // 128)))
+    worst_all = 0.0
+    for (i0, i1, j0, j1) in tiles:
+        D, R, AB = oracle_rowmajor(w, A, B, C, rows=(i0, i1), cols=(j0, j1))
+        g = decode_out(raw(np.ascontiguousarray(out[0][i0:i1, j0:j1])), w.out_type)
+        ref = decode_out(raw(D), w.out_type)
+        cdec = (decode_out(raw(np.ascontiguousarray(C[0][i0:i1, j0:j1])), w.out_type)
+                if C is not None else None)
+        if exact:
+            assert values_equal(g, ref), f"tile {(i0, j0)} not bit-exact"
+        else:
+            ok, worst, idx = check_bound(g, ref, AB, cdec, w.k, w.alpha, w.beta, w.out_type)
+            assert ok, f"tile {(i0, j0)}: worst normalised error {worst}"
+            worst_all = max(worst_all, worst)
+    return worst_all
+
+
+SMALL = ["fp16_gemm_256", "fp16_batched_512x256"]
+LARGE = ["fp16_gemm_8192", "bf16_proj_16384x4096x4096", "tf32_gemm_4096x4096x16384"]
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_small_workload_full_random(handle, name):
+    w = wl.WORKLOADS[name]
+    A, B, C = wl.draw(w)
+    out = _run_workload(handle, w, A, B, C)
+    _check_full(w, A, B, C, out, exact=False)
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_small_workload_full_integer(handle, name):
+    w = wl.with_dist(wl.WORKLOADS[name], "integer")
+    A, B, C = wl.draw(w)
+    out = _run_workload(handle, w, A, B, C)
+    _check_full(w, A, B, C, out, exact=True)
+
+
+@pytest.mark.timeout(900)
+@pytest.mark.parametrize("name", LARGE)
+def test_large_workload_sampled_random(handle, name):
+    w = wl.WORKLOADS[name]
+    A, B, C = wl.draw(w)
+    out = _run_workload(handle, w, A, B, C)
+    worst = _check_sampled(w, A, B, C, out, exact=False)
+    print(f"{name}: worst normalised error over 64 tiles = {worst:.3e}")
+
+
+@pytest.mark.timeout(900)
+@pytest.mark.parametrize("name", LARGE)
+def test_large_workload_sampled_integer(handle, name):
+    w = wl.with_dist(wl.WORKLOADS[name], "integer")
+    A, B, C = wl.draw(w)
+    out = _run_workload(handle, w, A, B, C)
+    _check_sampled(w, A, B, C, out, exact=True, count=16)
+
+
+def test_timeout_is_reported_not_hung(handle):
+    """A bounded wait that runs out (a stage nobody fills) ends the kernel with a
+    TIMEOUT status in the error word; the context stays usable afterwards."""
+    h = tcg.Handle()
+    A = torch.ones(256, 256, dtype=torch.float16, device="cuda")
+    B = torch.ones(256, 256, dtype=torch.float16, device="cuda")
+    C = torch.zeros(256, 256, device="cuda")
+    tcg.check(tcg.tcg_set_debug(h.h, 200_000_000, 1))          # 0.2 s, skip one load
+    tcg.gemm_rowmajor(h, A, B, C)
+    st = tcg.tcg_get_device_error(h.h)
+    assert st == tcg.TCG_STATUS_TIMEOUT
+    assert tcg.tcg_last_device_error_bits(h.h) != 0
+    tcg.check(tcg.tcg_set_debug(h.h, 0, 0))
+    tcg.gemm_rowmajor(h, A, B, C)
+    assert tcg.tcg_get_device_error(h.h) == tcg.TCG_STATUS_SUCCESS
+    torch.cuda.synchronize()
+    assert torch.all(C == 256.0)
+    h.close()
