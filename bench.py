@@ -204,9 +204,9 @@ def time_oracle(w, A, B, C, blocks, nthreads):
 def cpu_baseline(w, A, B, C, budget_s=12.0):
     """The oracle timed on this host's cores on a bounded sample of the workload."""
     nthreads = os.cpu_count() or 1
-    blk = oracle_blocks(w, A, B, 128, 1, seed=w.seed)
+    blk = oracle_blocks(w, A, B, 128, 4, seed=w.seed)
     dt1, fl1 = time_oracle(w, A, B, C, blk, nthreads)
-    count = max(1, min(256, int(budget_s / max(dt1, 1e-6))))
+    count = max(4, min(1024, int(budget_s / max(dt1 / len(blk), 1e-6))))
     blocks = oracle_blocks(w, A, B, 128, count, seed=w.seed)
     dt, fl = time_oracle(w, A, B, C, blocks, nthreads)
     return {"value": fl / dt / 1e12, "unit": UNIT, "cores": nthreads, "kind": "oracle",
@@ -290,7 +290,7 @@ def run_ours(args, w):
     tf32 = w.in_type == "f32"
     in_bytes = A.nbytes + B.nbytes + (C.nbytes if C is not None else 0)
     flush = None
-    if in_bytes < 2 * L2_BYTES:
+    if in_bytes <= L2_BYTES:
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
 
     def step():
@@ -390,6 +390,7 @@ def run_ours(args, w):
                    "alpha": w.alpha, "beta": w.beta, "seed": w.seed,
                    "l2": ("inputs larger than L2" if flush is None else
                           "L2 flushed between steps (write of a 258 MiB buffer)"),
+                   "input_bytes": in_bytes,
                    "parallelism": f"replicas x{world}"},
         "pct_of_peak": 100.0 * value / world / (peak if bound == "tensor" else float(
             peaks["bf16_tflops"])),

@@ -179,6 +179,14 @@ const char *tcg_status_string(tcgStatus_t s);
  * trap); 0 turns it off.  INVALID_VALUE: NULL h. */
 tcgStatus_t tcg_set_debug(tcgHandle_t h, uint64_t wait_limit_ns, int fault_inject);
 
+/* Kernel options (0 = default for each).  cta_group: 2 (default) runs each 256x256
+ * output tile on a pair of SMs (tcgen05 cta_group::2, B split between the pair's
+ * shared memories); 1 runs 128x256 tiles on single SMs.  group_m: how many tile rows
+ * the persistent scheduler walks together before moving along N (L2 reuse; default
+ * 8).  Both variants meet the same accuracy bound.  INVALID_VALUE: NULL h,
+ * cta_group outside 0..2, group_m outside 0..1024. */
+tcgStatus_t tcg_set_kernel_options(tcgHandle_t h, int cta_group, int group_m);
+
 /* Number of GEMM-path kernel launches this handle has made (for the
  * benchmark's launch count).  Returns 0 for NULL. */
 uint64_t tcg_launch_count(tcgHandle_t h);

@@ -38,7 +38,7 @@ TCG_COMPUTE_32F, TCG_COMPUTE_32F_FAST_TF32 = 0, 1
 EXPORTS = ("tcg_create", "tcg_destroy", "tcg_set_stream", "tcg_set_workspace",
            "tcg_gemm_workspace_size", "tcg_gemm_ex", "tcg_gemm_strided_batched",
            "tcg_get_device_error", "tcg_last_device_error_bits", "tcg_status_string",
-           "tcg_set_debug", "tcg_launch_count")
+           "tcg_set_debug", "tcg_launch_count", "tcg_set_kernel_options")
 
 _lock = threading.Lock()
 _lib = None
@@ -92,6 +92,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.tcg_set_debug.argtypes = [vp, ctypes.c_uint64, ci]
         lib.tcg_launch_count.restype = ctypes.c_uint64
         lib.tcg_launch_count.argtypes = [vp]
+        lib.tcg_set_kernel_options.restype = st
+        lib.tcg_set_kernel_options.argtypes = [vp, ci, ci]
         _lib = lib
         return lib
 
@@ -169,6 +171,10 @@ def tcg_set_debug(h: int, wait_limit_ns: int = 0, fault_inject: int = 0) -> int:
 
 def tcg_launch_count(h: int) -> int:
     return load_library().tcg_launch_count(h)
+
+
+def tcg_set_kernel_options(h: int, cta_group: int = 0, group_m: int = 0) -> int:
+    return load_library().tcg_set_kernel_options(h, cta_group, group_m)
 
 
 # ------------------------------------------------------------ conveniences

@@ -33,9 +33,10 @@ constexpr int kMapCacheSize = 32;
 struct MapKey {
     const void *ptr;
     int dtype;
-    uint64_t dims[3];
-    uint64_t strides[2];
-    uint32_t box[3];
+    int rank;
+    uint64_t dims[5];
+    uint64_t strides[4];
+    uint32_t box[5];
     bool operator==(const MapKey &o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
 };
 
@@ -60,6 +61,9 @@ struct tcgContext {
     int fault_inject = 0;
     uint64_t launches = 0;
     uint32_t last_err_bits = 0;
+    int cta_group = 2;
+    int group_m = 0;           // 0: choose per problem
+    int max_ctas[3] = {0, 0, 0};
     bool used = false;
     EncodeTiledFn encode = nullptr;
     MapEntry cache[kMapCacheSize];
@@ -198,18 +202,23 @@ CUtensorMapDataType map_type(tcgDataType_t t)
     }
 }
 
-// Rank-3 tiled map {inner, outer, batch} with 128-byte swizzle, zero fill out of range.
-tcgStatus_t get_map(tcgContext *h, const void *ptr, tcgDataType_t t, uint64_t inner,
-                    uint64_t outer, uint64_t batch, uint64_t ld_bytes, uint64_t bstride_bytes,
-                    uint32_t box_inner, uint32_t box_outer, CUtensorMap *out)
+// Tiled map of rank 3 or 5 with 128-byte swizzle and zero fill out of range, cached
+// per (pointer, type, dims, strides, box).
+tcgStatus_t get_map(tcgContext *h, const void *ptr, tcgDataType_t t, int rank,
+                    const uint64_t *dims, const uint64_t *strides, const uint32_t *box,
+                    CUtensorMap *out)
 {
     MapKey key;
     std::memset(&key, 0, sizeof key);
     key.ptr = ptr;
     key.dtype = static_cast<int>(t);
-    key.dims[0] = inner; key.dims[1] = outer; key.dims[2] = batch;
-    key.strides[0] = ld_bytes; key.strides[1] = bstride_bytes;
-    key.box[0] = box_inner; key.box[1] = box_outer; key.box[2] = 1;
+    key.rank = rank;
+    for (int i = 0; i < rank; ++i) {
+        key.dims[i] = dims[i];
+        key.box[i] = box[i];
+        if (i < rank - 1)
+            key.strides[i] = strides[i];
+    }
     for (int i = 0; i < kMapCacheSize; ++i) {
         if (h->cache[i].valid && h->cache[i].key == key) {
             *out = h->cache[i].map;
@@ -217,11 +226,11 @@ tcgStatus_t get_map(tcgContext *h, const void *ptr, tcgDataType_t t, uint64_t in
         }
     }
     alignas(64) CUtensorMap map;
-    const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = h->encode(&map, map_type(t), 3, const_cast<void *>(ptr), key.dims, key.strides,
-                           key.box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = h->encode(&map, map_type(t), static_cast<cuuint32_t>(rank),
+                           const_cast<void *>(ptr), key.dims, key.strides, key.box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return TCG_STATUS_EXECUTION_FAILED;
     MapEntry &e = h->cache[h->cache_next];
@@ -233,27 +242,49 @@ tcgStatus_t get_map(tcgContext *h, const void *ptr, tcgDataType_t t, uint64_t in
     return TCG_STATUS_SUCCESS;
 }
 
-// Map for one operand as the kernel loads it.  rows = M (for A) or N (for B); box_rows
-// = 128 (A) or 256 (B).  K-major: {K, rows, batch}, box {k_per_block, box_rows}.
-// M/N-major: {rows, K, batch}, box {mn_box, k_per_block}.
+// Map for one operand as the kernel loads it (see OperandMode).  rows = M (for A) or
+// N (for B); box_rows = the rows one CTA loads per stage (128 for A; 256 or 128 for B).
 tcgStatus_t operand_map(tcgContext *h, const void *ptr, tcgDataType_t t, bool kmajor,
                         int64_t rows, int64_t k, int64_t ld, int64_t stride, int64_t batch,
-                        int box_rows, int k_per_block, int mn_box, bool *bcast, CUtensorMap *out)
+                        int box_rows, int k_per_block, int mn_box, bool *bcast, int *mode,
+                        CUtensorMap *out)
 {
     const int es = elem_size(t);
     const bool bc = (batch > 1 && stride == 0);
     *bcast = bc;
     const uint64_t nb = bc ? 1 : static_cast<uint64_t>(batch);
     const uint64_t ldb = static_cast<uint64_t>(ld) * es;
-    const uint64_t inner = kmajor ? k : rows, outer = kmajor ? rows : k;
+    const uint64_t outer = kmajor ? rows : k;
     uint64_t bstride = static_cast<uint64_t>(stride) * es;
     if (nb == 1)
         bstride = ldb * outer;                  // unused; any legal value
     if (bstride == 0)
         bstride = 16;
-    if (kmajor)
-        return get_map(h, ptr, t, inner, outer, nb, ldb, bstride, k_per_block, box_rows, out);
-    return get_map(h, ptr, t, inner, outer, nb, ldb, bstride, mn_box, k_per_block, out);
+    if (kmajor) {
+        *mode = kK;
+        const uint64_t dims[3] = {static_cast<uint64_t>(k), static_cast<uint64_t>(rows), nb};
+        const uint64_t str[2] = {ldb, bstride};
+        const uint32_t box[3] = {static_cast<uint32_t>(k_per_block),
+                                 static_cast<uint32_t>(box_rows), 1};
+        return get_map(h, ptr, t, 3, dims, str, box, out);
+    }
+    if (es == 2 && rows % 64 == 0 && k % 8 == 0) {
+        // Element (r, p) = (64*c2 + c0, 8*c3 + c1): every coordinate TMA accepts maps
+        // inside the matrix, so zero fill covers exactly the ragged K tail.
+        *mode = kMNInter;
+        const uint64_t dims[5] = {64, 8, static_cast<uint64_t>(rows / 64),
+                                  static_cast<uint64_t>(k / 8), nb};
+        const uint64_t str[4] = {ldb, 64ull * es, 8ull * ldb, bstride};
+        const uint32_t box[5] = {64, 8, static_cast<uint32_t>(box_rows / 64),
+                                 static_cast<uint32_t>(k_per_block / 8), 1};
+        return get_map(h, ptr, t, 5, dims, str, box, out);
+    }
+    *mode = kMNChunk;
+    const uint64_t dims[3] = {static_cast<uint64_t>(rows), static_cast<uint64_t>(k), nb};
+    const uint64_t str[2] = {ldb, bstride};
+    const uint32_t box[3] = {static_cast<uint32_t>(mn_box), static_cast<uint32_t>(k_per_block),
+                             1};
+    return get_map(h, ptr, t, 3, dims, str, box, out);
 }
 
 int out_kind(tcgDataType_t c)
@@ -349,17 +380,16 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
         sB = p.n * kp;
     }
 
+    const int cg = h->cta_group;
     GemmArgs a;
     std::memset(&a, 0, sizeof a);
     a.m = m; a.n = n; a.k = k; a.batch = batch;
-    a.num_m_tiles = (m + kBM - 1) / kBM;
+    a.num_m_tiles = (m + kBM * cg - 1) / (kBM * cg);
     a.num_n_tiles = (n + kBN - 1) / kBN;
     a.k_per_block = tf32 ? 32 : 64;
     a.num_k_blocks = (k + a.k_per_block - 1) / a.k_per_block;
     a.total_tiles = a.num_m_tiles * a.num_n_tiles * batch;
-    a.group_m = 16;
-    a.a_kmajor = a_kmajor ? 1 : 0;
-    a.b_kmajor = b_kmajor ? 1 : 0;
+    a.group_m = h->group_m > 0 ? h->group_m : 8;
     a.is_tf32 = tf32 ? 1 : 0;
     a.mn_box = tf32 ? 32 : 64;
     const uint32_t fmt = tf32 ? 2u : (p.Atype == TCG_R_16BF ? 1u : 0u);
@@ -368,7 +398,7 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
               | ((a_kmajor ? 0u : 1u) << 15)          // A: 0 = K-major, 1 = M-major
               | ((b_kmajor ? 0u : 1u) << 16)          // B: 0 = K-major, 1 = N-major
               | (static_cast<uint32_t>(kBN >> 3) << 17)
-              | (static_cast<uint32_t>(kBM >> 4) << 24);
+              | (static_cast<uint32_t>((kBM * cg) >> 4) << 24);   // M = 128 or 256
     a.alpha = p.alpha;
     a.beta = p.beta;
     a.C = p.C;
@@ -383,18 +413,21 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
     CUtensorMap tmA, tmB;
     bool abc = false, bbc = false;
     st = operand_map(h, Aop, at, a_kmajor, p.m, p.k, lda, sA, p.batch, kBM, a.k_per_block,
-                     a.mn_box, &abc, &tmA);
+                     a.mn_box, &abc, &a.a_mode, &tmA);
     if (st != TCG_STATUS_SUCCESS)
         return st;
-    st = operand_map(h, Bop, at, b_kmajor, p.n, p.k, ldb, sB, p.batch, kBN, a.k_per_block,
-                     a.mn_box, &bbc, &tmB);
+    st = operand_map(h, Bop, at, b_kmajor, p.n, p.k, ldb, sB, p.batch, kBN / cg, a.k_per_block,
+                     a.mn_box, &bbc, &a.b_mode, &tmB);
     if (st != TCG_STATUS_SUCCESS)
         return st;
     a.a_bcast = abc ? 1 : 0;
     a.b_bcast = bbc ? 1 : 0;
 
-    const int grid = a.total_tiles < h->num_sms ? a.total_tiles : h->num_sms;
-    cudaError_t e = launch_gemm(tmA, tmB, a, ok, grid, h->stream);
+    if (h->max_ctas[cg] == 0)
+        h->max_ctas[cg] = gemm_max_resident_ctas(cg, h->num_sms);
+    const int64_t want = static_cast<int64_t>(a.total_tiles) * cg;
+    const int grid = static_cast<int>(want < h->max_ctas[cg] ? want : h->max_ctas[cg]);
+    cudaError_t e = launch_gemm(tmA, tmB, a, ok, cg, grid, h->stream);
     h->launches += 1;
     return e == cudaSuccess ? TCG_STATUS_SUCCESS : TCG_STATUS_EXECUTION_FAILED;
 }
@@ -531,5 +564,14 @@ tcgStatus_t tcg_set_debug(tcgHandle_t h, uint64_t wait_limit_ns, int fault_injec
 }
 
 uint64_t tcg_launch_count(tcgHandle_t h) { return h ? h->launches : 0; }
+
+tcgStatus_t tcg_set_kernel_options(tcgHandle_t h, int cta_group, int group_m)
+{
+    if (!h || cta_group < 0 || cta_group > 2 || group_m < 0 || group_m > 1024)
+        return TCG_STATUS_INVALID_VALUE;
+    h->cta_group = cta_group ? cta_group : 2;
+    h->group_m = group_m;
+    return TCG_STATUS_SUCCESS;
+}
 
 }  // extern "C"

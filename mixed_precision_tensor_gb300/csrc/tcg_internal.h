@@ -7,20 +7,30 @@
 
 namespace tcg {
 
-// Tile shape of the persistent GEMM kernel (one CTA per SM).
-constexpr int kBM = 128;               // rows of D per tile (MMA M, TMEM lanes)
+// Tile shape of the persistent GEMM kernel (one CTA per SM).  With a CTA pair
+// (cta_group::2) a tile is 256 x 256: each CTA of the pair holds 128 rows of A and 128
+// rows of B per stage and 128 rows of the accumulator; with a single CTA a tile is
+// 128 x 256 and the CTA holds all 256 rows of B.
+constexpr int kBM = 128;               // rows of D per CTA (MMA M per CTA, TMEM lanes)
 constexpr int kBN = 256;               // columns of D per tile (MMA N, TMEM columns)
 constexpr int kRowBytes = 128;         // one 128-byte swizzle row of K per stage
-constexpr int kStages = 4;             // shared-memory ring depth
 constexpr int kABytes = kBM * kRowBytes;           // 16 KiB per stage
-constexpr int kBBytes = kBN * kRowBytes;           // 32 KiB per stage
-constexpr int kStageBytes = kABytes + kBBytes;     // 48 KiB per stage
+constexpr int kRingBytes = 192 * 1024;             // shared-memory operand ring
 constexpr int kAccBufs = 2;            // TMEM accumulator double buffer
 constexpr int kTmemCols = kAccBufs * kBN;          // 512 columns = all of TMEM
-constexpr int kEpiWarps = 4;
-constexpr int kThreads = 32 * (2 + kEpiWarps);     // producer, MMA, 4 epilogue warps
+constexpr int kEpiWarps = 8;           // two warps per TMEM lane quarter
+constexpr int kThreads = 32 * (2 + kEpiWarps);     // producer, MMA, 8 epilogue warps
 constexpr int kBarrierBytes = 256;
-constexpr int kSmemBytes = kStages * kStageBytes + kBarrierBytes + 1024;  // + alignment slack
+constexpr int kSmemBytes = kRingBytes + kBarrierBytes + 1024;  // + alignment slack
+
+template <int CG>
+struct TileCfg {
+    static constexpr int kBRows = kBN / CG;                  // B rows loaded per CTA
+    static constexpr int kBBytes = kBRows * kRowBytes;
+    static constexpr int kStageBytes = kABytes + kBBytes;    // 48 KiB (1 CTA), 32 KiB (pair)
+    static constexpr int kStages = kRingBytes / kStageBytes; // 4 (1 CTA), 6 (pair)
+    static constexpr int kTileM = kBM * CG;                  // rows of D per tile
+};
 
 // Bits of the device error word (which bounded wait gave up).
 constexpr uint32_t kErrProducer = 1u;    // producer waiting for a free stage
@@ -31,13 +41,24 @@ constexpr uint32_t kErrDrain = 16u;      // end-of-kernel drain
 
 enum OutKind { kOutF32 = 0, kOutF16 = 1, kOutBF16 = 2 };
 
+// How an operand tile sits in global and shared memory.
+//   kK:        K contiguous.  3-D map {K, rows, batch}; shared tile = rows of 128 B
+//              along K, 8-row groups 1 KiB apart.
+//   kMNChunk:  M/N contiguous.  3-D map {rows, K, batch}; one box per 64-element
+//              (128-byte) chunk of rows, each chunk holding all K rows of the stage.
+//   kMNInter:  M/N contiguous, rows % 64 == 0 and K % 8 == 0.  5-D map
+//              {64, 8, rows/64, K/8, batch}; one box per stage that interleaves the
+//              chunks inside every 8-row K group (1 KiB core blocks), which is the
+//              layout the tensor core reads at full rate.
+enum OperandMode { kK = 0, kMNChunk = 1, kMNInter = 2 };
+
 struct GemmArgs {
     int m, n, k;
     int batch;
     int num_m_tiles, num_n_tiles, num_k_blocks;
     int total_tiles;
     int group_m;               // tile rasterisation: group of m-tiles walked together
-    int a_kmajor, b_kmajor;    // operand majorness in global memory
+    int a_mode, b_mode;        // OperandMode of A and B
     int a_bcast, b_bcast;      // batch stride 0: always batch coordinate 0
     int is_tf32;               // kind::tf32 (else kind::f16)
     int k_per_block;           // K elements per stage: 64 (16-bit) or 32 (TF32)
@@ -53,8 +74,11 @@ struct GemmArgs {
 };
 
 // Launchers (tcg_kernels.cu).  Return the launch's cudaError_t.
+// cta_group: 1 (128x256 tiles, one CTA) or 2 (256x256 tiles, CTA pairs; grid even).
 cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &a,
-                        int out_kind, int grid, cudaStream_t s);
+                        int out_kind, int cta_group, int grid, cudaStream_t s);
+// Largest number of CTAs of the GEMM kernel that can be resident at once.
+int gemm_max_resident_ctas(int cta_group, int num_sms);
 cudaError_t launch_scale(void *D, const void *C, int m, int n, int64_t ldc, int64_t strideC,
                          int batch, float beta, int out_kind, int grid, cudaStream_t s);
 cudaError_t launch_tf32_pack(const void *in, int64_t ld, int64_t stride_in, int in_kmajor,

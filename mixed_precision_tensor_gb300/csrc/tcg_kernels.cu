@@ -37,9 +37,11 @@
 
 namespace tcg {
 
+constexpr int kMaxStages = TileCfg<2>::kStages;
+
 struct SmemCtl {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
     uint64_t acc_full[kAccBufs];
     uint64_t acc_empty[kAccBufs];
     uint64_t drain;
@@ -48,8 +50,21 @@ struct SmemCtl {
 };
 static_assert(sizeof(SmemCtl) <= kBarrierBytes, "barrier area too small");
 
+// Raise the abort flag in this CTA and, for a pair, in the peer CTA.
+template <int CG>
+__device__ __forceinline__ void raise_abort(SmemCtl *ctl, const GemmArgs &p, uint32_t err_bit)
+{
+    ctl->abort_flag = 1;
+    if constexpr (CG == 2)
+        st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int *>(&ctl->abort_flag)),
+                                          cluster_ctarank() ^ 1u),
+                              1u);
+    atomicOr(p.err, err_bit);
+}
+
 // Bounded wait on an mbarrier phase.  Returns false if the kernel was aborted or the
 // limit ran out (then the error bit is recorded and the abort flag raised).
+template <int CG>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, SmemCtl *ctl,
                                              const GemmArgs &p, uint32_t err_bit,
                                              bool honour_abort = true)
@@ -63,8 +78,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, Smem
         if (honour_abort && ctl->abort_flag)
             return false;
         if (globaltimer_ns() - t0 > p.wait_limit_ns) {
-            ctl->abort_flag = 1;
-            atomicOr(p.err, err_bit);
+            raise_abort<CG>(ctl, p, err_bit);
             return false;
         }
     }
@@ -106,11 +120,23 @@ __device__ __forceinline__ float load_c(const void *C, int64_t idx)
         return __bfloat162float(static_cast<const __nv_bfloat16 *>(C)[idx]);
 }
 
-template <int OUT>
+// CG = 1: one CTA per 128x256 tile.  CG = 2: a CTA pair (cluster of 2) per 256x256 tile;
+// the even CTA issues the MMAs (cta_group::2), both CTAs load their halves of A and B
+// and signal the even CTA's "full" barrier, the MMA completion is multicast to both
+// CTAs' "empty" and "accumulator full" barriers, and both CTAs' epilogues report to the
+// even CTA's "accumulator empty" barrier.
+template <int OUT, int CG, bool TF32>
 __global__ void __launch_bounds__(kThreads, 1)
     tcg_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB, const GemmArgs p)
 {
+    using Cfg = TileCfg<CG>;
+    constexpr int kStages = Cfg::kStages;
+    constexpr int kBRows = Cfg::kBRows;
+    constexpr int kBBytes = Cfg::kBBytes;
+    constexpr int kStageBytes = Cfg::kStageBytes;
+    constexpr int kTileM = Cfg::kTileM;
+
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms.
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -118,10 +144,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *base_ptr = smem_raw + (base - raw_u32);
     const uint32_t a_smem = base;
     const uint32_t b_smem = base + kStages * kABytes;
-    SmemCtl *ctl = reinterpret_cast<SmemCtl *>(base_ptr + kStages * kStageBytes);
+    SmemCtl *ctl = reinterpret_cast<SmemCtl *>(base_ptr + kRingBytes);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = (CG == 2) ? cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    const int cluster_id = blockIdx.x / CG;
+    const int num_clusters = gridDim.x / CG;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -130,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int a = 0; a < kAccBufs; ++a) {
             mbar_init(smem_u32(&ctl->acc_full[a]), 1);
-            mbar_init(smem_u32(&ctl->acc_empty[a]), kEpiWarps);
+            mbar_init(smem_u32(&ctl->acc_empty[a]), kEpiWarps * CG);
         }
         mbar_init(smem_u32(&ctl->drain), 1);
         ctl->abort_flag = 0;
@@ -138,70 +168,117 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB);
     }
+    __syncwarp();
     if (warp == 1) {
-        tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
-        tmem_relinquish();
+        if constexpr (CG == 2) {
+            tmem_alloc_pair(smem_u32(&ctl->tmem_base), kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(&ctl->tmem_base), kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
-    __syncthreads();
+    if constexpr (CG == 2)
+        cluster_sync_all();
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
 
     // Byte offsets of successive K slices (one MMA each) inside a stage, and the
-    // descriptor strides, per operand majorness.
-    const int esize = p.is_tf32 ? 4 : 2;
-    const uint32_t k_mma = 32u / esize;                       // K per MMA instruction
+    // descriptor strides, per operand majorness.  The MMA kind is a template argument:
+    // the issuing thread's loop must stay branch-free, as its instruction rate is what
+    // keeps the tensor core fed.
+    constexpr uint32_t kEsize = TF32 ? 4u : 2u;
+    constexpr uint32_t kKmma = 32u / kEsize;                  // K per MMA instruction
+    constexpr int kMmasPerStage = kRowBytes / 32;             // 4
     const uint32_t chunk_bytes = static_cast<uint32_t>(p.k_per_block) * kRowBytes;
-    const uint32_t a_kstep = p.a_kmajor ? 32u : k_mma * kRowBytes;
-    const uint32_t b_kstep = p.b_kmajor ? 32u : k_mma * kRowBytes;
-    const uint32_t a_lbo = p.a_kmajor ? 16u : chunk_bytes;
-    const uint32_t b_lbo = p.b_kmajor ? 16u : chunk_bytes;
-    constexpr uint32_t kSbo = 8 * kRowBytes;                  // 8-row group stride
-    const int mmas_per_stage = kRowBytes / 32;                // 4
-    uint32_t issued_mask = 0, issued_parity = 0;              // producer: loads issued per stage
+    // Per operand: byte step between successive K slices, and the descriptor's
+    // leading / stride byte offsets (see OperandMode).
+    auto layout = [&](int mode, int rows, uint32_t &kstep, uint32_t &lbo, uint32_t &sbo) {
+        if (mode == kK) {
+            kstep = 32u;                                      // 32 bytes further along K
+            lbo = 16u;                                        // unused for this layout
+            sbo = 8 * kRowBytes;
+        } else if (mode == kMNChunk) {
+            kstep = kKmma * kRowBytes;                        // kKmma rows of 128 B
+            lbo = chunk_bytes;                                // next 64-element chunk
+            sbo = 8 * kRowBytes;                              // next 8-row K group
+        } else {
+            const uint32_t nchunks = static_cast<uint32_t>(rows) / 64u;
+            kstep = (kKmma / 8u) * nchunks * 1024u;           // kKmma/8 K groups
+            lbo = 1024u;                                      // next chunk, same K group
+            sbo = nchunks * 1024u;                            // next K group
+        }
+    };
+    uint32_t a_kstep, a_lbo, a_sbo, b_kstep, b_lbo, b_sbo;
+    layout(p.a_mode, kBM, a_kstep, a_lbo, a_sbo);
+    layout(p.b_mode, kBRows, b_kstep, b_lbo, b_sbo);
+    // Descriptors of stage 0, K slice 0; other slices add (byte offset >> 4) to the
+    // start-address field (bits 0-13), which cannot overflow in 227 KB of shared memory.
+    const uint64_t a_desc0 = smem_desc_sw128(a_smem, a_lbo, a_sbo);
+    const uint64_t b_desc0 = smem_desc_sw128(b_smem, b_lbo, b_sbo);
+    uint32_t issued_mask = 0, issued_parity = 0;              // leader producer: loads per stage
 
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------------------ producer
             int stage = 0;
             uint32_t phase = 0;
-            bool skip_once = p.fault_inject != 0;
+            bool skip_once = p.fault_inject != 0 && leader;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
+            for (int t = cluster_id; ok && t < p.total_tiles; t += num_clusters) {
                 int b, mt, nt;
                 tile_coords(p, t, b, mt, nt);
-                const int m0 = mt * kBM, n0 = nt * kBN;
+                const int m0 = mt * kTileM + static_cast<int>(rank) * kBM;
+                const int n0 = nt * kBN + static_cast<int>(rank) * kBRows;
                 const int za = p.a_bcast ? 0 : b, zb = p.b_bcast ? 0 : b;
                 for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-                    const uint32_t fb = smem_u32(&ctl->full[stage]);
-                    if (!wait_bounded(smem_u32(&ctl->empty[stage]), phase ^ 1u, ctl, p,
-                                      kErrProducer)) {
+                    const uint32_t fb_local = smem_u32(&ctl->full[stage]);
+                    const uint32_t fb = (CG == 2) ? mapa_shared(fb_local, 0) : fb_local;
+                    if (!wait_bounded<CG>(smem_u32(&ctl->empty[stage]), phase ^ 1u, ctl, p,
+                                          kErrProducer)) {
                         ok = false;
                         break;
                     }
                     if (skip_once) {
                         skip_once = false;  // test hook: this stage is never filled
                     } else {
-                        mbar_arrive_expect_tx(fb, kStageBytes);
+                        if (leader) {
+                            mbar_arrive_expect_tx(fb_local, kStageBytes * CG);
+                            issued_mask |= 1u << stage;
+                            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                        }
                         const uint32_t sa = a_smem + stage * kABytes;
                         const uint32_t sb = b_smem + stage * kBBytes;
                         const int k0 = kb * p.k_per_block;
-                        if (p.a_kmajor) {
-                            tma_load_3d(sa, &tmA, fb, k0, m0, za);
-                        } else {
-                            for (int h = 0; h < kBM / p.mn_box; ++h)
-                                tma_load_3d(sa + h * chunk_bytes, &tmA, fb, m0 + h * p.mn_box, k0,
-                                            za);
-                        }
-                        if (p.b_kmajor) {
-                            tma_load_3d(sb, &tmB, fb, k0, n0, zb);
-                        } else {
-                            for (int h = 0; h < kBN / p.mn_box; ++h)
-                                tma_load_3d(sb + h * chunk_bytes, &tmB, fb, n0 + h * p.mn_box, k0,
-                                            zb);
-                        }
-                        issued_mask |= 1u << stage;
-                        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                        // One operand tile: `rows` rows starting at row0, K slice k0.
+                        auto load = [&](uint32_t dst, const CUtensorMap *map, int mode, int rows,
+                                        int row0, int z) {
+                            if (mode == kK) {
+                                if constexpr (CG == 2)
+                                    tma_load_3d_pair(dst, map, fb, k0, row0, z);
+                                else
+                                    tma_load_3d(dst, map, fb, k0, row0, z);
+                            } else if (mode == kMNChunk) {
+                                for (int h = 0; h < rows / p.mn_box; ++h) {
+                                    if constexpr (CG == 2)
+                                        tma_load_3d_pair(dst + h * chunk_bytes, map, fb,
+                                                         row0 + h * p.mn_box, k0, z);
+                                    else
+                                        tma_load_3d(dst + h * chunk_bytes, map, fb,
+                                                    row0 + h * p.mn_box, k0, z);
+                                }
+                            } else {
+                                if constexpr (CG == 2)
+                                    tma_load_5d_pair(dst, map, fb, 0, 0, row0 / 64, k0 / 8, z);
+                                else
+                                    tma_load_5d(dst, map, fb, 0, 0, row0 / 64, k0 / 8, z);
+                            }
+                        };
+                        load(sa, &tmA, p.a_mode, kBM, m0, za);
+                        load(sb, &tmB, p.b_mode, kBRows, n0, zb);
                     }
                     if (++stage == kStages) {
                         stage = 0;
@@ -211,40 +288,53 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             // ----------------------------------------------------------- MMA issue
             int stage = 0;
             uint32_t phase = 0;
             int it = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x, ++it) {
+            for (int t = cluster_id; ok && t < p.total_tiles; t += num_clusters, ++it) {
                 const int acc = it & 1;
                 const uint32_t acc_phase = (it >> 1) & 1;
-                if (!wait_bounded(smem_u32(&ctl->acc_empty[acc]), acc_phase ^ 1u, ctl, p,
-                                  kErrMmaAcc)) {
+                if (!wait_bounded<CG>(smem_u32(&ctl->acc_empty[acc]), acc_phase ^ 1u, ctl, p,
+                                      kErrMmaAcc)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
                 for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-                    if (!wait_bounded(smem_u32(&ctl->full[stage]), phase, ctl, p, kErrMmaFull)) {
+                    if (!wait_bounded<CG>(smem_u32(&ctl->full[stage]), phase, ctl, p,
+                                          kErrMmaFull)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = a_smem + stage * kABytes;
-                    const uint32_t sb = b_smem + stage * kBBytes;
-                    for (int kk = 0; kk < mmas_per_stage; ++kk) {
-                        const uint64_t ad = smem_desc_sw128(sa + kk * a_kstep, a_lbo, kSbo);
-                        const uint64_t bd = smem_desc_sw128(sb + kk * b_kstep, b_lbo, kSbo);
+                    const uint64_t ad_s = a_desc0 + ((static_cast<uint32_t>(stage) * kABytes) >> 4);
+                    const uint64_t bd_s = b_desc0 + ((static_cast<uint32_t>(stage) * kBBytes) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < kMmasPerStage; ++kk) {
+                        const uint64_t ad = ad_s + ((kk * a_kstep) >> 4);
+                        const uint64_t bd = bd_s + ((kk * b_kstep) >> 4);
                         const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
-                        if (p.is_tf32)
-                            mma_tf32(d_tmem, ad, bd, p.idesc, accum);
-                        else
-                            mma_f16(d_tmem, ad, bd, p.idesc, accum);
+                        if constexpr (CG == 2) {
+                            if constexpr (TF32)
+                                mma_tf32_pair(d_tmem, ad, bd, p.idesc, accum);
+                            else
+                                mma_f16_pair(d_tmem, ad, bd, p.idesc, accum);
+                        } else {
+                            if constexpr (TF32)
+                                mma_tf32(d_tmem, ad, bd, p.idesc, accum);
+                            else
+                                mma_f16(d_tmem, ad, bd, p.idesc, accum);
+                        }
                     }
-                    mma_commit(smem_u32(&ctl->empty[stage]));  // stage free once read
+                    // the stage is free (in both CTAs) once these MMAs have read it
+                    if constexpr (CG == 2)
+                        mma_commit_pair_mc(smem_u32(&ctl->empty[stage]), 0x3);
+                    else
+                        mma_commit(smem_u32(&ctl->empty[stage]));
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -252,52 +342,76 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok)
                     break;
-                mma_commit(smem_u32(&ctl->acc_full[acc]));     // accumulator ready
+                // accumulator ready (in both CTAs)
+                if constexpr (CG == 2)
+                    mma_commit_pair_mc(smem_u32(&ctl->acc_full[acc]), 0x3);
+                else
+                    mma_commit(smem_u32(&ctl->acc_full[acc]));
             }
             // Every MMA issued so far must be complete before TMEM is released.
-            mma_commit(smem_u32(&ctl->drain));
-            wait_bounded(smem_u32(&ctl->drain), 0, ctl, p, kErrDrain, false);
+            if constexpr (CG == 2)
+                mma_commit_pair(smem_u32(&ctl->drain));
+            else
+                mma_commit(smem_u32(&ctl->drain));
+            wait_bounded<CG>(smem_u32(&ctl->drain), 0, ctl, p, kErrDrain, false);
         }
     } else {
         // -------------------------------------------------------------- epilogue
         const int q = warp & 3;                       // TMEM lane quarter of this warp
+        const int half = (warp - 2) >> 2;             // which 128 columns of the tile
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+        const uint32_t acc_empty_local = smem_u32(&ctl->acc_empty[0]);
         int it = 0;
-        for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++it) {
+        for (int t = cluster_id; t < p.total_tiles; t += num_clusters, ++it) {
             const int acc = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
-            bool ok = wait_bounded(smem_u32(&ctl->acc_full[acc]), acc_phase, ctl, p, kErrEpilogue);
+            bool ok = wait_bounded<CG>(smem_u32(&ctl->acc_full[acc]), acc_phase, ctl, p,
+                                       kErrEpilogue);
             if (!__all_sync(0xffffffffu, ok))
                 break;
             tc_fence_after();
             int b, mt, nt;
             tile_coords(p, t, b, mt, nt);
-            const int row = mt * kBM + q * 32 + lane;
+            const int row = mt * kTileM + static_cast<int>(rank) * kBM + q * 32 + lane;
             const bool row_ok = row < p.m;
             const int64_t boff = static_cast<int64_t>(b) * p.strideC;
-            for (int c = 0; c < kBN / 32; ++c) {
+            const int64_t row_base = boff + row;
+            constexpr int kChunks = kBN / 2 / 32;      // 4 chunks of 32 columns per warp
+#pragma unroll 1
+            for (int c = 0; c < kChunks; ++c) {
+                __syncwarp();                          // tcgen05.ld is warp-collective
+                const int ccol = half * (kBN / 2) + c * 32;     // column within the tile
+                const int col0 = nt * kBN + ccol;
+                // C first: 32 independent loads in flight before anything is stored.
+                float cv[32];
+                if (p.beta != 0.0f) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        cv[j] = (row_ok && col0 + j < p.n)
+                                    ? load_c<OUT>(p.C, row_base + static_cast<int64_t>(col0 + j) * p.ldc)
+                                    : 0.0f;
+                }
                 uint32_t v[32];
-                tmem_ld_32x32b_x32(tmem_base + lane_off + static_cast<uint32_t>(acc * kBN + c * 32),
-                                   v);
+                tmem_ld_32x32b_x32(tmem_base + lane_off + static_cast<uint32_t>(acc * kBN + ccol), v);
                 tmem_ld_wait();
-                if (c == kBN / 32 - 1) {
-                    // Accumulator fully read: hand it back to the MMA warp.
+                if (c == kChunks - 1) {
+                    // This warp has read its part of the accumulator: report to the MMA CTA.
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive(smem_u32(&ctl->acc_empty[acc]));
+                    if (lane == 0) {
+                        const uint32_t bar = acc_empty_local + static_cast<uint32_t>(acc * 8);
+                        mbar_arrive_cluster(CG == 2 ? mapa_shared(bar, 0) : bar);
+                    }
                 }
-                const int col0 = nt * kBN + c * 32;
                 if (row_ok) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int col = col0 + j;
                         if (col < p.n) {
-                            const int64_t idx = boff + row + static_cast<int64_t>(col) * p.ldc;
                             float r = p.alpha * __uint_as_float(v[j]);
                             if (p.beta != 0.0f)
-                                r = fmaf(p.beta, load_c<OUT>(p.C, idx), r);
-                            store_out<OUT>(p.D, idx, r);
+                                r = fmaf(p.beta, cv[j], r);
+                            store_out<OUT>(p.D, row_base + static_cast<int64_t>(col) * p.ldc, r);
                         }
                     }
                 }
@@ -306,18 +420,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     tc_fence_before();
-    __syncthreads();
+    if constexpr (CG == 2)
+        cluster_sync_all();
+    else
+        __syncthreads();
     if (ctl->abort_flag && warp == 0 && lane == 0) {
-        // Aborted: let every load already issued land before the CTA leaves.
-        for (int s = 0; s < kStages; ++s)
-            if (issued_mask & (1u << s))
-                wait_bounded(smem_u32(&ctl->full[s]), (issued_parity >> s) & 1u, ctl, p,
-                             kErrDrain, false);
+        // Aborted: let every load already issued land before the CTA leaves.  The
+        // leader waits on its stage barriers (which count both CTAs' bytes); both CTAs
+        // then give straggling copies a further 20 us.
+        if (leader)
+            for (int s = 0; s < kStages; ++s)
+                if (issued_mask & (1u << s))
+                    wait_bounded<CG>(smem_u32(&ctl->full[s]), (issued_parity >> s) & 1u, ctl, p,
+                                     kErrDrain, false);
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 20000ull) {
+        }
     }
-    __syncthreads();
+    if constexpr (CG == 2)
+        cluster_sync_all();
+    else
+        __syncthreads();
     if (warp == 1) {
+        __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, kTmemCols);
+        if constexpr (CG == 2)
+            tmem_dealloc_pair(tmem_base, kTmemCols);
+        else
+            tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
@@ -392,24 +522,81 @@ __global__ void __launch_bounds__(256) tcg_tf32_pack_kernel(const uint32_t *__re
     }
 }
 
-cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &a,
-                        int out_kind, int grid, cudaStream_t s)
+typedef void (*GemmKernelFn)(const CUtensorMap, const CUtensorMap, const GemmArgs);
+
+static GemmKernelFn gemm_fn(int out_kind, int cta_group, bool tf32)
 {
-    static bool attr_set[3] = {false, false, false};
-    void (*fn)(const CUtensorMap, const CUtensorMap, const GemmArgs) = nullptr;
+    if (tf32)   // TF32 inputs always produce FP32 output
+        return cta_group == 2 ? tcg_gemm_kernel<kOutF32, 2, true> : tcg_gemm_kernel<kOutF32, 1, true>;
+    if (cta_group == 2) {
+        switch (out_kind) {
+        case kOutF32: return tcg_gemm_kernel<kOutF32, 2, false>;
+        case kOutF16: return tcg_gemm_kernel<kOutF16, 2, false>;
+        default: return tcg_gemm_kernel<kOutBF16, 2, false>;
+        }
+    }
     switch (out_kind) {
-    case kOutF32: fn = tcg_gemm_kernel<kOutF32>; break;
-    case kOutF16: fn = tcg_gemm_kernel<kOutF16>; break;
-    default: fn = tcg_gemm_kernel<kOutBF16>; break;
+    case kOutF32: return tcg_gemm_kernel<kOutF32, 1, false>;
+    case kOutF16: return tcg_gemm_kernel<kOutF16, 1, false>;
+    default: return tcg_gemm_kernel<kOutBF16, 1, false>;
     }
-    if (!attr_set[out_kind]) {
-        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemBytes);
-        if (e != cudaSuccess)
-            return e;
-        attr_set[out_kind] = true;
+}
+
+static cudaError_t prepare(GemmKernelFn fn)
+{
+    // cudaFuncSetAttribute is cheap; doing it per launch keeps the code free of
+    // per-device caches.
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+}
+
+int gemm_max_resident_ctas(int cta_group, int num_sms)
+{
+    GemmKernelFn fn = gemm_fn(kOutF32, cta_group, false);
+    if (prepare(fn) != cudaSuccess) {
+        cudaGetLastError();
+        return num_sms / cta_group * cta_group;
     }
-    fn<<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, a);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(num_sms / cta_group * cta_group, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cta_group;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, fn, &cfg) != cudaSuccess || clusters <= 0) {
+        cudaGetLastError();
+        return num_sms / cta_group * cta_group;
+    }
+    return clusters * cta_group;
+}
+
+cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &a,
+                        int out_kind, int cta_group, int grid, cudaStream_t s)
+{
+    GemmKernelFn fn = gemm_fn(out_kind, cta_group, a.is_tf32 != 0);
+    cudaError_t e = prepare(fn);
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cta_group;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, fn, tmA, tmB, a);
+    if (e != cudaSuccess)
+        return e;
     return cudaGetLastError();
 }
 

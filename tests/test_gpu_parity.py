@@ -33,6 +33,15 @@ def handle(cuda_device):
     h.close()
 
 
+@pytest.fixture(scope="module", params=[1, 2], ids=["1sm", "2sm"])
+def any_handle(cuda_device, request):
+    """A handle on each kernel variant: single-SM 128x256 tiles, SM-pair 256x256 tiles."""
+    h = tcg.Handle()
+    tcg.check(tcg.tcg_set_kernel_options(h.h, request.param, 0))
+    yield h
+    h.close()
+
+
 def _to_storage(x64, t):
     if t == "f16":
         return x64.astype(np.float32).astype(np.float16).view(np.uint16)
@@ -156,7 +165,8 @@ RAGGED = [(1, 1, 1), (7, 17, 15), (129, 255, 257), (200, 127, 1000), (257, 513, 
 @pytest.mark.parametrize("m,n,k", RAGGED)
 @pytest.mark.parametrize("in_t,out_t", [("f16", "f32"), ("f16", "f16"), ("bf16", "f32"),
                                         ("bf16", "bf16"), ("f32", "f32")])
-def test_ragged_integer_bitexact(handle, m, n, k, in_t, out_t):
+def test_ragged_integer_bitexact(any_handle, m, n, k, in_t, out_t):
+    handle = any_handle
     res, guards = run_colmajor(handle, N, N, m, n, k, 1.0, 1.0, in_t, out_t, seed=m * 7 + n + k,
                                dist="integer")
     assert guards, "guard band or ldc padding overwritten"
@@ -176,7 +186,8 @@ def test_ragged_random_within_bound(handle, m, n, k, in_t, out_t):
 @pytest.mark.parametrize("transa", [N, T])
 @pytest.mark.parametrize("transb", [N, T])
 @pytest.mark.parametrize("in_t", ["f16", "bf16", "f32"])
-def test_all_op_combinations(handle, transa, transb, in_t):
+def test_all_op_combinations(any_handle, transa, transb, in_t):
+    handle = any_handle
     m, n, k = 300, 520, 200
     res, guards = run_colmajor(handle, transa, transb, m, n, k, 1.0, 1.0, in_t, "f32",
                                seed=5 + transa * 2 + transb, dist="integer", extra_ld=2)
@@ -188,9 +199,29 @@ def test_all_op_combinations(handle, transa, transb, in_t):
     _assert_results(res, k, 1.5, 0.25, "f32", exact=False)
 
 
+# M/N multiples of 64 and K a multiple of 8: M/N-major operands take the interleaved
+# (5-D tensor map) layout; K % 64 != 0 exercises its zero-filled K tail.
+INTERLEAVED = [(320, 448, 200), (192, 64, 8), (640, 384, 1000), (128, 128, 72)]
+
+
+@pytest.mark.parametrize("m,n,k", INTERLEAVED)
+@pytest.mark.parametrize("transa", [N, T])
+@pytest.mark.parametrize("transb", [N, T])
+def test_interleaved_mn_layout(any_handle, m, n, k, transa, transb):
+    for in_t in ("f16", "bf16"):
+        res, guards = run_colmajor(any_handle, transa, transb, m, n, k, 1.0, 1.0, in_t, "f32",
+                                   seed=m + n + k + transa, dist="integer")
+        assert guards
+        _assert_results(res, k, 1.0, 1.0, "f32", exact=True)
+    res, guards = run_colmajor(any_handle, transa, transb, m, n, k, 0.5, 2.0, "f16", "f16",
+                               seed=7 * m + k, dist="uniform", batch=2)
+    assert guards
+    _assert_results(res, k, 0.5, 2.0, "f16", exact=False)
+
+
 @pytest.mark.parametrize("in_t,out_t", [("f16", "f16"), ("f16", "f32"), ("f32", "f32")])
-def test_strided_batched_ragged(handle, in_t, out_t):
-    res, guards = run_colmajor(handle, N, T, 100, 72, 40, 1.0, 0.5, in_t, out_t, seed=77,
+def test_strided_batched_ragged(any_handle, in_t, out_t):
+    res, guards = run_colmajor(any_handle, N, T, 100, 72, 40, 1.0, 0.5, in_t, out_t, seed=77,
                                dist="integer", batch=5)
     assert guards
     _assert_results(res, 40, 1.0, 0.5, out_t, exact=True)
@@ -344,10 +375,12 @@ def test_large_workload_sampled_integer(handle, name):
     _check_sampled(w, A, B, C, out, exact=True, count=16)
 
 
-def test_timeout_is_reported_not_hung(handle):
+@pytest.mark.parametrize("cta_group", [1, 2])
+def test_timeout_is_reported_not_hung(cuda_device, cta_group):
     """A bounded wait that runs out (a stage nobody fills) ends the kernel with a
     TIMEOUT status in the error word; the context stays usable afterwards."""
     h = tcg.Handle()
+    tcg.check(tcg.tcg_set_kernel_options(h.h, cta_group, 0))
     A = torch.ones(256, 256, dtype=torch.float16, device="cuda")
     B = torch.ones(256, 256, dtype=torch.float16, device="cuda")
     C = torch.zeros(256, 256, device="cuda")
