@@ -158,6 +158,46 @@ tcgStatus_t tcg_gemm_strided_batched(tcgHandle_t h, tcgOp_t transa, tcgOp_t tran
                                      tcgDataType_t Ctype, int64_t ldc, int64_t strideC,
                                      int64_t batch_count, tcgComputeType_t compute);
 
+/*
+ * TF32 GEMM that allocates nothing.  The pages have no counterpart to this entry
+ * point: it exists for callers that cannot allocate device memory when they call
+ * -- a latency-critical loop that cannot afford cudaMalloc/cudaFree (they
+ * synchronise the device and take unbounded time), or a process whose device
+ * memory belongs to another allocator (a framework's caching pool, a fixed
+ * budget) that must not see raw allocations.
+ *
+ * Computes the same D = alpha*op(A)*op(B) + beta*C as tcg_gemm_ex with Atype =
+ * Btype = Ctype = TCG_R_32F and TCG_COMPUTE_32F_FAST_TF32, with the same argument
+ * rules and accuracy, on `stream` (a cudaStream_t; NULL = legacy default stream).
+ * No handle: the caller passes inputs and outputs and nothing else.
+ *
+ * Scratch: the TF32-rounded operand copies live in one fixed 32 MiB device array
+ * compiled into the library; every GPU that loads libtcg holds that array until
+ * the process exits.  A call needs (m + n) * round_up(k, 4) * 4 bytes (each part
+ * rounded up to 256 bytes) of it; larger problems return TCG_STATUS_NOT_SUPPORTED
+ * before any device work (use tcg_gemm_ex with a workspace for them).
+ *
+ * All calls share that array, which keeps the last call's contents: calls that
+ * overlap on the GPU (different streams, or different host threads without
+ * ordering) race on it and give wrong results -- keep them on one stream or
+ * otherwise ordered.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) and the tensor-map encoder with that device current; make
+ * that first call before any stream capture.  The call makes no cudaMalloc,
+ * cudaFree or other allocating call.  A bounded device wait that runs out stops
+ * the kernel early (output undefined) without a status: this entry point has no
+ * handle to report it through.
+ *
+ * Returns SUCCESS once queued; INVALID_VALUE for the argument errors of
+ * tcg_gemm_ex; NOT_SUPPORTED for problems beyond the scratch size;
+ * ARCH_MISMATCH off sm_103; NOT_INITIALIZED / EXECUTION_FAILED for CUDA errors.
+ */
+tcgStatus_t tcg_gemm_tf32_noalloc(void *stream, tcgOp_t transa, tcgOp_t transb, int64_t m,
+                                  int64_t n, int64_t k, float alpha, const float *A,
+                                  int64_t lda, const float *B, int64_t ldb, float beta,
+                                  float *C, int64_t ldc);
+
 /* Synchronise the handle's stream, then return and clear the sticky device
  * error word: SUCCESS, or TIMEOUT if a bounded wait inside a kernel gave up
  * (the kernel then stopped early and its output is undefined), or

@@ -38,7 +38,8 @@ TCG_COMPUTE_32F, TCG_COMPUTE_32F_FAST_TF32 = 0, 1
 EXPORTS = ("tcg_create", "tcg_destroy", "tcg_set_stream", "tcg_set_workspace",
            "tcg_gemm_workspace_size", "tcg_gemm_ex", "tcg_gemm_strided_batched",
            "tcg_get_device_error", "tcg_last_device_error_bits", "tcg_status_string",
-           "tcg_set_debug", "tcg_launch_count", "tcg_set_kernel_options")
+           "tcg_set_debug", "tcg_launch_count", "tcg_set_kernel_options",
+           "tcg_gemm_tf32_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -94,6 +95,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.tcg_launch_count.argtypes = [vp]
         lib.tcg_set_kernel_options.restype = st
         lib.tcg_set_kernel_options.argtypes = [vp, ci, ci]
+        lib.tcg_gemm_tf32_noalloc.restype = st
+        lib.tcg_gemm_tf32_noalloc.argtypes = [vp, ci, ci, i64, i64, i64, f32, vp, i64, vp, i64,
+                                              f32, vp, i64]
         _lib = lib
         return lib
 
@@ -175,6 +179,15 @@ def tcg_launch_count(h: int) -> int:
 
 def tcg_set_kernel_options(h: int, cta_group: int = 0, group_m: int = 0) -> int:
     return load_library().tcg_set_kernel_options(h, cta_group, group_m)
+
+
+def tcg_gemm_tf32_noalloc(stream, transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C,
+                          ldc) -> int:
+    """TF32 GEMM with its scratch in a fixed device array (no allocation); ``stream``
+    is a raw cudaStream_t (int) or None.  See include/tcg.h."""
+    return load_library().tcg_gemm_tf32_noalloc(stream, transa, transb, m, n, k, float(alpha),
+                                                _ptr(A), lda, _ptr(B), ldb, float(beta),
+                                                _ptr(C), ldc)
 
 
 # ------------------------------------------------------------ conveniences

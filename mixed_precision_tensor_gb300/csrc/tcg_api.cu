@@ -12,6 +12,7 @@
 //      min(tiles, SMs) CTAs on the handle's stream.
 
 #include <cstdlib>
+#include <mutex>
 #include <cstring>
 #include <new>
 
@@ -575,3 +576,179 @@ tcgStatus_t tcg_set_kernel_options(tcgHandle_t h, int cta_group, int group_m)
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free TF32 GEMM (tcg_gemm_tf32_noalloc).
+//
+// Some callers cannot allocate device memory at the moment they multiply: a
+// latency-critical loop cannot afford cudaMalloc/cudaFree (they synchronise the
+// device and take unbounded time), and a process whose device memory is owned by
+// another allocator (a framework's caching pool, a fixed memory budget) must not
+// make raw allocations behind that allocator's back.  The TF32 path needs scratch
+// memory for its rounded, K-major operand copies, so this entry point keeps that
+// scratch in a fixed array compiled into the library instead of a workspace.
+//
+// The array is a file-scope __device__ object: every GPU that loads the library
+// holds it (kNoAllocScratchBytes) until the process exits.  Host code must not
+// use its name as a pointer (on the host it only stands in for the symbol); the
+// device address is looked up once per device with cudaGetSymbolAddress.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;   // 32 MiB
+
+__device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+__device__ __align__(256) uint32_t g_noalloc_err;
+
+struct NoAllocDevice {
+    bool ready = false;
+    void *scratch = nullptr;     // device address of g_noalloc_scratch
+    uint32_t *err = nullptr;     // device address of g_noalloc_err
+    EncodeTiledFn encode = nullptr;
+    int num_sms = 0;
+    int max_ctas = 0;
+};
+
+constexpr int kNoAllocMaxDevices = 64;
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+std::mutex g_noalloc_mutex;
+
+// Once per device, with that device current: resolve the scratch and error-word
+// addresses and the tensor-map encoder, and size the persistent grid.
+tcgStatus_t noalloc_setup(int dev, NoAllocDevice **out)
+{
+    if (dev < 0 || dev >= kNoAllocMaxDevices)
+        return TCG_STATUS_NOT_SUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    NoAllocDevice &d = g_noalloc_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return TCG_STATUS_NOT_INITIALIZED;
+        }
+        if (major != 10 || minor != 3)
+            return TCG_STATUS_ARCH_MISMATCH;
+        void *scratch = nullptr, *err = nullptr;
+        if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess ||
+            cudaGetSymbolAddress(&err, g_noalloc_err) != cudaSuccess || !scratch || !err) {
+            cudaGetLastError();
+            return TCG_STATUS_NOT_INITIALIZED;
+        }
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn) {
+            cudaGetLastError();
+            return TCG_STATUS_NOT_INITIALIZED;
+        }
+        d.scratch = scratch;
+        d.err = static_cast<uint32_t *>(err);
+        d.encode = reinterpret_cast<EncodeTiledFn>(fn);
+        d.num_sms = sms;
+        d.max_ctas = gemm_max_resident_ctas(2, sms);
+        d.ready = true;
+    }
+    *out = &d;
+    return TCG_STATUS_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" tcgStatus_t tcg_gemm_tf32_noalloc(void *stream, tcgOp_t transa, tcgOp_t transb,
+                                             int64_t m, int64_t n, int64_t k, float alpha,
+                                             const float *A, int64_t lda, const float *B,
+                                             int64_t ldb, float beta, float *C, int64_t ldc)
+{
+    Problem p{transa, transb, m, n, k, alpha, beta, A, TCG_R_32F, lda, 0, B, TCG_R_32F, ldb, 0,
+              C, TCG_R_32F, ldc, 0, 1, TCG_COMPUTE_32F_FAST_TF32, false};
+    tcgStatus_t st = check_args(p);
+    if (st != TCG_STATUS_SUCCESS || m == 0 || n == 0)
+        return st;
+    const bool product = k > 0 && alpha != 0.0f;
+    if (product && tf32_ws_bytes(m, n, k, 1) > kNoAllocScratchBytes)
+        return TCG_STATUS_NOT_SUPPORTED;     // operands do not fit the fixed scratch
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return TCG_STATUS_NOT_INITIALIZED;
+    }
+    NoAllocDevice *d = nullptr;
+    st = noalloc_setup(dev, &d);
+    if (st != TCG_STATUS_SUCCESS)
+        return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (!product) {
+        // D = beta*C: no operands, no scratch.
+        int64_t blocks = (m * n + 255) / 256;
+        const int64_t cap = static_cast<int64_t>(d->num_sms) * 8;
+        if (blocks > cap)
+            blocks = cap;
+        return launch_scale(C, C, static_cast<int>(m), static_cast<int>(n), ldc, 0, 1, beta,
+                            kOutF32, static_cast<int>(blocks), s) == cudaSuccess
+                   ? TCG_STATUS_SUCCESS
+                   : TCG_STATUS_EXECUTION_FAILED;
+    }
+
+    // A handle-like context on the stack: map encoding only, nothing allocated.
+    tcgContext ctx;
+    ctx.device = dev;
+    ctx.num_sms = d->num_sms;
+    ctx.encode = d->encode;
+
+    // Round to TF32 into K-major copies inside the fixed scratch.
+    const int kp = static_cast<int>((k + 3) / 4 * 4);
+    uint8_t *Ak = static_cast<uint8_t *>(d->scratch);
+    uint8_t *Bk = Ak + ((size_t)(m * kp) * 4 + 255) / 256 * 256;
+    const bool a_kmajor = transa == TCG_OP_T, b_kmajor = transb == TCG_OP_N;
+    const int grid_pack = d->num_sms * 8;
+    if (cudaMemsetAsync(d->err, 0, sizeof(uint32_t), s) != cudaSuccess ||
+        launch_tf32_pack(A, lda, 0, a_kmajor ? 1 : 0, static_cast<int>(m), static_cast<int>(k), 1,
+                         Ak, kp, m * kp, grid_pack, s) != cudaSuccess ||
+        launch_tf32_pack(B, ldb, 0, b_kmajor ? 1 : 0, static_cast<int>(n), static_cast<int>(k), 1,
+                         Bk, kp, n * kp, grid_pack, s) != cudaSuccess) {
+        cudaGetLastError();
+        return TCG_STATUS_EXECUTION_FAILED;
+    }
+
+    constexpr int cg = 2;
+    GemmArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.m = static_cast<int>(m); a.n = static_cast<int>(n); a.k = static_cast<int>(k); a.batch = 1;
+    a.num_m_tiles = static_cast<int>((m + kBM * cg - 1) / (kBM * cg));
+    a.num_n_tiles = static_cast<int>((n + kBN - 1) / kBN);
+    a.k_per_block = 32;
+    a.num_k_blocks = static_cast<int>((k + 31) / 32);
+    a.total_tiles = a.num_m_tiles * a.num_n_tiles;
+    a.group_m = 8;
+    a.is_tf32 = 1;
+    a.mn_box = 32;
+    a.idesc = (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(kBN >> 3) << 17) |
+              (static_cast<uint32_t>((kBM * cg) >> 4) << 24);
+    a.alpha = alpha;
+    a.beta = beta;
+    a.C = C;
+    a.D = C;
+    a.ldc = ldc;
+    a.strideC = 0;
+    a.err = d->err;
+    a.wait_limit_ns = kDefaultWaitNs;
+    CUtensorMap tmA, tmB;
+    bool bca = false, bcb = false;
+    st = operand_map(&ctx, Ak, TCG_R_32F, true, m, k, kp, m * kp, 1, kBM, a.k_per_block, a.mn_box,
+                     &bca, &a.a_mode, &tmA);
+    if (st == TCG_STATUS_SUCCESS)
+        st = operand_map(&ctx, Bk, TCG_R_32F, true, n, k, kp, n * kp, 1, kBN / cg, a.k_per_block,
+                         a.mn_box, &bcb, &a.b_mode, &tmB);
+    if (st != TCG_STATUS_SUCCESS)
+        return st;
+    const int64_t want = static_cast<int64_t>(a.total_tiles) * cg;
+    const int grid = static_cast<int>(want < d->max_ctas ? want : d->max_ctas);
+    if (launch_gemm(tmA, tmB, a, kOutF32, cg, grid, s) != cudaSuccess) {
+        cudaGetLastError();
+        return TCG_STATUS_EXECUTION_FAILED;
+    }
+    return TCG_STATUS_SUCCESS;
+}
