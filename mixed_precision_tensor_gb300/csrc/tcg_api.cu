@@ -269,14 +269,16 @@ tcgStatus_t operand_map(tcgContext *h, const void *ptr, tcgDataType_t t, bool km
                                  static_cast<uint32_t>(box_rows), 1};
         return get_map(h, ptr, t, 3, dims, str, box, out);
     }
-    if (es == 2 && rows % 64 == 0 && k % 8 == 0) {
-        // Element (r, p) = (64*c2 + c0, 8*c3 + c1): every coordinate TMA accepts maps
+    const int64_t c = 128 / es;                 // elements per 128-byte chunk
+    if (rows % c == 0 && k % 8 == 0) {
+        // Element (r, p) = (c*c2 + c0, 8*c3 + c1): every coordinate TMA accepts maps
         // inside the matrix, so zero fill covers exactly the ragged K tail.
         *mode = kMNInter;
-        const uint64_t dims[5] = {64, 8, static_cast<uint64_t>(rows / 64),
+        const uint64_t dims[5] = {static_cast<uint64_t>(c), 8, static_cast<uint64_t>(rows / c),
                                   static_cast<uint64_t>(k / 8), nb};
-        const uint64_t str[4] = {ldb, 64ull * es, 8ull * ldb, bstride};
-        const uint32_t box[5] = {64, 8, static_cast<uint32_t>(box_rows / 64),
+        const uint64_t str[4] = {ldb, 128ull, 8ull * ldb, bstride};
+        const uint32_t box[5] = {static_cast<uint32_t>(c), 8,
+                                 static_cast<uint32_t>(box_rows / c),
                                  static_cast<uint32_t>(k_per_block / 8), 1};
         return get_map(h, ptr, t, 5, dims, str, box, out);
     }
@@ -336,7 +338,10 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
     int64_t sA = p.batched ? p.strideA : 0, sB = p.batched ? p.strideB : 0;
 
     if (tf32) {
-        // Round to TF32 (nearest even) into K-major packed copies in the workspace.
+        // Round to TF32 (nearest even) into K-major copies of op(A) and op(B) in the
+        // workspace (the tensor core takes TF32 operands K-major only and truncates the low
+        // 13 bits of FP32 input): K-major operands are rounded in place order, M/N-major
+        // ones transposed on the way.
         const size_t need = tf32_ws_bytes(p.m, p.n, p.k, p.batch);
         void *ws = nullptr;
         if (h->ws_user) {
@@ -363,13 +368,17 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
         const int64_t kp = (p.k + 3) / 4 * 4;
         uint8_t *Ak = static_cast<uint8_t *>(ws);
         uint8_t *Bk = Ak + ((size_t)(p.batch * p.m * kp) * 4 + 255) / 256 * 256;
-        const int grid = h->num_sms * 8;
-        // op(A) element (i, p): A[p + i*lda] if A^T else A[i + p*lda]
-        cudaError_t e = launch_tf32_pack(p.A, p.lda, sA, a_kmajor ? 1 : 0, m, k, batch, Ak, kp,
-                                         p.m * kp, grid, h->stream);
+        // a batch stride of 0 (one operand shared by all batches) stays shared
+        const int64_t nba = sA == 0 ? 1 : p.batch, nbb = sB == 0 ? 1 : p.batch;
+        cudaError_t e = a_kmajor
+            ? launch_tf32_round(p.A, p.lda, sA, p.k, p.m, nba, Ak, kp, p.m * kp, 0, h->stream)
+            : launch_tf32_transpose_round(p.A, p.lda, sA, p.m, p.k, nba, Ak, kp, p.m * kp,
+                                          h->stream);
         if (e == cudaSuccess)
-            e = launch_tf32_pack(p.B, p.ldb, sB, b_kmajor ? 1 : 0, n, k, batch, Bk, kp,
-                                 p.n * kp, grid, h->stream);
+            e = b_kmajor
+                ? launch_tf32_round(p.B, p.ldb, sB, p.k, p.n, nbb, Bk, kp, p.n * kp, 0, h->stream)
+                : launch_tf32_transpose_round(p.B, p.ldb, sB, p.n, p.k, nbb, Bk, kp, p.n * kp,
+                                              h->stream);
         h->launches += 2;
         if (e != cudaSuccess)
             return TCG_STATUS_EXECUTION_FAILED;
@@ -377,8 +386,8 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
         Bop = Bk;
         a_kmajor = b_kmajor = true;
         lda = ldb = kp;
-        sA = p.m * kp;
-        sB = p.n * kp;
+        sA = sA == 0 ? 0 : p.m * kp;
+        sB = sB == 0 ? 0 : p.n * kp;
     }
 
     const int cg = h->cta_group;

@@ -46,8 +46,10 @@ enum OutKind { kOutF32 = 0, kOutF16 = 1, kOutBF16 = 2 };
 //              along K, 8-row groups 1 KiB apart.
 //   kMNChunk:  M/N contiguous.  3-D map {rows, K, batch}; one box per 64-element
 //              (128-byte) chunk of rows, each chunk holding all K rows of the stage.
-//   kMNInter:  M/N contiguous, rows % 64 == 0 and K % 8 == 0.  5-D map
-//              {64, 8, rows/64, K/8, batch}; one box per stage that interleaves the
+//   kMNInter:  M/N contiguous, rows % c == 0 and K % 8 == 0, with c = 128 bytes /
+//              element size (64 for 16-bit operands; TF32 operands are always K-major).
+//              5-D map
+//              {c, 8, rows/c, K/8, batch}; one box per stage that interleaves the
 //              chunks inside every 8-row K group (1 KiB core blocks), which is the
 //              layout the tensor core reads at full rate.
 enum OperandMode { kK = 0, kMNChunk = 1, kMNInter = 2 };
@@ -81,6 +83,19 @@ cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const Ge
 int gemm_max_resident_ctas(int cta_group, int num_sms);
 cudaError_t launch_scale(void *D, const void *C, int m, int n, int64_t ldc, int64_t strideC,
                          int batch, float beta, int out_kind, int grid, cudaStream_t s);
+// Round FP32 -> TF32 (nearest even).  The tensor core takes TF32 operands K-major only
+// and truncates the low 13 bits of FP32 input, so every TF32 operand gets a rounded,
+// K-major copy: launch_tf32_round keeps an operand that is already K-major (rows = K,
+// cols = M or N; ld, ld_out and strides multiples of 4 elements, 16-byte aligned
+// pointers); launch_tf32_transpose_round turns an M/N-major one (rows = M or N along
+// the contiguous dimension) into a K-major copy with leading dimension ld_out.
+cudaError_t launch_tf32_round(const void *in, int64_t ld, int64_t stride_in, int64_t rows,
+                              int64_t cols, int64_t batch, void *out, int64_t ld_out,
+                              int64_t stride_out, int grid, cudaStream_t s);
+cudaError_t launch_tf32_transpose_round(const void *in, int64_t ld, int64_t stride_in,
+                                        int64_t rows, int64_t k, int64_t batch, void *out,
+                                        int64_t ld_out, int64_t stride_out, cudaStream_t s);
+// Round FP32 -> TF32 into a K-major packed copy (used by tcg_gemm_tf32_noalloc).
 cudaError_t launch_tf32_pack(const void *in, int64_t ld, int64_t stride_in, int in_kmajor,
                              int rows, int k, int batch, void *out, int64_t ld_out,
                              int64_t stride_out, int grid, cudaStream_t s);

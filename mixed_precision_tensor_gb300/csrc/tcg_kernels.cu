@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             lbo = chunk_bytes;                                // next 64-element chunk
             sbo = 8 * kRowBytes;                              // next 8-row K group
         } else {
-            const uint32_t nchunks = static_cast<uint32_t>(rows) / 64u;
+            const uint32_t nchunks = static_cast<uint32_t>(rows / p.mn_box);
             kstep = (kKmma / 8u) * nchunks * 1024u;           // kKmma/8 K groups
             lbo = 1024u;                                      // next chunk, same K group
             sbo = nchunks * 1024u;                            // next K group
@@ -272,9 +272,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 }
                             } else {
                                 if constexpr (CG == 2)
-                                    tma_load_5d_pair(dst, map, fb, 0, 0, row0 / 64, k0 / 8, z);
+                                    tma_load_5d_pair(dst, map, fb, 0, 0, row0 / p.mn_box, k0 / 8, z);
                                 else
-                                    tma_load_5d(dst, map, fb, 0, 0, row0 / 64, k0 / 8, z);
+                                    tma_load_5d(dst, map, fb, 0, 0, row0 / p.mn_box, k0 / 8, z);
                             }
                         };
                         load(sa, &tmA, p.a_mode, kBM, m0, za);
@@ -573,6 +573,109 @@ int gemm_max_resident_ctas(int cta_group, int num_sms)
         return num_sms / cta_group * cta_group;
     }
     return clusters * cta_group;
+}
+
+// K-major operand (K contiguous, `ld` elements per row of op, `rows` = K, `cols` = M or
+// N): out[b][c][r] = tf32(in[b][c][r]), 4 elements (16 bytes) per access.  ld, ld_out
+// and the strides are multiples of 4 elements and the pointers 16-byte aligned, so r runs
+// up to round_up(rows, 4), which stays inside every column's storage.
+__global__ void __launch_bounds__(256) tcg_tf32_round_kernel(const uint4 *__restrict__ in,
+                                                             int64_t ld4, int64_t stride_in4,
+                                                             int rows4, int cols, int batch,
+                                                             uint4 *__restrict__ out,
+                                                             int64_t ld_out4, int64_t stride_out4)
+{
+    for (int b = blockIdx.z; b < batch; b += gridDim.z)
+        for (int c = blockIdx.y; c < cols; c += gridDim.y) {
+            const uint4 *src = in + b * stride_in4 + static_cast<int64_t>(c) * ld4;
+            uint4 *dst = out + b * stride_out4 + static_cast<int64_t>(c) * ld_out4;
+            for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < rows4;
+                 r += gridDim.x * blockDim.x) {
+                uint4 v = src[r];
+                v.x = tf32_rne_bits(v.x);
+                v.y = tf32_rne_bits(v.y);
+                v.z = tf32_rne_bits(v.z);
+                v.w = tf32_rne_bits(v.w);
+                dst[r] = v;
+            }
+        }
+}
+
+// M/N-major operand: element (r, p) (r < rows along M or N, p < k along K) at
+// in[b*stride_in + r + p*ld]; writes the K-major copy out[b*stride_out + p + r*ld_out],
+// rounded.  64 x 64 tiles through shared memory: every warp reads and writes whole
+// 128-byte runs; the 65-word row pitch keeps the transposed reads free of bank conflicts.
+__global__ void __launch_bounds__(256) tcg_tf32_transpose_round_kernel(
+    const uint32_t *__restrict__ in, int64_t ld, int64_t stride_in, int rows, int k, int batch,
+    uint32_t *__restrict__ out, int64_t ld_out, int64_t stride_out)
+{
+    __shared__ uint32_t tile[64][65];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r_tiles = (rows + 63) / 64, p_tiles = (k + 63) / 64;
+    for (int b = blockIdx.z; b < batch; b += gridDim.z)
+        for (int pt = blockIdx.y; pt < p_tiles; pt += gridDim.y)
+            for (int rt = blockIdx.x; rt < r_tiles; rt += gridDim.x) {
+                const int r0 = rt * 64, p0 = pt * 64;
+                const uint32_t *src = in + b * stride_in;
+                uint32_t *dst = out + b * stride_out;
+                __syncthreads();
+                for (int i = warp; i < 64; i += 8) {          // row p0 + i of the tile
+                    const int pp = p0 + i;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int r = r0 + lane + 32 * h;
+                        tile[i][lane + 32 * h] =
+                            (pp < k && r < rows) ? src[r + static_cast<int64_t>(pp) * ld] : 0u;
+                    }
+                }
+                __syncthreads();
+                for (int i = warp; i < 64; i += 8) {          // output row r0 + i
+                    const int r = r0 + i;
+                    if (r >= rows)
+                        continue;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int pp = p0 + lane + 32 * h;
+                        if (pp < k)
+                            dst[pp + static_cast<int64_t>(r) * ld_out] =
+                                tf32_rne_bits(tile[lane + 32 * h][i]);
+                    }
+                }
+            }
+}
+
+static inline unsigned clamp_grid(int64_t v, int64_t cap)
+{
+    return static_cast<unsigned>(v < 1 ? 1 : (v > cap ? cap : v));
+}
+
+cudaError_t launch_tf32_round(const void *in, int64_t ld, int64_t stride_in, int64_t rows,
+                              int64_t cols, int64_t batch, void *out, int64_t ld_out,
+                              int64_t stride_out, int grid, cudaStream_t s)
+{
+    (void)grid;
+    const int64_t rows4 = (rows + 3) / 4;
+    const dim3 g(clamp_grid((rows4 + 255) / 256, 1 << 16), clamp_grid(cols, 65535),
+                 clamp_grid(batch, 65535));
+    tcg_tf32_round_kernel<<<g, 256, 0, s>>>(static_cast<const uint4 *>(in), ld / 4,
+                                            stride_in / 4, static_cast<int>(rows4),
+                                            static_cast<int>(cols), static_cast<int>(batch),
+                                            static_cast<uint4 *>(out), ld_out / 4,
+                                            stride_out / 4);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tf32_transpose_round(const void *in, int64_t ld, int64_t stride_in,
+                                        int64_t rows, int64_t k, int64_t batch, void *out,
+                                        int64_t ld_out, int64_t stride_out, cudaStream_t s)
+{
+    const dim3 g(clamp_grid((rows + 63) / 64, (int64_t(1) << 31) - 1),
+                 clamp_grid((k + 63) / 64, 65535), clamp_grid(batch, 65535));
+    tcg_tf32_transpose_round_kernel<<<g, 256, 0, s>>>(
+        static_cast<const uint32_t *>(in), ld, stride_in, static_cast<int>(rows),
+        static_cast<int>(k), static_cast<int>(batch), static_cast<uint32_t *>(out), ld_out,
+        stride_out);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &a,

@@ -208,7 +208,7 @@ INTERLEAVED = [(320, 448, 200), (192, 64, 8), (640, 384, 1000), (128, 128, 72)]
 @pytest.mark.parametrize("transa", [N, T])
 @pytest.mark.parametrize("transb", [N, T])
 def test_interleaved_mn_layout(any_handle, m, n, k, transa, transb):
-    for in_t in ("f16", "bf16"):
+    for in_t in ("f16", "bf16", "f32"):
         res, guards = run_colmajor(any_handle, transa, transb, m, n, k, 1.0, 1.0, in_t, "f32",
                                    seed=m + n + k + transa, dist="integer")
         assert guards
