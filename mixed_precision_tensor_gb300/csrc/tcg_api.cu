@@ -35,6 +35,7 @@ struct MapKey {
     const void *ptr;
     int dtype;
     int rank;
+    int swizzle;
     uint64_t dims[5];
     uint64_t strides[4];
     uint32_t box[5];
@@ -207,13 +208,14 @@ CUtensorMapDataType map_type(tcgDataType_t t)
 // per (pointer, type, dims, strides, box).
 tcgStatus_t get_map(tcgContext *h, const void *ptr, tcgDataType_t t, int rank,
                     const uint64_t *dims, const uint64_t *strides, const uint32_t *box,
-                    CUtensorMap *out)
+                    CUtensorMap *out, bool swizzle = true)
 {
     MapKey key;
     std::memset(&key, 0, sizeof key);
     key.ptr = ptr;
     key.dtype = static_cast<int>(t);
     key.rank = rank;
+    key.swizzle = swizzle ? 1 : 0;
     for (int i = 0; i < rank; ++i) {
         key.dims[i] = dims[i];
         key.box[i] = box[i];
@@ -230,7 +232,8 @@ tcgStatus_t get_map(tcgContext *h, const void *ptr, tcgDataType_t t, int rank,
     const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = h->encode(&map, map_type(t), static_cast<cuuint32_t>(rank),
                            const_cast<void *>(ptr), key.dims, key.strides, key.box, estr,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return TCG_STATUS_EXECUTION_FAILED;
@@ -288,6 +291,23 @@ tcgStatus_t operand_map(tcgContext *h, const void *ptr, tcgDataType_t t, bool km
     const uint32_t box[3] = {static_cast<uint32_t>(mn_box), static_cast<uint32_t>(k_per_block),
                              1};
     return get_map(h, ptr, t, 3, dims, str, box, out);
+}
+
+// Map of D (= C) for the epilogue: {m, n, batch}, box {128 rows, chunk columns, 1}, no
+// swizzle; TMA loads of C zero-fill and TMA stores of D clip outside the matrix.
+tcgStatus_t output_map(tcgContext *h, void *C, tcgDataType_t t, int64_t m, int64_t n,
+                       int64_t ldc, int64_t strideC, int64_t batch, CUtensorMap *out)
+{
+    const int es = elem_size(t);
+    const uint64_t ldb = static_cast<uint64_t>(ldc) * es;
+    uint64_t bstride = static_cast<uint64_t>(strideC) * es;
+    if (batch <= 1 || bstride == 0)
+        bstride = ldb * static_cast<uint64_t>(n);       // unused; any legal value
+    const uint64_t dims[3] = {static_cast<uint64_t>(m), static_cast<uint64_t>(n),
+                              static_cast<uint64_t>(batch < 1 ? 1 : batch)};
+    const uint64_t str[2] = {ldb, bstride};
+    const uint32_t box[3] = {static_cast<uint32_t>(kBM), static_cast<uint32_t>(epi_cols(es)), 1};
+    return get_map(h, C, t, 3, dims, str, box, out, false);
 }
 
 int out_kind(tcgDataType_t c)
@@ -433,11 +453,15 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
     a.a_bcast = abc ? 1 : 0;
     a.b_bcast = bbc ? 1 : 0;
 
+    CUtensorMap tmD;
+    st = output_map(h, p.C, p.Ctype, p.m, p.n, p.ldc, strideC, p.batch, &tmD);
+    if (st != TCG_STATUS_SUCCESS)
+        return st;
     if (h->max_ctas[cg] == 0)
         h->max_ctas[cg] = gemm_max_resident_ctas(cg, h->num_sms);
     const int64_t want = static_cast<int64_t>(a.total_tiles) * cg;
     const int grid = static_cast<int>(want < h->max_ctas[cg] ? want : h->max_ctas[cg]);
-    cudaError_t e = launch_gemm(tmA, tmB, a, ok, cg, grid, h->stream);
+    cudaError_t e = launch_gemm(tmA, tmB, tmD, a, ok, cg, grid, h->stream);
     h->launches += 1;
     return e == cudaSuccess ? TCG_STATUS_SUCCESS : TCG_STATUS_EXECUTION_FAILED;
 }
@@ -753,9 +777,13 @@ extern "C" tcgStatus_t tcg_gemm_tf32_noalloc(void *stream, tcgOp_t transa, tcgOp
                          a.mn_box, &bcb, &a.b_mode, &tmB);
     if (st != TCG_STATUS_SUCCESS)
         return st;
+    CUtensorMap tmD;
+    st = output_map(&ctx, C, TCG_R_32F, m, n, ldc, 0, 1, &tmD);
+    if (st != TCG_STATUS_SUCCESS)
+        return st;
     const int64_t want = static_cast<int64_t>(a.total_tiles) * cg;
     const int grid = static_cast<int>(want < d->max_ctas ? want : d->max_ctas);
-    if (launch_gemm(tmA, tmB, a, kOutF32, cg, grid, s) != cudaSuccess) {
+    if (launch_gemm(tmA, tmB, tmD, a, kOutF32, cg, grid, s) != cudaSuccess) {
         cudaGetLastError();
         return TCG_STATUS_EXECUTION_FAILED;
     }

@@ -15,20 +15,31 @@ constexpr int kBM = 128;               // rows of D per CTA (MMA M per CTA, TMEM
 constexpr int kBN = 256;               // columns of D per tile (MMA N, TMEM columns)
 constexpr int kRowBytes = 128;         // one 128-byte swizzle row of K per stage
 constexpr int kABytes = kBM * kRowBytes;           // 16 KiB per stage
-constexpr int kRingBytes = 192 * 1024;             // shared-memory operand ring
 constexpr int kAccBufs = 2;            // TMEM accumulator double buffer
 constexpr int kTmemCols = kAccBufs * kBN;          // 512 columns = all of TMEM
 constexpr int kEpiWarps = 8;           // two warps per TMEM lane quarter
 constexpr int kThreads = 32 * (2 + kEpiWarps);     // producer, MMA, 8 epilogue warps
+// Shared memory: operand ring + epilogue staging = kDataBytes.  Epilogue staging: each
+// half of the epilogue (4 warps, 128 rows) owns kEpiBufs buffers of one 128-row chunk
+// of D (16 FP32 or 32 16-bit columns: 8 KiB), loaded with C by TMA when beta != 0 and
+// written back by TMA.  With beta != 0 four buffers keep C three chunks ahead; without C
+// two suffice and the operand ring keeps the space.
+constexpr int kDataBytes = 224 * 1024;
+constexpr int kEpiChunkBytes = 8 * 1024;
 constexpr int kBarrierBytes = 256;
-constexpr int kSmemBytes = kRingBytes + kBarrierBytes + 1024;  // + alignment slack
+constexpr int kSmemBytes = kDataBytes + kBarrierBytes + 1024;  // + alignment slack
+// Columns of D per epilogue chunk for an output of `bytes` per element.
+__host__ __device__ constexpr int epi_cols(int out_bytes) { return kEpiChunkBytes / (kBM * out_bytes); }
 
-template <int CG>
+template <int CG, bool BETA>
 struct TileCfg {
+    static constexpr int kEpiBufs = BETA ? 4 : 2;
+    static constexpr int kEpiBytes = 2 * kEpiBufs * kEpiChunkBytes;   // 64 or 32 KiB
+    static constexpr int kRingBytes = kDataBytes - kEpiBytes;         // 160 or 192 KiB
     static constexpr int kBRows = kBN / CG;                  // B rows loaded per CTA
     static constexpr int kBBytes = kBRows * kRowBytes;
     static constexpr int kStageBytes = kABytes + kBBytes;    // 48 KiB (1 CTA), 32 KiB (pair)
-    static constexpr int kStages = kRingBytes / kStageBytes; // 4 (1 CTA), 6 (pair)
+    static constexpr int kStages = kRingBytes / kStageBytes; // pair: 6 (5 with C); 1 CTA: 4 (3)
     static constexpr int kTileM = kBM * CG;                  // rows of D per tile
 };
 
@@ -77,8 +88,9 @@ struct GemmArgs {
 
 // Launchers (tcg_kernels.cu).  Return the launch's cudaError_t.
 // cta_group: 1 (128x256 tiles, one CTA) or 2 (256x256 tiles, CTA pairs; grid even).
-cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &a,
-                        int out_kind, int cta_group, int grid, cudaStream_t s);
+// tmD maps D (= C) as {m, n, batch} with box {128, epi_cols(out bytes), 1}, no swizzle.
+cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmD,
+                        const GemmArgs &a, int out_kind, int cta_group, int grid, cudaStream_t s);
 // Largest number of CTAs of the GEMM kernel that can be resident at once.
 int gemm_max_resident_ctas(int cta_group, int num_sms);
 cudaError_t launch_scale(void *D, const void *C, int m, int n, int64_t ldc, int64_t strideC,

@@ -37,13 +37,15 @@
 
 namespace tcg {
 
-constexpr int kMaxStages = TileCfg<2>::kStages;
+constexpr int kMaxStages = TileCfg<2, false>::kStages;
+constexpr int kMaxEpiBufs = 4;
 
 struct SmemCtl {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
     uint64_t acc_full[kAccBufs];
     uint64_t acc_empty[kAccBufs];
+    uint64_t c_full[2][kMaxEpiBufs];   // epilogue half x staging buffer: C chunk landed
     uint64_t drain;
     uint32_t tmem_base;
     volatile int abort_flag;
@@ -110,6 +112,28 @@ __device__ __forceinline__ void store_out(void *D, int64_t idx, float v)
 }
 
 template <int OUT>
+__device__ __forceinline__ float load_smem(const uint8_t *buf, int idx)
+{
+    if constexpr (OUT == kOutF32)
+        return reinterpret_cast<const float *>(buf)[idx];
+    else if constexpr (OUT == kOutF16)
+        return __half2float(reinterpret_cast<const __half *>(buf)[idx]);
+    else
+        return __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(buf)[idx]);
+}
+
+template <int OUT>
+__device__ __forceinline__ void store_smem(uint8_t *buf, int idx, float v)
+{
+    if constexpr (OUT == kOutF32)
+        reinterpret_cast<float *>(buf)[idx] = v;
+    else if constexpr (OUT == kOutF16)
+        reinterpret_cast<__half *>(buf)[idx] = __float2half_rn(v);
+    else
+        reinterpret_cast<__nv_bfloat16 *>(buf)[idx] = __float2bfloat16_rn(v);
+}
+
+template <int OUT>
 __device__ __forceinline__ float load_c(const void *C, int64_t idx)
 {
     if constexpr (OUT == kOutF32)
@@ -125,13 +149,17 @@ __device__ __forceinline__ float load_c(const void *C, int64_t idx)
 // and signal the even CTA's "full" barrier, the MMA completion is multicast to both
 // CTAs' "empty" and "accumulator full" barriers, and both CTAs' epilogues report to the
 // even CTA's "accumulator empty" barrier.
-template <int OUT, int CG, bool TF32>
+template <int OUT, int CG, bool TF32, bool BETA>
 __global__ void __launch_bounds__(kThreads, 1)
     tcg_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                    const __grid_constant__ CUtensorMap tmB, const GemmArgs p)
+                    const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmD, const GemmArgs p)
 {
-    using Cfg = TileCfg<CG>;
+    using Cfg = TileCfg<CG, BETA>;
     constexpr int kStages = Cfg::kStages;
+    constexpr int kRingBytes = Cfg::kRingBytes;
+    constexpr int kEpiBufs = Cfg::kEpiBufs;
+    constexpr int kEpiBytes = Cfg::kEpiBytes;
     constexpr int kBRows = Cfg::kBRows;
     constexpr int kBBytes = Cfg::kBBytes;
     constexpr int kStageBytes = Cfg::kStageBytes;
@@ -144,7 +172,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *base_ptr = smem_raw + (base - raw_u32);
     const uint32_t a_smem = base;
     const uint32_t b_smem = base + kStages * kABytes;
-    SmemCtl *ctl = reinterpret_cast<SmemCtl *>(base_ptr + kRingBytes);
+    const uint32_t epi_smem = base + kRingBytes;
+    uint8_t *epi_ptr = base_ptr + kRingBytes;
+    SmemCtl *ctl = reinterpret_cast<SmemCtl *>(base_ptr + kRingBytes + kEpiBytes);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -162,11 +192,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&ctl->acc_full[a]), 1);
             mbar_init(smem_u32(&ctl->acc_empty[a]), kEpiWarps * CG);
         }
+        for (int h = 0; h < 2; ++h)
+            for (int bf = 0; bf < kEpiBufs; ++bf)
+                mbar_init(smem_u32(&ctl->c_full[h][bf]), 1);
         mbar_init(smem_u32(&ctl->drain), 1);
         ctl->abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB);
+        tma_prefetch_map(&tmD);
     }
     __syncwarp();
     if (warp == 1) {
@@ -357,42 +391,91 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // -------------------------------------------------------------- epilogue
-        const int q = warp & 3;                       // TMEM lane quarter of this warp
-        const int half = (warp - 2) >> 2;             // which 128 columns of the tile
+        // Two halves of 4 warps; half h owns TMEM columns [128h, 128h + 128) of each tile
+        // for all 128 rows (warp w reads TMEM lane quarter w % 4), in chunks of kCols
+        // columns.  Per chunk: C (with beta != 0) lands by TMA in a staging buffer, every
+        // thread combines its row with the accumulator in place (the buffer is a
+        // column-major 128 x kCols block of D), and the half's leader writes the block to
+        // D with one TMA store, which clips rows >= m and columns >= n.  The chunks of all
+        // tiles form one sequence g = 0, 1, ... per half; with beta != 0 the C loads run
+        // kEpiBufs - 1 chunks ahead of it (across tile boundaries).
+        constexpr int kOutBytes = OUT == kOutF32 ? 4 : 2;
+        constexpr int kCols = epi_cols(kOutBytes);             // 16 (FP32) or 32 (16-bit)
+        constexpr int kChunks = (kBN / 2) / kCols;             // per half per tile
+        constexpr int kAhead = BETA ? kEpiBufs - 1 : 0;        // C loads in flight
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const bool half_leader = (warp == 2 + 4 * half) && lane == 0;
+        const uint32_t bar_id = 1u + static_cast<uint32_t>(half);
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t acc_empty_local = smem_u32(&ctl->acc_empty[0]);
+        const uint32_t stage0 = epi_smem + static_cast<uint32_t>(half * kEpiBufs * kEpiChunkBytes);
+        uint8_t *stage0_ptr = epi_ptr + half * kEpiBufs * kEpiChunkBytes;
+        const int rl = q * 32 + lane;                           // row within the CTA's 128
+
+        // Origin (first row, first column, batch) of chunk number gg of this half.
+        auto chunk_origin = [&](uint32_t gg, int &x, int &y, int &z) -> bool {
+            const int tile = cluster_id + static_cast<int>(gg / kChunks) * num_clusters;
+            if (tile >= p.total_tiles)
+                return false;
+            const int c = static_cast<int>(gg % kChunks);
+            int b, mt, nt;
+            tile_coords(p, tile, b, mt, nt);
+            x = mt * kTileM + static_cast<int>(rank) * kBM;
+            y = nt * kBN + half * (kBN / 2) + c * kCols;
+            z = b;
+            return true;
+        };
+        // Leader: start the C load of chunk gg (if it exists) into buffer gg % kEpiBufs.
+        uint32_t issued = 0;          // C loads issued: chunks [0, issued)
+        auto load_c_chunk = [&](uint32_t gg) {
+            int x, y, z;
+            if (!chunk_origin(gg, x, y, z))
+                return;
+            const uint32_t buf = gg % kEpiBufs;
+            const uint32_t bar = smem_u32(&ctl->c_full[half][buf]);
+            if (x < p.m && y < p.n) {
+                mbar_arrive_expect_tx(bar, kEpiChunkBytes);
+                tma_load_3d(stage0 + buf * kEpiChunkBytes, &tmD, bar, x, y, z);
+            } else {
+                mbar_arrive(bar);       // nothing of this chunk is in the matrix
+            }
+            issued = gg + 1;
+        };
+        if (BETA && half_leader)
+            for (uint32_t gg = 0; gg < static_cast<uint32_t>(kAhead); ++gg)
+                load_c_chunk(gg);
+        uint32_t g = 0;                                         // chunks done by this half
         int it = 0;
         for (int t = cluster_id; t < p.total_tiles; t += num_clusters, ++it) {
             const int acc = it & 1;
             const uint32_t acc_phase = (it >> 1) & 1;
             bool ok = wait_bounded<CG>(smem_u32(&ctl->acc_full[acc]), acc_phase, ctl, p,
                                        kErrEpilogue);
-            if (!__all_sync(0xffffffffu, ok))
+            if (named_barrier_or(bar_id, 128, !ok || ctl->abort_flag))
                 break;
             tc_fence_after();
-            int b, mt, nt;
-            tile_coords(p, t, b, mt, nt);
-            const int row = mt * kTileM + static_cast<int>(rank) * kBM + q * 32 + lane;
-            const bool row_ok = row < p.m;
-            const int64_t boff = static_cast<int64_t>(b) * p.strideC;
-            const int64_t row_base = boff + row;
-            constexpr int kChunks = kBN / 2 / 32;      // 4 chunks of 32 columns per warp
+            bool aborted = false;
 #pragma unroll 1
-            for (int c = 0; c < kChunks; ++c) {
-                __syncwarp();                          // tcgen05.ld is warp-collective
-                const int ccol = half * (kBN / 2) + c * 32;     // column within the tile
-                const int col0 = nt * kBN + ccol;
-                // C first: 32 independent loads in flight before anything is stored.
-                float cv[32];
-                if (p.beta != 0.0f) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        cv[j] = (row_ok && col0 + j < p.n)
-                                    ? load_c<OUT>(p.C, row_base + static_cast<int64_t>(col0 + j) * p.ldc)
-                                    : 0.0f;
+            for (int c = 0; c < kChunks; ++c, ++g) {
+                const uint32_t buf = g % kEpiBufs;
+                uint8_t *sbuf = stage0_ptr + buf * kEpiChunkBytes;
+                if constexpr (BETA) {
+                    ok = wait_bounded<CG>(smem_u32(&ctl->c_full[half][buf]),
+                                          (g / kEpiBufs) & 1u, ctl, p, kErrEpilogue);
+                    if (named_barrier_or(bar_id, 128, !ok || ctl->abort_flag)) {
+                        aborted = true;
+                        break;
+                    }
                 }
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tmem_base + lane_off + static_cast<uint32_t>(acc * kBN + ccol), v);
+                __syncwarp();                                   // tcgen05.ld is warp-collective
+                const uint32_t taddr = tmem_base + lane_off +
+                                       static_cast<uint32_t>(acc * kBN + half * (kBN / 2) + c * kCols);
+                uint32_t v[kCols];
+                if constexpr (kCols == 16)
+                    tmem_ld_32x32b_x16(taddr, v);
+                else
+                    tmem_ld_32x32b_x32(taddr, v);
                 tmem_ld_wait();
                 if (c == kChunks - 1) {
                     // This warp has read its part of the accumulator: report to the MMA CTA.
@@ -403,19 +486,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive_cluster(CG == 2 ? mapa_shared(bar, 0) : bar);
                     }
                 }
-                if (row_ok) {
+                int cx, cy, cz;
+                chunk_origin(g, cx, cy, cz);
+                // A TMA store writes the last row run of a column in whole 16-byte units,
+                // which would touch rows >= m inside the ldc padding: a chunk that crosses
+                // row m at a non-16-byte boundary is stored by the threads instead.
+                const bool thread_store =
+                    cx + kBM > p.m && (static_cast<int64_t>(p.m) * kOutBytes) % 16 != 0;
+                float r[kCols];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int col = col0 + j;
-                        if (col < p.n) {
-                            float r = p.alpha * __uint_as_float(v[j]);
-                            if (p.beta != 0.0f)
-                                r = fmaf(p.beta, cv[j], r);
-                            store_out<OUT>(p.D, row_base + static_cast<int64_t>(col) * p.ldc, r);
-                        }
-                    }
+                for (int j = 0; j < kCols; ++j) {
+                    r[j] = p.alpha * __uint_as_float(v[j]);
+                    if constexpr (BETA)
+                        r[j] = fmaf(p.beta, load_smem<OUT>(sbuf, j * kBM + rl), r[j]);
                 }
+                if (!thread_store) {
+#pragma unroll
+                    for (int j = 0; j < kCols; ++j)
+                        store_smem<OUT>(sbuf, j * kBM + rl, r[j]);
+                } else if (cx + rl < p.m) {
+                    const int64_t base_idx = static_cast<int64_t>(cz) * p.strideC + cx + rl;
+#pragma unroll
+                    for (int j = 0; j < kCols; ++j)
+                        if (cy + j < p.n)
+                            store_out<OUT>(p.D, base_idx + static_cast<int64_t>(cy + j) * p.ldc,
+                                           r[j]);
+                }
+                fence_proxy_async_shared();
+                named_barrier_sync(bar_id, 128);               // the block is complete
+                if (half_leader) {
+                    if (!thread_store && cx < p.m && cy < p.n)
+                        tma_store_3d(&tmD, stage0 + buf * kEpiChunkBytes, cx, cy, cz);
+                    bulk_commit_group();
+                    // The buffer of chunk g + 1 (no C) or g + kAhead (C) was last stored
+                    // from by chunk g + 1 - kEpiBufs: allow only this chunk's store pending.
+                    bulk_wait_group_read<1>();
+                    if constexpr (BETA)
+                        load_c_chunk(g + kAhead);
+                }
+                named_barrier_sync(bar_id, 128);               // the next buffer is free
             }
+            if (aborted)
+                break;
+        }
+        if (half_leader) {
+            // Aborted with C loads in flight: let them land (bounded).
+            for (uint32_t gg = g; gg < issued; ++gg)
+                wait_bounded<CG>(smem_u32(&ctl->c_full[half][gg % kEpiBufs]),
+                                 (gg / kEpiBufs) & 1u, ctl, p, kErrDrain, false);
+            bulk_wait_group_all();
         }
     }
 
@@ -522,24 +641,26 @@ __global__ void __launch_bounds__(256) tcg_tf32_pack_kernel(const uint32_t *__re
     }
 }
 
-typedef void (*GemmKernelFn)(const CUtensorMap, const CUtensorMap, const GemmArgs);
+typedef void (*GemmKernelFn)(const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                             const GemmArgs);
 
-static GemmKernelFn gemm_fn(int out_kind, int cta_group, bool tf32)
+template <int CG, bool BETA>
+static GemmKernelFn gemm_fn_cg(int out_kind, bool tf32)
 {
     if (tf32)   // TF32 inputs always produce FP32 output
-        return cta_group == 2 ? tcg_gemm_kernel<kOutF32, 2, true> : tcg_gemm_kernel<kOutF32, 1, true>;
-    if (cta_group == 2) {
-        switch (out_kind) {
-        case kOutF32: return tcg_gemm_kernel<kOutF32, 2, false>;
-        case kOutF16: return tcg_gemm_kernel<kOutF16, 2, false>;
-        default: return tcg_gemm_kernel<kOutBF16, 2, false>;
-        }
-    }
+        return tcg_gemm_kernel<kOutF32, CG, true, BETA>;
     switch (out_kind) {
-    case kOutF32: return tcg_gemm_kernel<kOutF32, 1, false>;
-    case kOutF16: return tcg_gemm_kernel<kOutF16, 1, false>;
-    default: return tcg_gemm_kernel<kOutBF16, 1, false>;
+    case kOutF32: return tcg_gemm_kernel<kOutF32, CG, false, BETA>;
+    case kOutF16: return tcg_gemm_kernel<kOutF16, CG, false, BETA>;
+    default: return tcg_gemm_kernel<kOutBF16, CG, false, BETA>;
     }
+}
+
+static GemmKernelFn gemm_fn(int out_kind, int cta_group, bool tf32, bool beta)
+{
+    if (cta_group == 2)
+        return beta ? gemm_fn_cg<2, true>(out_kind, tf32) : gemm_fn_cg<2, false>(out_kind, tf32);
+    return beta ? gemm_fn_cg<1, true>(out_kind, tf32) : gemm_fn_cg<1, false>(out_kind, tf32);
 }
 
 static cudaError_t prepare(GemmKernelFn fn)
@@ -551,7 +672,7 @@ static cudaError_t prepare(GemmKernelFn fn)
 
 int gemm_max_resident_ctas(int cta_group, int num_sms)
 {
-    GemmKernelFn fn = gemm_fn(kOutF32, cta_group, false);
+    GemmKernelFn fn = gemm_fn(kOutF32, cta_group, false, false);
     if (prepare(fn) != cudaSuccess) {
         cudaGetLastError();
         return num_sms / cta_group * cta_group;
@@ -678,10 +799,10 @@ cudaError_t launch_tf32_transpose_round(const void *in, int64_t ld, int64_t stri
     return cudaGetLastError();
 }
 
-cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const GemmArgs &a,
-                        int out_kind, int cta_group, int grid, cudaStream_t s)
+cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmD,
+                        const GemmArgs &a, int out_kind, int cta_group, int grid, cudaStream_t s)
 {
-    GemmKernelFn fn = gemm_fn(out_kind, cta_group, a.is_tf32 != 0);
+    GemmKernelFn fn = gemm_fn(out_kind, cta_group, a.is_tf32 != 0, a.beta != 0.0f);
     cudaError_t e = prepare(fn);
     if (e != cudaSuccess)
         return e;
@@ -697,7 +818,7 @@ cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const Ge
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, fn, tmA, tmB, a);
+    e = cudaLaunchKernelEx(&cfg, fn, tmA, tmB, tmD, a);
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
