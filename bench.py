@@ -379,6 +379,16 @@ def run_ours(args, w):
         achieved = w.algorithmic_bytes() / (kernel_ms * 1e-3) / 1e9
         unit = "GB/s"
     traffic = traffic_record("tcg_gemm_kernel", w.name)
+    # Dense tensor peak at the SM clock sampled during the timed region: SMs x nominal
+    # dense FLOP per clock per SM (8192 for FP16/BF16 kind::f16, half for kind::tf32; the
+    # rate that ncu's tensor-pipe utilisation counter treats as 100%).
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    per_clk = 8192 if w.in_type != "f32" else 4096
+    at_clock = None
+    if clocks and clocks.get("sm_mhz"):
+        pk = sms * per_clk * clocks["sm_mhz"] * 1e6 / 1e12
+        at_clock = {"sm_mhz": clocks["sm_mhz"], "sms": sms, "flop_per_clk_per_sm": per_clk,
+                    "peak_tflops": pk, "frac": value / world / pk}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": step_ms_max, "higher_is_better": True,
@@ -394,6 +404,7 @@ def run_ours(args, w):
                    "parallelism": f"replicas x{world}"},
         "pct_of_peak": 100.0 * value / world / (peak if bound == "tensor" else float(
             peaks["bf16_tflops"])),
+        "tensor_peak_at_clock": at_clock,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{peak_src} ({'bf16_tflops' if bound == 'tensor' else 'hbm_gbs'})"},
