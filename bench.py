@@ -195,7 +195,8 @@ def time_oracle(w, A, B, C, blocks, nthreads):
                     rawv(B[0]).reshape(-1), codes[w.in_type], w.n,
                     rawv(A[0]).reshape(-1), codes[w.in_type], w.k,
                     w.beta, None if C is None else rawv(C[0]).reshape(-1), codes[w.out_type],
-                    w.n, tf32=(w.in_type == "f32"), rows=(j0, j1), cols=(i0, i1),
+                    w.n, tf32=(w.in_type == "f32" and w.compute != "3xtf32"),
+                    rows=(j0, j1), cols=(i0, i1),
                     nthreads=nthreads, want_r=False, want_abs=False)
         flops += 2.0 * (i1 - i0) * (j1 - j0) * w.k
     return time.perf_counter() - t0, flops
@@ -294,7 +295,8 @@ def run_ours(args, w):
         flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
 
     def step():
-        tcg.gemm_rowmajor(h, dA, dB, dC, alpha=w.alpha, beta=w.beta, tf32=tf32)
+        tcg.gemm_rowmajor(h, dA, dB, dC, alpha=w.alpha, beta=w.beta, tf32=tf32,
+                          split3=w.compute == "3xtf32")
 
     with torch.cuda.stream(stream):
         for _ in range(max(3, args.warmup)):
@@ -372,6 +374,8 @@ def run_ours(args, w):
         peak = float(peaks["bf16_tflops"])        # FP16 and BF16 share the dense rate
         if w.in_type == "f32":
             peak = peak / 2.0                     # TF32 dense rate: half of FP16/BF16
+        if w.compute == "3xtf32":
+            peak = peak / 3.0                     # three TF32 products per useful product
         achieved = w.flops / (kernel_ms * 1e-3) / 1e12
         unit = "TFLOP/s"
     else:
@@ -383,7 +387,7 @@ def run_ours(args, w):
     # dense FLOP per clock per SM (8192 for FP16/BF16 kind::f16, half for kind::tf32; the
     # rate that ncu's tensor-pipe utilisation counter treats as 100%).
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    per_clk = 8192 if w.in_type != "f32" else 4096
+    per_clk = 8192 if w.in_type != "f32" else (4096 // 3 if w.compute == "3xtf32" else 4096)
     at_clock = None
     if clocks and clocks.get("sm_mhz"):
         pk = sms * per_clk * clocks["sm_mhz"] * 1e6 / 1e12
@@ -393,7 +397,8 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": step_ms_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": {"f16": "f16", "bf16": "bf16", "f32": "tf32"}[w.in_type],
+        "dtype": {"f16": "f16", "bf16": "bf16", "f32": "tf32"}[w.in_type] +
+                 ("x3" if w.compute == "3xtf32" else ""),
         "data": "synthetic",
         "config": {"workload": w.name, "m": w.m, "n": w.n, "k": w.k, "batch": w.batch,
                    "in": w.in_type, "accumulate": "f32", "out": w.out_type,

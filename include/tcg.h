@@ -35,6 +35,7 @@
  *     16F  / 32F            / 32F or 16F
  *     16BF / 32F            / 32F or 16BF
  *     32F  / 32F_FAST_TF32  / 32F
+ *     32F  / 32F_3XTF32     / 32F
  *
  * Ownership and threading.  The caller owns every device buffer; libtcg never
  * frees or keeps them.  All calls are asynchronous on the handle's stream and
@@ -78,7 +79,15 @@ typedef enum {
 
 typedef enum {
     TCG_COMPUTE_32F = 0,            /* exact products, FP32 accumulation */
-    TCG_COMPUTE_32F_FAST_TF32 = 1   /* FP32 inputs rounded (RNE) to TF32 first */
+    TCG_COMPUTE_32F_FAST_TF32 = 1,  /* FP32 inputs rounded (RNE) to TF32 first */
+    /* FP32 inputs as two TF32 words each, x = hi + lo with hi = RNE_tf32(x) and
+     * lo = RNE_tf32(x - hi); D = alpha*(lo_A*hi_B + hi_A*lo_B + hi_A*hi_B) + beta*C,
+     * three tensor-core products accumulated in FP32 (lo_A*lo_B, at most 2^-22 relative,
+     * is dropped): multi-word emulation of a higher-precision product, "NVIDIA Tensor
+     * Core混合精度计算原理与应用解析", section 5.1.  Accuracy against the exact product of
+     * the FP32 inputs: |D - exact| <= (k + 8)*2^-23*(|alpha|*(|A||B|)_ij + |beta|*|C_ij|).
+     * Needs twice the TF32 workspace. */
+    TCG_COMPUTE_32F_3XTF32 = 2
 } tcgComputeType_t;
 
 typedef struct tcgContext *tcgHandle_t;

@@ -33,7 +33,7 @@ TCG_STATUS_TIMEOUT = 6
 TCG_STATUS_ALLOC_FAILED = 7
 TCG_OP_N, TCG_OP_T = 0, 1
 TCG_R_16F, TCG_R_16BF, TCG_R_32F = 0, 1, 2
-TCG_COMPUTE_32F, TCG_COMPUTE_32F_FAST_TF32 = 0, 1
+TCG_COMPUTE_32F, TCG_COMPUTE_32F_FAST_TF32, TCG_COMPUTE_32F_3XTF32 = 0, 1, 2
 
 EXPORTS = ("tcg_create", "tcg_destroy", "tcg_set_stream", "tcg_set_workspace",
            "tcg_gemm_workspace_size", "tcg_gemm_ex", "tcg_gemm_strided_batched",
@@ -234,7 +234,8 @@ def check(status: int, what: str = "") -> None:
         raise TcgError(status, what)
 
 
-def gemm_rowmajor(handle: Handle, A, B, C, alpha=1.0, beta=0.0, tf32=False) -> None:
+def gemm_rowmajor(handle: Handle, A, B, C, alpha=1.0, beta=0.0, tf32=False,
+                  split3=False) -> None:
     """Row-major D = alpha*A@B + beta*C in place in C (torch CUDA tensors).
 
     A: (m, k) or (batch, m, k); B: (k, n) or (batch, k, n); C: (m, n) or
@@ -247,6 +248,8 @@ def gemm_rowmajor(handle: Handle, A, B, C, alpha=1.0, beta=0.0, tf32=False) -> N
     at, ct = dtype_code(A.dtype), dtype_code(C.dtype)
     comp = TCG_COMPUTE_32F_FAST_TF32 if (tf32 or A.dtype.is_floating_point and
                                          at == TCG_R_32F) else TCG_COMPUTE_32F
+    if split3:
+        comp = TCG_COMPUTE_32F_3XTF32
     if not batched:
         s = tcg_gemm_ex(handle.h, TCG_OP_N, TCG_OP_N, n, m, k, alpha, B, at, n, A, at, k, beta,
                         C, ct, n, comp)

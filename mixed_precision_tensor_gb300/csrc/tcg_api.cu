@@ -102,7 +102,8 @@ tcgStatus_t check_args(const Problem &p)
         return TCG_STATUS_INVALID_VALUE;
     if (!valid_type(p.Atype) || !valid_type(p.Btype) || !valid_type(p.Ctype))
         return TCG_STATUS_INVALID_VALUE;
-    if (p.compute != TCG_COMPUTE_32F && p.compute != TCG_COMPUTE_32F_FAST_TF32)
+    if (p.compute != TCG_COMPUTE_32F && p.compute != TCG_COMPUTE_32F_FAST_TF32 &&
+        p.compute != TCG_COMPUTE_32F_3XTF32)
         return TCG_STATUS_INVALID_VALUE;
     if (p.m < 0 || p.n < 0 || p.k < 0 || p.batch < 0)
         return TCG_STATUS_INVALID_VALUE;
@@ -110,7 +111,7 @@ tcgStatus_t check_args(const Problem &p)
     if (p.Atype != p.Btype)
         return TCG_STATUS_NOT_SUPPORTED;
     if (p.Atype == TCG_R_32F) {
-        if (p.compute != TCG_COMPUTE_32F_FAST_TF32 || p.Ctype != TCG_R_32F)
+        if (p.compute == TCG_COMPUTE_32F || p.Ctype != TCG_R_32F)
             return TCG_STATUS_NOT_SUPPORTED;
     } else {
         if (p.compute != TCG_COMPUTE_32F)
@@ -350,8 +351,11 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
         return e == cudaSuccess ? TCG_STATUS_SUCCESS : TCG_STATUS_EXECUTION_FAILED;
     }
 
-    const bool tf32 = p.compute == TCG_COMPUTE_32F_FAST_TF32;
+    // TF32 compute and the three-product split both run on rounded K-major copies.
+    const bool split3 = p.compute == TCG_COMPUTE_32F_3XTF32;
+    const bool tf32 = p.compute == TCG_COMPUTE_32F_FAST_TF32 || split3;
     const void *Aop = p.A, *Bop = p.B;
+    const void *Alo = nullptr, *Blo = nullptr;
     bool a_kmajor = p.transa == TCG_OP_T;   // op(A) = A^T: K is A's contiguous dim
     bool b_kmajor = p.transb == TCG_OP_N;   // op(B) = B:   K is B's contiguous dim
     int64_t lda = p.lda, ldb = p.ldb;
@@ -361,8 +365,9 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
         // Round to TF32 (nearest even) into K-major copies of op(A) and op(B) in the
         // workspace (the tensor core takes TF32 operands K-major only and truncates the low
         // 13 bits of FP32 input): K-major operands are rounded in place order, M/N-major
-        // ones transposed on the way.
-        const size_t need = tf32_ws_bytes(p.m, p.n, p.k, p.batch);
+        // ones transposed on the way.  The split also writes the low words (x - hi).
+        const size_t one = tf32_ws_bytes(p.m, p.n, p.k, p.batch);
+        const size_t need = split3 ? 2 * one : one;
         void *ws = nullptr;
         if (h->ws_user) {
             if (h->ws_user_bytes < need)
@@ -388,22 +393,27 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
         const int64_t kp = (p.k + 3) / 4 * 4;
         uint8_t *Ak = static_cast<uint8_t *>(ws);
         uint8_t *Bk = Ak + ((size_t)(p.batch * p.m * kp) * 4 + 255) / 256 * 256;
+        uint8_t *Akl = split3 ? Ak + one : nullptr;
+        uint8_t *Bkl = split3 ? Bk + one : nullptr;
         // a batch stride of 0 (one operand shared by all batches) stays shared
         const int64_t nba = sA == 0 ? 1 : p.batch, nbb = sB == 0 ? 1 : p.batch;
         cudaError_t e = a_kmajor
-            ? launch_tf32_round(p.A, p.lda, sA, p.k, p.m, nba, Ak, kp, p.m * kp, 0, h->stream)
-            : launch_tf32_transpose_round(p.A, p.lda, sA, p.m, p.k, nba, Ak, kp, p.m * kp,
+            ? launch_tf32_round(p.A, p.lda, sA, p.k, p.m, nba, Ak, kp, p.m * kp, Akl, h->stream)
+            : launch_tf32_transpose_round(p.A, p.lda, sA, p.m, p.k, nba, Ak, kp, p.m * kp, Akl,
                                           h->stream);
         if (e == cudaSuccess)
             e = b_kmajor
-                ? launch_tf32_round(p.B, p.ldb, sB, p.k, p.n, nbb, Bk, kp, p.n * kp, 0, h->stream)
+                ? launch_tf32_round(p.B, p.ldb, sB, p.k, p.n, nbb, Bk, kp, p.n * kp, Bkl,
+                                    h->stream)
                 : launch_tf32_transpose_round(p.B, p.ldb, sB, p.n, p.k, nbb, Bk, kp, p.n * kp,
-                                              h->stream);
+                                              Bkl, h->stream);
         h->launches += 2;
         if (e != cudaSuccess)
             return TCG_STATUS_EXECUTION_FAILED;
         Aop = Ak;
         Bop = Bk;
+        Alo = Akl;
+        Blo = Bkl;
         a_kmajor = b_kmajor = true;
         lda = ldb = kp;
         sA = sA == 0 ? 0 : p.m * kp;
@@ -411,59 +421,72 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
     }
 
     const int cg = h->cta_group;
-    GemmArgs a;
-    std::memset(&a, 0, sizeof a);
-    a.m = m; a.n = n; a.k = k; a.batch = batch;
-    a.num_m_tiles = (m + kBM * cg - 1) / (kBM * cg);
-    a.num_n_tiles = (n + kBN - 1) / kBN;
-    a.k_per_block = tf32 ? 32 : 64;
-    a.num_k_blocks = (k + a.k_per_block - 1) / a.k_per_block;
-    a.total_tiles = a.num_m_tiles * a.num_n_tiles * batch;
-    a.group_m = h->group_m > 0 ? h->group_m : 8;
-    a.is_tf32 = tf32 ? 1 : 0;
-    a.mn_box = tf32 ? 32 : 64;
-    const uint32_t fmt = tf32 ? 2u : (p.Atype == TCG_R_16BF ? 1u : 0u);
-    a.idesc = (1u << 4)                               // D: FP32
-              | (fmt << 7) | (fmt << 10)              // A, B formats
-              | ((a_kmajor ? 0u : 1u) << 15)          // A: 0 = K-major, 1 = M-major
-              | ((b_kmajor ? 0u : 1u) << 16)          // B: 0 = K-major, 1 = N-major
-              | (static_cast<uint32_t>(kBN >> 3) << 17)
-              | (static_cast<uint32_t>((kBM * cg) >> 4) << 24);   // M = 128 or 256
-    a.alpha = p.alpha;
-    a.beta = p.beta;
-    a.C = p.C;
-    a.D = p.C;
-    a.ldc = p.ldc;
-    a.strideC = strideC;
-    a.err = h->d_err;
-    a.wait_limit_ns = h->wait_limit_ns;
-    a.fault_inject = h->fault_inject;
-
     const tcgDataType_t at = tf32 ? TCG_R_32F : p.Atype;
-    CUtensorMap tmA, tmB;
-    bool abc = false, bbc = false;
-    st = operand_map(h, Aop, at, a_kmajor, p.m, p.k, lda, sA, p.batch, kBM, a.k_per_block,
-                     a.mn_box, &abc, &a.a_mode, &tmA);
-    if (st != TCG_STATUS_SUCCESS)
-        return st;
-    st = operand_map(h, Bop, at, b_kmajor, p.n, p.k, ldb, sB, p.batch, kBN / cg, a.k_per_block,
-                     a.mn_box, &bbc, &a.b_mode, &tmB);
-    if (st != TCG_STATUS_SUCCESS)
-        return st;
-    a.a_bcast = abc ? 1 : 0;
-    a.b_bcast = bbc ? 1 : 0;
-
     CUtensorMap tmD;
     st = output_map(h, p.C, p.Ctype, p.m, p.n, p.ldc, strideC, p.batch, &tmD);
     if (st != TCG_STATUS_SUCCESS)
         return st;
     if (h->max_ctas[cg] == 0)
         h->max_ctas[cg] = gemm_max_resident_ctas(cg, h->num_sms);
-    const int64_t want = static_cast<int64_t>(a.total_tiles) * cg;
-    const int grid = static_cast<int>(want < h->max_ctas[cg] ? want : h->max_ctas[cg]);
-    cudaError_t e = launch_gemm(tmA, tmB, tmD, a, ok, cg, grid, h->stream);
-    h->launches += 1;
-    return e == cudaSuccess ? TCG_STATUS_SUCCESS : TCG_STATUS_EXECUTION_FAILED;
+
+    // One launch of the GEMM kernel: D = alpha * opA * opB + beta * C.
+    auto gemm_launch = [&](const void *opA, const void *opB, float beta) -> tcgStatus_t {
+        GemmArgs a;
+        std::memset(&a, 0, sizeof a);
+        a.m = m; a.n = n; a.k = k; a.batch = batch;
+        a.num_m_tiles = (m + kBM * cg - 1) / (kBM * cg);
+        a.num_n_tiles = (n + kBN - 1) / kBN;
+        a.k_per_block = tf32 ? 32 : 64;
+        a.num_k_blocks = (k + a.k_per_block - 1) / a.k_per_block;
+        a.total_tiles = a.num_m_tiles * a.num_n_tiles * batch;
+        a.group_m = h->group_m > 0 ? h->group_m : 8;
+        a.is_tf32 = tf32 ? 1 : 0;
+        a.mn_box = tf32 ? 32 : 64;
+        const uint32_t fmt = tf32 ? 2u : (p.Atype == TCG_R_16BF ? 1u : 0u);
+        a.idesc = (1u << 4)                               // D: FP32
+                  | (fmt << 7) | (fmt << 10)              // A, B formats
+                  | ((a_kmajor ? 0u : 1u) << 15)          // A: 0 = K-major, 1 = M-major
+                  | ((b_kmajor ? 0u : 1u) << 16)          // B: 0 = K-major, 1 = N-major
+                  | (static_cast<uint32_t>(kBN >> 3) << 17)
+                  | (static_cast<uint32_t>((kBM * cg) >> 4) << 24);   // M = 128 or 256
+        a.alpha = p.alpha;
+        a.beta = beta;
+        a.C = p.C;
+        a.D = p.C;
+        a.ldc = p.ldc;
+        a.strideC = strideC;
+        a.err = h->d_err;
+        a.wait_limit_ns = h->wait_limit_ns;
+        a.fault_inject = h->fault_inject;
+        CUtensorMap tmA, tmB;
+        bool abc = false, bbc = false;
+        tcgStatus_t s2 = operand_map(h, opA, at, a_kmajor, p.m, p.k, lda, sA, p.batch, kBM,
+                                     a.k_per_block, a.mn_box, &abc, &a.a_mode, &tmA);
+        if (s2 != TCG_STATUS_SUCCESS)
+            return s2;
+        s2 = operand_map(h, opB, at, b_kmajor, p.n, p.k, ldb, sB, p.batch, kBN / cg,
+                         a.k_per_block, a.mn_box, &bbc, &a.b_mode, &tmB);
+        if (s2 != TCG_STATUS_SUCCESS)
+            return s2;
+        a.a_bcast = abc ? 1 : 0;
+        a.b_bcast = bbc ? 1 : 0;
+        const int64_t want = static_cast<int64_t>(a.total_tiles) * cg;
+        const int grid = static_cast<int>(want < h->max_ctas[cg] ? want : h->max_ctas[cg]);
+        cudaError_t e = launch_gemm(tmA, tmB, tmD, a, ok, cg, grid, h->stream);
+        h->launches += 1;
+        return e == cudaSuccess ? TCG_STATUS_SUCCESS : TCG_STATUS_EXECUTION_FAILED;
+    };
+
+    if (!split3)
+        return gemm_launch(Aop, Bop, p.beta);
+    // Three products, the small ones first, accumulated into D in FP32 ("NVIDIA Tensor
+    // Core混合精度计算原理与应用解析", section 5.1); lo_A * lo_B (<= 2^-22 relative) is dropped.
+    st = gemm_launch(Alo, Bop, p.beta);
+    if (st == TCG_STATUS_SUCCESS)
+        st = gemm_launch(Aop, Blo, 1.0f);
+    if (st == TCG_STATUS_SUCCESS)
+        st = gemm_launch(Aop, Bop, 1.0f);
+    return st;
 }
 
 }  // namespace
@@ -520,9 +543,13 @@ tcgStatus_t tcg_gemm_workspace_size(tcgOp_t transa, tcgOp_t transb, int64_t m, i
     (void)transb;
     if (!bytes || m < 0 || n < 0 || k < 0 || batch_count < 0 || !valid_type(Atype))
         return TCG_STATUS_INVALID_VALUE;
-    *bytes = (compute == TCG_COMPUTE_32F_FAST_TF32 && Atype == TCG_R_32F && k > 0)
-                 ? tf32_ws_bytes(m, n, k, batch_count)
-                 : 0;
+    *bytes = 0;
+    if (Atype == TCG_R_32F && k > 0) {
+        if (compute == TCG_COMPUTE_32F_FAST_TF32)
+            *bytes = tf32_ws_bytes(m, n, k, batch_count);
+        else if (compute == TCG_COMPUTE_32F_3XTF32)
+            *bytes = 2 * tf32_ws_bytes(m, n, k, batch_count);
+    }
     return TCG_STATUS_SUCCESS;
 }
 

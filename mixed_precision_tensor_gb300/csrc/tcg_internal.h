@@ -101,12 +101,15 @@ cudaError_t launch_scale(void *D, const void *C, int m, int n, int64_t ldc, int6
 // cols = M or N; ld, ld_out and strides multiples of 4 elements, 16-byte aligned
 // pointers); launch_tf32_transpose_round turns an M/N-major one (rows = M or N along
 // the contiguous dimension) into a K-major copy with leading dimension ld_out.
+// out_lo (nullable): also write the low word of the two-word TF32 split (out = high
+// word) in the same layout as out.
 cudaError_t launch_tf32_round(const void *in, int64_t ld, int64_t stride_in, int64_t rows,
                               int64_t cols, int64_t batch, void *out, int64_t ld_out,
-                              int64_t stride_out, int grid, cudaStream_t s);
+                              int64_t stride_out, void *out_lo, cudaStream_t s);
 cudaError_t launch_tf32_transpose_round(const void *in, int64_t ld, int64_t stride_in,
                                         int64_t rows, int64_t k, int64_t batch, void *out,
-                                        int64_t ld_out, int64_t stride_out, cudaStream_t s);
+                                        int64_t ld_out, int64_t stride_out, void *out_lo,
+                                        cudaStream_t s);
 // Round FP32 -> TF32 into a K-major packed copy (used by tcg_gemm_tf32_noalloc).
 cudaError_t launch_tf32_pack(const void *in, int64_t ld, int64_t stride_in, int in_kmajor,
                              int rows, int k, int batch, void *out, int64_t ld_out,

@@ -696,28 +696,57 @@ int gemm_max_resident_ctas(int cta_group, int num_sms)
     return clusters * cta_group;
 }
 
+// Two-word TF32 split of an FP32 value ("NVIDIA Tensor Core混合精度计算原理与应用解析",
+// section 5.1: represent each operand by pieces the tensor core multiplies exactly):
+// hi = RNE_tf32(x), lo = RNE_tf32(x - hi).  x - hi is exact in FP32 (hi is within a
+// factor of two of x), so x = hi + lo up to 2^-22 |x|.  Inf and NaN keep hi = x, lo = 0;
+// a finite x that rounds past the largest TF32 value is truncated instead, so hi stays
+// finite and lo carries the rest.
+__device__ __forceinline__ void tf32_split_bits(uint32_t u, uint32_t &hi, uint32_t &lo)
+{
+    hi = tf32_rne_bits(u);
+    if ((u & 0x7F800000u) == 0x7F800000u) {
+        lo = 0u;
+        return;
+    }
+    if ((hi & 0x7F800000u) == 0x7F800000u)
+        hi = u & 0xFFFFE000u;
+    lo = tf32_rne_bits(__float_as_uint(__uint_as_float(u) - __uint_as_float(hi)));
+}
+
 // K-major operand (K contiguous, `ld` elements per row of op, `rows` = K, `cols` = M or
-// N): out[b][c][r] = tf32(in[b][c][r]), 4 elements (16 bytes) per access.  ld, ld_out
+// N): out[b][c][r] = tf32(in[b][c][r]), 4 elements (16 bytes) per access.  With out_lo
+// the two-word split is written instead: out = hi, out_lo = lo (same layout).  ld, ld_out
 // and the strides are multiples of 4 elements and the pointers 16-byte aligned, so r runs
 // up to round_up(rows, 4), which stays inside every column's storage.
 __global__ void __launch_bounds__(256) tcg_tf32_round_kernel(const uint4 *__restrict__ in,
                                                              int64_t ld4, int64_t stride_in4,
                                                              int rows4, int cols, int batch,
                                                              uint4 *__restrict__ out,
-                                                             int64_t ld_out4, int64_t stride_out4)
+                                                             int64_t ld_out4, int64_t stride_out4,
+                                                             uint4 *__restrict__ out_lo)
 {
     for (int b = blockIdx.z; b < batch; b += gridDim.z)
         for (int c = blockIdx.y; c < cols; c += gridDim.y) {
             const uint4 *src = in + b * stride_in4 + static_cast<int64_t>(c) * ld4;
-            uint4 *dst = out + b * stride_out4 + static_cast<int64_t>(c) * ld_out4;
+            const int64_t o = b * stride_out4 + static_cast<int64_t>(c) * ld_out4;
             for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < rows4;
                  r += gridDim.x * blockDim.x) {
                 uint4 v = src[r];
-                v.x = tf32_rne_bits(v.x);
-                v.y = tf32_rne_bits(v.y);
-                v.z = tf32_rne_bits(v.z);
-                v.w = tf32_rne_bits(v.w);
-                dst[r] = v;
+                if (out_lo) {
+                    uint4 lo;
+                    tf32_split_bits(v.x, v.x, lo.x);
+                    tf32_split_bits(v.y, v.y, lo.y);
+                    tf32_split_bits(v.z, v.z, lo.z);
+                    tf32_split_bits(v.w, v.w, lo.w);
+                    out_lo[o + r] = lo;
+                } else {
+                    v.x = tf32_rne_bits(v.x);
+                    v.y = tf32_rne_bits(v.y);
+                    v.z = tf32_rne_bits(v.z);
+                    v.w = tf32_rne_bits(v.w);
+                }
+                out[o + r] = v;
             }
         }
 }
@@ -728,7 +757,7 @@ __global__ void __launch_bounds__(256) tcg_tf32_round_kernel(const uint4 *__rest
 // 128-byte runs; the 65-word row pitch keeps the transposed reads free of bank conflicts.
 __global__ void __launch_bounds__(256) tcg_tf32_transpose_round_kernel(
     const uint32_t *__restrict__ in, int64_t ld, int64_t stride_in, int rows, int k, int batch,
-    uint32_t *__restrict__ out, int64_t ld_out, int64_t stride_out)
+    uint32_t *__restrict__ out, int64_t ld_out, int64_t stride_out, uint32_t *__restrict__ out_lo)
 {
     __shared__ uint32_t tile[64][65];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -757,9 +786,17 @@ __global__ void __launch_bounds__(256) tcg_tf32_transpose_round_kernel(
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int pp = p0 + lane + 32 * h;
-                        if (pp < k)
-                            dst[pp + static_cast<int64_t>(r) * ld_out] =
-                                tf32_rne_bits(tile[lane + 32 * h][i]);
+                        if (pp < k) {
+                            const int64_t o = pp + static_cast<int64_t>(r) * ld_out;
+                            if (out_lo) {
+                                uint32_t hi, lo;
+                                tf32_split_bits(tile[lane + 32 * h][i], hi, lo);
+                                dst[o] = hi;
+                                out_lo[b * stride_out + o] = lo;
+                            } else {
+                                dst[o] = tf32_rne_bits(tile[lane + 32 * h][i]);
+                            }
+                        }
                     }
                 }
             }
@@ -772,9 +809,8 @@ static inline unsigned clamp_grid(int64_t v, int64_t cap)
 
 cudaError_t launch_tf32_round(const void *in, int64_t ld, int64_t stride_in, int64_t rows,
                               int64_t cols, int64_t batch, void *out, int64_t ld_out,
-                              int64_t stride_out, int grid, cudaStream_t s)
+                              int64_t stride_out, void *out_lo, cudaStream_t s)
 {
-    (void)grid;
     const int64_t rows4 = (rows + 3) / 4;
     const dim3 g(clamp_grid((rows4 + 255) / 256, 1 << 16), clamp_grid(cols, 65535),
                  clamp_grid(batch, 65535));
@@ -782,20 +818,21 @@ cudaError_t launch_tf32_round(const void *in, int64_t ld, int64_t stride_in, int
                                             stride_in / 4, static_cast<int>(rows4),
                                             static_cast<int>(cols), static_cast<int>(batch),
                                             static_cast<uint4 *>(out), ld_out / 4,
-                                            stride_out / 4);
+                                            stride_out / 4, static_cast<uint4 *>(out_lo));
     return cudaGetLastError();
 }
 
 cudaError_t launch_tf32_transpose_round(const void *in, int64_t ld, int64_t stride_in,
                                         int64_t rows, int64_t k, int64_t batch, void *out,
-                                        int64_t ld_out, int64_t stride_out, cudaStream_t s)
+                                        int64_t ld_out, int64_t stride_out, void *out_lo,
+                                        cudaStream_t s)
 {
     const dim3 g(clamp_grid((rows + 63) / 64, (int64_t(1) << 31) - 1),
                  clamp_grid((k + 63) / 64, 65535), clamp_grid(batch, 65535));
     tcg_tf32_transpose_round_kernel<<<g, 256, 0, s>>>(
         static_cast<const uint32_t *>(in), ld, stride_in, static_cast<int>(rows),
         static_cast<int>(k), static_cast<int>(batch), static_cast<uint32_t *>(out), ld_out,
-        stride_out);
+        stride_out, static_cast<uint32_t *>(out_lo));
     return cudaGetLastError();
 }
 

@@ -32,6 +32,7 @@ class Workload:
     batch: int
     seed: int
     dist: str           # input distribution recipe, see draw()
+    compute: str = ""   # "" (the input type's default) or "3xtf32" (FP32 as two TF32 words)
 
     @property
     def flops(self) -> float:
@@ -59,9 +60,13 @@ WORKLOADS = {
                                           "f32", "f32", 1.0, 0.0, 1, 3, "uniform"),
     "fp16_batched_512x256": Workload("fp16_batched_512x256", 256, 256, 256, "f16", "f16", 1.0,
                                      0.5, 512, 4, "pow2"),
+    # not one of the five above: the multi-word (3xTF32) variant of the TF32 workload
+    "fp32_3xtf32_4096x4096x16384": Workload("fp32_3xtf32_4096x4096x16384", 4096, 4096, 16384,
+                                            "f32", "f32", 1.0, 0.0, 1, 3, "uniform",
+                                            "3xtf32"),
 }
 # Canonical order: small check case first, the headline case second.
-WORKLOAD_ORDER = list(WORKLOADS)
+WORKLOAD_ORDER = list(WORKLOADS)[:5]
 HEADLINE = "fp16_gemm_8192"
 
 

@@ -55,7 +55,8 @@ def handle(lib):
 PA, PB, PC = 0x10000, 0x20000, 0x30000
 F16, BF16, F32 = tcg.TCG_R_16F, tcg.TCG_R_16BF, tcg.TCG_R_32F
 N, T = tcg.TCG_OP_N, tcg.TCG_OP_T
-C32, TF32 = tcg.TCG_COMPUTE_32F, tcg.TCG_COMPUTE_32F_FAST_TF32
+C32, TF32, SPLIT3 = (tcg.TCG_COMPUTE_32F, tcg.TCG_COMPUTE_32F_FAST_TF32,
+                     tcg.TCG_COMPUTE_32F_3XTF32)
 INV, NSUP = tcg.TCG_STATUS_INVALID_VALUE, tcg.TCG_STATUS_NOT_SUPPORTED
 
 
@@ -85,6 +86,8 @@ def gemm(h, transa=N, transb=N, m=64, n=64, k=64, alpha=1.0, A=PA, at=F16, lda=6
     (dict(at=F32, bt=F32, comp=TF32, ct=F16, ldc=64), NSUP),
     (dict(at=F16, bt=F16, comp=TF32), NSUP),
     (dict(at=F16, bt=F16, ct=BF16), NSUP),    # 16-bit output must match the input type
+    (dict(at=F16, bt=F16, comp=SPLIT3), NSUP),                       # split needs FP32 inputs
+    (dict(at=F32, bt=F32, comp=SPLIT3, ct=F16, ldc=64), NSUP),      # and FP32 output
 ])
 def test_argument_checks(handle, kw, status):
     assert gemm(handle, **kw) == status
@@ -129,6 +132,7 @@ def test_workspace_size_query(lib):
     ws = tcg.tcg_gemm_workspace_size(N, N, 100, 50, 30, F32, TF32)
     kp = 32
     assert ws >= (100 + 50) * kp * 4
+    assert tcg.tcg_gemm_workspace_size(N, N, 100, 50, 30, F32, SPLIT3) == 2 * ws
     assert tcg.tcg_set_workspace(tcg.tcg_create(), 0x1000 + 16, 1024) == INV   # not 256-aligned
 
 

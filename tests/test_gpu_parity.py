@@ -82,7 +82,7 @@ CANARY = {"f32": np.array([0x7FC0DEAD], dtype=np.uint32).view(np.float32)[0],
 
 
 def run_colmajor(h, transa, transb, m, n, k, alpha, beta, in_t, out_t, seed, dist,
-                 extra_ld=0, batch=1):
+                 extra_ld=0, batch=1, split3=False):
     """One column-major call through the C ABI on padded buffers with guard bands;
     returns (got, ref, R, absAB, Cdecoded) as column-major (m, n) blocks per batch,
     plus a flag saying whether the guard bands survived."""
@@ -119,6 +119,8 @@ def run_colmajor(h, transa, transb, m, n, k, alpha, beta, in_t, out_t, seed, dis
     dC = _t(Cbuf).to(dev)
     cptr = dC.data_ptr() + guard * Cbuf.itemsize
     comp = tcg.TCG_COMPUTE_32F_FAST_TF32 if in_t == "f32" else tcg.TCG_COMPUTE_32F
+    if split3:
+        comp = tcg.TCG_COMPUTE_32F_3XTF32
     if batch == 1:
         s = tcg.tcg_gemm_ex(h.h, transa, transb, m, n, k, alpha, dA, CODE[in_t], lda, dB,
                             CODE[in_t], ldb, beta, cptr, CODE[out_t], ldc, comp)
@@ -140,7 +142,7 @@ def run_colmajor(h, transa, transb, m, n, k, alpha, beta, in_t, out_t, seed, dis
         D, R, AB = oracle.gemm(transa, transb, m, n, k, alpha, Araw[b * sA:(b + 1) * sA],
                                TYPE_CODE[in_t], lda, Braw[b * sB:(b + 1) * sB], TYPE_CODE[in_t],
                                ldb, beta, Cin[b * sC:(b + 1) * sC], TYPE_CODE[out_t], ldc,
-                               tf32=(in_t == "f32"))
+                               tf32=(in_t == "f32" and not split3))
         got = body[b, : ldc * n].reshape(n, ldc)[:, :m].T
         cdec = _decode(Cin[b * sC:(b + 1) * sC][: ldc * n].reshape(n, ldc)[:, :m].T, out_t)
         results.append((got, D, R, AB, cdec))
@@ -225,6 +227,42 @@ def test_strided_batched_ragged(any_handle, in_t, out_t):
                                dist="integer", batch=5)
     assert guards
     _assert_results(res, 40, 1.0, 0.5, out_t, exact=True)
+
+
+SPLIT3_SHAPES = [(1, 1, 1), (129, 255, 257), (300, 520, 1000), (256, 256, 4096), (64, 900, 33)]
+
+
+@pytest.mark.parametrize("m,n,k", SPLIT3_SHAPES)
+@pytest.mark.parametrize("transa,transb", [(N, N), (T, N), (N, T), (T, T)])
+def test_split3_tf32_recovers_fp32_accuracy(any_handle, m, n, k, transa, transb):
+    """Three-product TF32 split ("NVIDIA Tensor Core混合精度计算原理与应用解析", section
+    5.1) against the oracle's exact product of the FP32 inputs: within
+    (k + 8)*2^-23*(|alpha||A||B| + |beta||C|), and far below plain TF32's error."""
+    kw = dict(seed=31 * m + n + k + transa, dist="uniform")
+    res3, guards = run_colmajor(any_handle, transa, transb, m, n, k, 0.75, -0.5, "f32", "f32",
+                                split3=True, **kw)
+    assert guards
+    res1, _ = run_colmajor(any_handle, transa, transb, m, n, k, 0.75, -0.5, "f32", "f32",
+                           **kw)
+    (got3, D, R, AB, cdec), (got1, _, _, _, _) = res3[0], res1[0]
+    scale = 0.75 * AB + 0.5 * np.abs(cdec)
+    bound = (k + 8) * 2.0 ** -23 * scale
+    err3 = np.abs(got3.astype(np.float64) - R)
+    err1 = np.abs(got1.astype(np.float64) - R)
+    assert np.all(err3 <= bound), f"worst {np.max(err3 / np.maximum(bound, 1e-300))}"
+    # plain TF32 (one product of rounded inputs) carries the inputs' 2^-11 rounding; the
+    # split leaves only the FP32 accumulation error, which grows with k: it must still be
+    # clearly better (measured ~20x at k = 4096, more for small k)
+    if k >= 8:
+        assert np.max(err1 / np.maximum(scale, 1e-30)) > 8 * np.max(err3 / np.maximum(scale, 1e-30))
+
+
+def test_split3_batched_and_integer_exact(any_handle):
+    res, guards = run_colmajor(any_handle, N, T, 100, 72, 40, 1.0, 0.5, "f32", "f32", seed=91,
+                               dist="integer", batch=3, split3=True)
+    assert guards
+    for got, D, R, AB, cdec in res:
+        assert values_equal(got.astype(np.float64), R)
 
 
 def test_degenerate_cases(handle):
