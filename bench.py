@@ -183,7 +183,8 @@ def time_oracle(w, A, B, C, blocks, nthreads):
     import numpy as np
 
     import oracle
-    codes = {"f16": oracle.F16, "bf16": oracle.BF16, "f32": oracle.F32}
+    codes = {"f16": oracle.F16, "bf16": oracle.BF16, "f32": oracle.F32, "e4m3": oracle.F8E4M3,
+             "e5m2": oracle.F8E5M2}
 
     def rawv(x):
         return x.view(np.uint16) if x.dtype == np.float16 else x
@@ -280,7 +281,8 @@ def run_ours(args, w):
 
     def to_dev(x, t):
         tt = host(x).to(dev)
-        return tt.view(torch.bfloat16) if t == "bf16" else tt
+        views = {"bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+        return tt.view(views[t]) if t in views else tt
     dA, dB = to_dev(A, w.in_type), to_dev(B, w.in_type)
     oshape = (w.m, w.n) if squeeze else (w.batch, w.m, w.n)
     dC0 = to_dev(C, w.out_type) if C is not None else None
@@ -345,9 +347,13 @@ def run_ours(args, w):
     h2d = hA.nbytes + hB.nbytes + (hC.nbytes if hC is not None else 0)
     d2h = hD.nbytes
 
+    in_views = {"bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+
     def e2e_step():
-        dA.copy_(hA.view(torch.bfloat16) if w.in_type == "bf16" else hA, non_blocking=True)
-        dB.copy_(hB.view(torch.bfloat16) if w.in_type == "bf16" else hB, non_blocking=True)
+        dA.copy_(hA.view(in_views[w.in_type]) if w.in_type in in_views else hA,
+                 non_blocking=True)
+        dB.copy_(hB.view(in_views[w.in_type]) if w.in_type in in_views else hB,
+                 non_blocking=True)
         if hC is not None:
             dC.copy_(hC.view(torch.bfloat16) if w.out_type == "bf16" else hC, non_blocking=True)
         step()
@@ -374,6 +380,8 @@ def run_ours(args, w):
         peak = float(peaks["bf16_tflops"])        # FP16 and BF16 share the dense rate
         if w.in_type == "f32":
             peak = peak / 2.0                     # TF32 dense rate: half of FP16/BF16
+        if w.in_type in ("e4m3", "e5m2"):
+            peak = peak * 2.0                     # FP8 dense rate: twice FP16/BF16
         if w.compute == "3xtf32":
             peak = peak / 3.0                     # three TF32 products per useful product
         achieved = w.flops / (kernel_ms * 1e-3) / 1e12
@@ -387,7 +395,8 @@ def run_ours(args, w):
     # dense FLOP per clock per SM (8192 for FP16/BF16 kind::f16, half for kind::tf32; the
     # rate that ncu's tensor-pipe utilisation counter treats as 100%).
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    per_clk = 8192 if w.in_type != "f32" else (4096 // 3 if w.compute == "3xtf32" else 4096)
+    per_clk = {"f32": 4096 // 3 if w.compute == "3xtf32" else 4096, "e4m3": 16384,
+               "e5m2": 16384}.get(w.in_type, 8192)
     at_clock = None
     if clocks and clocks.get("sm_mhz"):
         pk = sms * per_clk * clocks["sm_mhz"] * 1e6 / 1e12
@@ -397,7 +406,8 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": step_ms_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": {"f16": "f16", "bf16": "bf16", "f32": "tf32"}[w.in_type] +
+        "dtype": {"f16": "f16", "bf16": "bf16", "f32": "tf32", "e4m3": "e4m3",
+                  "e5m2": "e5m2"}[w.in_type] +
                  ("x3" if w.compute == "3xtf32" else ""),
         "data": "synthetic",
         "config": {"workload": w.name, "m": w.m, "n": w.n, "k": w.k, "batch": w.batch,

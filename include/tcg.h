@@ -36,6 +36,10 @@
  *     16BF / 32F            / 32F or 16BF
  *     32F  / 32F_FAST_TF32  / 32F
  *     32F  / 32F_3XTF32     / 32F
+ *     8F_E4M3 or 8F_E5M2 (A and B alike) / 32F / 32F, 16F or 16BF
+ *   FP8 inputs ("NVIDIA Tensor Core混合精度计算原理与应用解析", section 4.3.1: E4M3 and
+ *   E5M2) are multiplied exactly and accumulated in FP32 like the 16-bit ones; their
+ *   leading dimensions must be multiples of 16 elements (16 bytes).
  *
  * Ownership and threading.  The caller owns every device buffer; libtcg never
  * frees or keeps them.  All calls are asynchronous on the handle's stream and
@@ -72,9 +76,11 @@ typedef enum {
 typedef enum { TCG_OP_N = 0, TCG_OP_T = 1 } tcgOp_t;
 
 typedef enum {
-    TCG_R_16F = 0,   /* IEEE binary16 */
-    TCG_R_16BF = 1,  /* bfloat16: upper 16 bits of an IEEE binary32 */
-    TCG_R_32F = 2    /* IEEE binary32 */
+    TCG_R_16F = 0,     /* IEEE binary16 */
+    TCG_R_16BF = 1,    /* bfloat16: upper 16 bits of an IEEE binary32 */
+    TCG_R_32F = 2,     /* IEEE binary32 */
+    TCG_R_8F_E4M3 = 3, /* FP8 1/4/3, bias 7, no Inf, max 448 (inputs only) */
+    TCG_R_8F_E5M2 = 4  /* FP8 1/5/2, bias 15, IEEE-style Inf/NaN (inputs only) */
 } tcgDataType_t;
 
 typedef enum {

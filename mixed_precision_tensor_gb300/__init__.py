@@ -32,7 +32,7 @@ TCG_STATUS_EXECUTION_FAILED = 5
 TCG_STATUS_TIMEOUT = 6
 TCG_STATUS_ALLOC_FAILED = 7
 TCG_OP_N, TCG_OP_T = 0, 1
-TCG_R_16F, TCG_R_16BF, TCG_R_32F = 0, 1, 2
+TCG_R_16F, TCG_R_16BF, TCG_R_32F, TCG_R_8F_E4M3, TCG_R_8F_E5M2 = 0, 1, 2, 3, 4
 TCG_COMPUTE_32F, TCG_COMPUTE_32F_FAST_TF32, TCG_COMPUTE_32F_3XTF32 = 0, 1, 2
 
 EXPORTS = ("tcg_create", "tcg_destroy", "tcg_set_stream", "tcg_set_workspace",
@@ -198,7 +198,8 @@ def dtype_code(t) -> int:
     import torch
     if not _TORCH_TYPE:
         _TORCH_TYPE.update({torch.float16: TCG_R_16F, torch.bfloat16: TCG_R_16BF,
-                            torch.float32: TCG_R_32F})
+                            torch.float32: TCG_R_32F, torch.float8_e4m3fn: TCG_R_8F_E4M3,
+                            torch.float8_e5m2: TCG_R_8F_E5M2})
     return _TORCH_TYPE[t]
 
 

@@ -74,9 +74,17 @@ struct tcgContext {
 
 namespace {
 
-int elem_size(tcgDataType_t t) { return t == TCG_R_32F ? 4 : 2; }
+int elem_size(tcgDataType_t t)
+{
+    return t == TCG_R_32F ? 4 : ((t == TCG_R_8F_E4M3 || t == TCG_R_8F_E5M2) ? 1 : 2);
+}
 
-bool valid_type(int t) { return t == TCG_R_16F || t == TCG_R_16BF || t == TCG_R_32F; }
+bool is_fp8(int t) { return t == TCG_R_8F_E4M3 || t == TCG_R_8F_E5M2; }
+
+bool valid_type(int t)
+{
+    return t == TCG_R_16F || t == TCG_R_16BF || t == TCG_R_32F || is_fp8(t);
+}
 
 int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
 
@@ -108,10 +116,13 @@ tcgStatus_t check_args(const Problem &p)
     if (p.m < 0 || p.n < 0 || p.k < 0 || p.batch < 0)
         return TCG_STATUS_INVALID_VALUE;
     // Supported (A/B, compute, C) combinations.
-    if (p.Atype != p.Btype)
+    if (p.Atype != p.Btype || is_fp8(p.Ctype))
         return TCG_STATUS_NOT_SUPPORTED;
     if (p.Atype == TCG_R_32F) {
         if (p.compute == TCG_COMPUTE_32F || p.Ctype != TCG_R_32F)
+            return TCG_STATUS_NOT_SUPPORTED;
+    } else if (is_fp8(p.Atype)) {
+        if (p.compute != TCG_COMPUTE_32F)       // FP32, FP16 or BF16 output
             return TCG_STATUS_NOT_SUPPORTED;
     } else {
         if (p.compute != TCG_COMPUTE_32F)
@@ -201,6 +212,8 @@ CUtensorMapDataType map_type(tcgDataType_t t)
     switch (t) {
     case TCG_R_16F: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     case TCG_R_16BF: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    case TCG_R_8F_E4M3:
+    case TCG_R_8F_E5M2: return CU_TENSOR_MAP_DATA_TYPE_UINT8;   // raw bytes
     default: return CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     }
 }
@@ -421,6 +434,7 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
     }
 
     const int cg = h->cta_group;
+    const bool fp8 = is_fp8(p.Atype);
     const tcgDataType_t at = tf32 ? TCG_R_32F : p.Atype;
     CUtensorMap tmD;
     st = output_map(h, p.C, p.Ctype, p.m, p.n, p.ldc, strideC, p.batch, &tmD);
@@ -436,13 +450,18 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
         a.m = m; a.n = n; a.k = k; a.batch = batch;
         a.num_m_tiles = (m + kBM * cg - 1) / (kBM * cg);
         a.num_n_tiles = (n + kBN - 1) / kBN;
-        a.k_per_block = tf32 ? 32 : 64;
+        const int es = elem_size(at);
+        a.k_per_block = 128 / es;                     // one 128-byte swizzle row of K
         a.num_k_blocks = (k + a.k_per_block - 1) / a.k_per_block;
         a.total_tiles = a.num_m_tiles * a.num_n_tiles * batch;
         a.group_m = h->group_m > 0 ? h->group_m : 8;
-        a.is_tf32 = tf32 ? 1 : 0;
-        a.mn_box = tf32 ? 32 : 64;
-        const uint32_t fmt = tf32 ? 2u : (p.Atype == TCG_R_16BF ? 1u : 0u);
+        a.kind = tf32 ? kKindTF32 : (fp8 ? kKindF8 : kKindF16);
+        a.mn_box = 128 / es;
+        // operand format codes: kind::f16 F16 = 0, BF16 = 1; kind::tf32 TF32 = 2;
+        // kind::f8f6f4 E4M3 = 0, E5M2 = 1
+        const uint32_t fmt = tf32 ? 2u
+                                  : (fp8 ? (p.Atype == TCG_R_8F_E5M2 ? 1u : 0u)
+                                         : (p.Atype == TCG_R_16BF ? 1u : 0u));
         a.idesc = (1u << 4)                               // D: FP32
                   | (fmt << 7) | (fmt << 10)              // A, B formats
                   | ((a_kmajor ? 0u : 1u) << 15)          // A: 0 = K-major, 1 = M-major
@@ -783,7 +802,7 @@ extern "C" tcgStatus_t tcg_gemm_tf32_noalloc(void *stream, tcgOp_t transa, tcgOp
     a.num_k_blocks = static_cast<int>((k + 31) / 32);
     a.total_tiles = a.num_m_tiles * a.num_n_tiles;
     a.group_m = 8;
-    a.is_tf32 = 1;
+    a.kind = kKindTF32;
     a.mn_box = 32;
     a.idesc = (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(kBN >> 3) << 17) |
               (static_cast<uint32_t>((kBM * cg) >> 4) << 24);

@@ -52,6 +52,11 @@ constexpr uint32_t kErrDrain = 16u;      // end-of-kernel drain
 
 enum OutKind { kOutF32 = 0, kOutF16 = 1, kOutBF16 = 2 };
 
+// MMA kind (operand formats): kind::f16 (FP16/BF16, K = 16 per instruction),
+// kind::tf32 (K = 8), kind::f8f6f4 with E4M3/E5M2 (K = 32).  Every kind reads 32 bytes
+// of K per instruction.
+enum MmaKind { kKindF16 = 0, kKindTF32 = 1, kKindF8 = 2 };
+
 // How an operand tile sits in global and shared memory.
 //   kK:        K contiguous.  3-D map {K, rows, batch}; shared tile = rows of 128 B
 //              along K, 8-row groups 1 KiB apart.
@@ -73,9 +78,9 @@ struct GemmArgs {
     int group_m;               // tile rasterisation: group of m-tiles walked together
     int a_mode, b_mode;        // OperandMode of A and B
     int a_bcast, b_bcast;      // batch stride 0: always batch coordinate 0
-    int is_tf32;               // kind::tf32 (else kind::f16)
-    int k_per_block;           // K elements per stage: 64 (16-bit) or 32 (TF32)
-    int mn_box;                // M/N elements per 128-byte run: 64 or 32
+    int kind;                  // MmaKind
+    int k_per_block;           // K elements per stage (128 bytes): 64, 32 (TF32), 128 (FP8)
+    int mn_box;                // M/N elements per 128-byte run: 64, 32 (TF32), 128 (FP8)
     uint32_t idesc;            // tcgen05 instruction descriptor
     float alpha, beta;
     const void *C;

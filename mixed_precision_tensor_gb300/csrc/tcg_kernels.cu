@@ -149,7 +149,7 @@ __device__ __forceinline__ float load_c(const void *C, int64_t idx)
 // and signal the even CTA's "full" barrier, the MMA completion is multicast to both
 // CTAs' "empty" and "accumulator full" barriers, and both CTAs' epilogues report to the
 // even CTA's "accumulator empty" barrier.
-template <int OUT, int CG, bool TF32, bool BETA>
+template <int OUT, int CG, int KIND, bool BETA>
 __global__ void __launch_bounds__(kThreads, 1)
     tcg_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // descriptor strides, per operand majorness.  The MMA kind is a template argument:
     // the issuing thread's loop must stay branch-free, as its instruction rate is what
     // keeps the tensor core fed.
-    constexpr uint32_t kEsize = TF32 ? 4u : 2u;
+    constexpr uint32_t kEsize = KIND == kKindTF32 ? 4u : (KIND == kKindF8 ? 1u : 2u);
     constexpr uint32_t kKmma = 32u / kEsize;                  // K per MMA instruction
     constexpr int kMmasPerStage = kRowBytes / 32;             // 4
     const uint32_t chunk_bytes = static_cast<uint32_t>(p.k_per_block) * kRowBytes;
@@ -353,13 +353,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t bd = bd_s + ((kk * b_kstep) >> 4);
                         const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
                         if constexpr (CG == 2) {
-                            if constexpr (TF32)
+                            if constexpr (KIND == kKindTF32)
                                 mma_tf32_pair(d_tmem, ad, bd, p.idesc, accum);
+                            else if constexpr (KIND == kKindF8)
+                                mma_f8_pair(d_tmem, ad, bd, p.idesc, accum);
                             else
                                 mma_f16_pair(d_tmem, ad, bd, p.idesc, accum);
                         } else {
-                            if constexpr (TF32)
+                            if constexpr (KIND == kKindTF32)
                                 mma_tf32(d_tmem, ad, bd, p.idesc, accum);
+                            else if constexpr (KIND == kKindF8)
+                                mma_f8(d_tmem, ad, bd, p.idesc, accum);
                             else
                                 mma_f16(d_tmem, ad, bd, p.idesc, accum);
                         }
@@ -645,22 +649,29 @@ typedef void (*GemmKernelFn)(const CUtensorMap, const CUtensorMap, const CUtenso
                              const GemmArgs);
 
 template <int CG, bool BETA>
-static GemmKernelFn gemm_fn_cg(int out_kind, bool tf32)
+static GemmKernelFn gemm_fn_cg(int out_kind, int kind)
 {
-    if (tf32)   // TF32 inputs always produce FP32 output
-        return tcg_gemm_kernel<kOutF32, CG, true, BETA>;
+    if (kind == kKindTF32)   // TF32 inputs always produce FP32 output
+        return tcg_gemm_kernel<kOutF32, CG, kKindTF32, BETA>;
+    if (kind == kKindF8) {
+        switch (out_kind) {
+        case kOutF32: return tcg_gemm_kernel<kOutF32, CG, kKindF8, BETA>;
+        case kOutF16: return tcg_gemm_kernel<kOutF16, CG, kKindF8, BETA>;
+        default: return tcg_gemm_kernel<kOutBF16, CG, kKindF8, BETA>;
+        }
+    }
     switch (out_kind) {
-    case kOutF32: return tcg_gemm_kernel<kOutF32, CG, false, BETA>;
-    case kOutF16: return tcg_gemm_kernel<kOutF16, CG, false, BETA>;
-    default: return tcg_gemm_kernel<kOutBF16, CG, false, BETA>;
+    case kOutF32: return tcg_gemm_kernel<kOutF32, CG, kKindF16, BETA>;
+    case kOutF16: return tcg_gemm_kernel<kOutF16, CG, kKindF16, BETA>;
+    default: return tcg_gemm_kernel<kOutBF16, CG, kKindF16, BETA>;
     }
 }
 
-static GemmKernelFn gemm_fn(int out_kind, int cta_group, bool tf32, bool beta)
+static GemmKernelFn gemm_fn(int out_kind, int cta_group, int kind, bool beta)
 {
     if (cta_group == 2)
-        return beta ? gemm_fn_cg<2, true>(out_kind, tf32) : gemm_fn_cg<2, false>(out_kind, tf32);
-    return beta ? gemm_fn_cg<1, true>(out_kind, tf32) : gemm_fn_cg<1, false>(out_kind, tf32);
+        return beta ? gemm_fn_cg<2, true>(out_kind, kind) : gemm_fn_cg<2, false>(out_kind, kind);
+    return beta ? gemm_fn_cg<1, true>(out_kind, kind) : gemm_fn_cg<1, false>(out_kind, kind);
 }
 
 static cudaError_t prepare(GemmKernelFn fn)
@@ -672,7 +683,7 @@ static cudaError_t prepare(GemmKernelFn fn)
 
 int gemm_max_resident_ctas(int cta_group, int num_sms)
 {
-    GemmKernelFn fn = gemm_fn(kOutF32, cta_group, false, false);
+    GemmKernelFn fn = gemm_fn(kOutF32, cta_group, kKindF16, false);
     if (prepare(fn) != cudaSuccess) {
         cudaGetLastError();
         return num_sms / cta_group * cta_group;
@@ -839,7 +850,7 @@ cudaError_t launch_tf32_transpose_round(const void *in, int64_t ld, int64_t stri
 cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmD,
                         const GemmArgs &a, int out_kind, int cta_group, int grid, cudaStream_t s)
 {
-    GemmKernelFn fn = gemm_fn(out_kind, cta_group, a.is_tf32 != 0, a.beta != 0.0f);
+    GemmKernelFn fn = gemm_fn(out_kind, cta_group, a.kind, a.beta != 0.0f);
     cudaError_t e = prepare(fn);
     if (e != cudaSuccess)
         return e;

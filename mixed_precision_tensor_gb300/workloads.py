@@ -10,6 +10,7 @@ numpy (FP16) or torch (BF16) round-to-nearest-even casts.
 Storage conventions of the returned arrays:
   * FP16 -> numpy float16
   * BF16 -> numpy uint16 holding the bfloat16 bit pattern
+  * FP8 (E4M3 / E5M2) -> numpy uint8 holding the bit pattern (torch casts)
   * FP32 -> numpy float32
 """
 from __future__ import annotations
@@ -25,7 +26,7 @@ class Workload:
     m: int
     n: int
     k: int
-    in_type: str        # "f16" | "bf16" | "f32" (f32 means TF32 compute)
+    in_type: str        # "f16" | "bf16" | "e4m3" | "e5m2" | "f32" (f32 means TF32 compute)
     out_type: str       # "f32" | "f16" | "bf16"
     alpha: float
     beta: float
@@ -40,7 +41,7 @@ class Workload:
 
     def algorithmic_bytes(self) -> int:
         """A and B read once, C read once when beta != 0, D written once."""
-        ein = {"f16": 2, "bf16": 2, "f32": 4}[self.in_type]
+        ein = {"f16": 2, "bf16": 2, "f32": 4, "e4m3": 1, "e5m2": 1}[self.in_type]
         eout = {"f16": 2, "bf16": 2, "f32": 4}[self.out_type]
         per = (self.m * self.k + self.k * self.n) * ein + self.m * self.n * eout
         if self.beta != 0.0:
@@ -60,7 +61,10 @@ WORKLOADS = {
                                           "f32", "f32", 1.0, 0.0, 1, 3, "uniform"),
     "fp16_batched_512x256": Workload("fp16_batched_512x256", 256, 256, 256, "f16", "f16", 1.0,
                                      0.5, 512, 4, "pow2"),
-    # not one of the five above: the multi-word (3xTF32) variant of the TF32 workload
+    # not one of the five above: FP8 inputs on the headline shape, and the multi-word
+    # (3xTF32) variant of the TF32 workload
+    "fp8e4m3_gemm_8192": Workload("fp8e4m3_gemm_8192", 8192, 8192, 8192, "e4m3", "f32", 1.0,
+                                  0.0, 1, 1, "uniform"),
     "fp32_3xtf32_4096x4096x16384": Workload("fp32_3xtf32_4096x4096x16384", 4096, 4096, 16384,
                                             "f32", "f32", 1.0, 0.0, 1, 3, "uniform",
                                             "3xtf32"),
@@ -86,7 +90,16 @@ def _to_bf16_bits(x32: np.ndarray) -> np.ndarray:
     return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
 
 
+def _to_fp8_bits(x32: np.ndarray, t: str) -> np.ndarray:
+    import torch
+    dt = torch.float8_e4m3fn if t == "e4m3" else torch.float8_e5m2
+    tt = torch.from_numpy(np.ascontiguousarray(x32, dtype=np.float32))
+    return tt.to(dt).view(torch.uint8).numpy()
+
+
 def _to_storage(x: np.ndarray, t: str) -> np.ndarray:
+    if t in ("e4m3", "e5m2"):
+        return _to_fp8_bits(x.astype(np.float32), t)
     if t == "f16":
         return x.astype(np.float32).astype(np.float16)
     if t == "bf16":

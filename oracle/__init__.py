@@ -31,7 +31,7 @@ _SRC = os.path.join(_HERE, "tcg_oracle.c")
 _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
 
-F16, BF16, F32 = 0, 1, 2
+F16, BF16, F32, F8E4M3, F8E5M2 = 0, 1, 2, 3, 4
 OP_N, OP_T = 0, 1
 
 _lock = threading.Lock()
@@ -64,6 +64,7 @@ def _load():
                                  dbl, vp, ci, i64, ci, i64, i64, i64, i64, vp, i64,
                                  vp, vp, ci]
         for name in ("orc_f16_to_f64_array", "orc_bf16_to_f64_array",
+                     "orc_f8e4m3_to_f64_array", "orc_f8e5m2_to_f64_array",
                      "orc_tf32_round_bits_array", "orc_f64_to_f16_array",
                      "orc_f64_to_bf16_array", "orc_f64_to_f32_array"):
             fn = getattr(lib, name)
@@ -100,6 +101,14 @@ def bf16_to_f64(bits):
     return _array_call("orc_bf16_to_f64_array", np.asarray(bits, dtype=np.uint16), np.float64)
 
 
+def f8e4m3_to_f64(bits):
+    return _array_call("orc_f8e4m3_to_f64_array", np.asarray(bits, dtype=np.uint8), np.float64)
+
+
+def f8e5m2_to_f64(bits):
+    return _array_call("orc_f8e5m2_to_f64_array", np.asarray(bits, dtype=np.uint8), np.float64)
+
+
 def tf32_round_bits(bits):
     return _array_call("orc_tf32_round_bits_array", np.asarray(bits, dtype=np.uint32), np.uint32)
 
@@ -116,7 +125,8 @@ def f64_to_f32(x):
     return _array_call("orc_f64_to_f32_array", np.asarray(x, dtype=np.float64), np.float32)
 
 
-_ELEM_DTYPE = {F16: np.uint16, BF16: np.uint16, F32: np.float32}
+_ELEM_DTYPE = {F16: np.uint16, BF16: np.uint16, F32: np.float32, F8E4M3: np.uint8,
+               F8E5M2: np.uint8}
 
 
 def gemm(transa, transb, m, n, k, alpha, A, atype, lda, B, btype, ldb, beta, C, ctype,
@@ -125,7 +135,8 @@ def gemm(transa, transb, m, n, k, alpha, A, atype, lda, B, btype, ldb, beta, C, 
     """Block of D = alpha*op(A)*op(B) + beta*C (column-major, BLAS arguments).
 
     ``A``, ``B``, ``C`` are flat numpy arrays holding the raw storage (FP16/BF16
-    as uint16 bit patterns, FP32 as float32); ``C`` may be None when beta == 0.
+    as uint16 bit patterns, FP8 as uint8 bit patterns, FP32 as float32); ``C`` may be
+    None when beta == 0.
     ``rows=(i0, i1)``, ``cols=(j0, j1)`` select the block of D to compute.
     Returns ``(D, R, absAB)``: D as a (i1-i0, j1-j0) array in the output storage
     type, R = alpha*S + beta*C in FP64 and absAB = sum_p |a_ip||b_pj|, or None

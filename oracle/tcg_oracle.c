@@ -34,6 +34,12 @@
  *  - BF16: 1 sign, 8 exponent, 7 mantissa bits, bias 127 (the upper half of an
  *    IEEE binary32; the pages name the type without defining it).
  *  - FP32: IEEE binary32.
+ *  - FP8 E4M3: 1 sign, 4 exponent, 3 mantissa bits, bias 7, subnormals, no
+ *    infinities, S.1111.111 is NaN (largest finite 448); FP8 E5M2: 1 sign, 5
+ *    exponent, 2 mantissa bits, bias 15, subnormals, IEEE-style Inf/NaN ("NVIDIA
+ *    Tensor Core混合精度计算原理与应用解析", section 4.3.1: the two FP8 formats, E4M3
+ *    with the smaller range and higher precision, E5M2 the other way round; the
+ *    pages give no bit layouts, these are the standard ones).
  */
 #include <math.h>
 #include <fenv.h>
@@ -42,7 +48,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_F32 = 2 };
+enum { ORC_F16 = 0, ORC_BF16 = 1, ORC_F32 = 2, ORC_F8E4M3 = 3, ORC_F8E5M2 = 4 };
 enum { ORC_OP_N = 0, ORC_OP_T = 1 };
 
 /* ------------------------------------------------------------------------ */
@@ -76,6 +82,36 @@ double orc_bf16_to_f64(uint16_t b)
         v = ldexp((double)f, -133);             /* f * 2^-126 * 2^-7 */
     else
         v = ldexp((double)(128 + f), e - 134);  /* (1 + f/128) * 2^(e-127) */
+    return sign ? -v : v;
+}
+
+double orc_f8e4m3_to_f64(uint8_t b)
+{
+    int sign = (b >> 7) & 1;
+    int e = (b >> 3) & 0xF;
+    int f = b & 0x7;
+    double v;
+    if (e == 0xF && f == 0x7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)f, -9);               /* f * 2^-6 * 2^-3 */
+    else
+        v = ldexp((double)(8 + f), e - 10);     /* (1 + f/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+double orc_f8e5m2_to_f64(uint8_t b)
+{
+    int sign = (b >> 7) & 1;
+    int e = (b >> 2) & 0x1F;
+    int f = b & 0x3;
+    double v;
+    if (e == 0x1F)
+        v = f ? NAN : INFINITY;
+    else if (e == 0)
+        v = ldexp((double)f, -16);              /* f * 2^-14 * 2^-2 */
+    else
+        v = ldexp((double)(4 + f), e - 17);     /* (1 + f/4) * 2^(e-15) */
     return sign ? -v : v;
 }
 
@@ -171,6 +207,10 @@ static double load_elem(const void *base, int type, int64_t idx, int tf32)
         return orc_f16_to_f64(((const uint16_t *)base)[idx]);
     case ORC_BF16:
         return orc_bf16_to_f64(((const uint16_t *)base)[idx]);
+    case ORC_F8E4M3:
+        return orc_f8e4m3_to_f64(((const uint8_t *)base)[idx]);
+    case ORC_F8E5M2:
+        return orc_f8e5m2_to_f64(((const uint8_t *)base)[idx]);
     default: {
         uint32_t u = ((const uint32_t *)base)[idx];
         return orc_f32_to_f64(tf32 ? orc_tf32_round_bits(u) : u);
@@ -335,6 +375,14 @@ void orc_f16_to_f64_array(const uint16_t *in, double *out, int64_t n)
 void orc_bf16_to_f64_array(const uint16_t *in, double *out, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i) out[i] = orc_bf16_to_f64(in[i]);
+}
+void orc_f8e4m3_to_f64_array(const uint8_t *in, double *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_f8e4m3_to_f64(in[i]);
+}
+void orc_f8e5m2_to_f64_array(const uint8_t *in, double *out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_f8e5m2_to_f64(in[i]);
 }
 void orc_tf32_round_bits_array(const uint32_t *in, uint32_t *out, int64_t n)
 {

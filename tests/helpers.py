@@ -12,7 +12,8 @@ import oracle
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
-TYPE_CODE = {"f16": oracle.F16, "bf16": oracle.BF16, "f32": oracle.F32}
+TYPE_CODE = {"f16": oracle.F16, "bf16": oracle.BF16, "f32": oracle.F32,
+             "e4m3": oracle.F8E4M3, "e5m2": oracle.F8E5M2}
 
 
 def raw(x: np.ndarray) -> np.ndarray:

@@ -54,6 +54,7 @@ def handle(lib):
 # anything dereferences them.
 PA, PB, PC = 0x10000, 0x20000, 0x30000
 F16, BF16, F32 = tcg.TCG_R_16F, tcg.TCG_R_16BF, tcg.TCG_R_32F
+E4M3, E5M2 = tcg.TCG_R_8F_E4M3, tcg.TCG_R_8F_E5M2
 N, T = tcg.TCG_OP_N, tcg.TCG_OP_T
 C32, TF32, SPLIT3 = (tcg.TCG_COMPUTE_32F, tcg.TCG_COMPUTE_32F_FAST_TF32,
                      tcg.TCG_COMPUTE_32F_3XTF32)
@@ -87,6 +88,10 @@ def gemm(h, transa=N, transb=N, m=64, n=64, k=64, alpha=1.0, A=PA, at=F16, lda=6
     (dict(at=F16, bt=F16, comp=TF32), NSUP),
     (dict(at=F16, bt=F16, ct=BF16), NSUP),    # 16-bit output must match the input type
     (dict(at=F16, bt=F16, comp=SPLIT3), NSUP),                       # split needs FP32 inputs
+    (dict(at=E4M3, bt=E5M2), NSUP),                                  # FP8 A and B alike
+    (dict(at=E4M3, bt=E4M3, ct=E4M3, ldc=64), NSUP),                 # FP8 is input-only
+    (dict(at=E4M3, bt=E4M3, comp=TF32), NSUP),
+    (dict(at=E5M2, bt=E5M2, lda=72), INV),                           # 72 bytes: not 16-byte
     (dict(at=F32, bt=F32, comp=SPLIT3, ct=F16, ldc=64), NSUP),      # and FP32 output
 ])
 def test_argument_checks(handle, kw, status):

@@ -22,8 +22,9 @@ from mixed_precision_tensor_gb300 import workloads as wl
 pytestmark = pytest.mark.gpu
 
 N, T = tcg.TCG_OP_N, tcg.TCG_OP_T
-CODE = {"f16": tcg.TCG_R_16F, "bf16": tcg.TCG_R_16BF, "f32": tcg.TCG_R_32F}
-ESIZE = {"f16": 2, "bf16": 2, "f32": 4}
+CODE = {"f16": tcg.TCG_R_16F, "bf16": tcg.TCG_R_16BF, "f32": tcg.TCG_R_32F,
+        "e4m3": tcg.TCG_R_8F_E4M3, "e5m2": tcg.TCG_R_8F_E5M2}
+ESIZE = {"f16": 2, "bf16": 2, "f32": 4, "e4m3": 1, "e5m2": 1}
 
 
 @pytest.fixture(scope="module")
@@ -43,6 +44,9 @@ def any_handle(cuda_device, request):
 
 
 def _to_storage(x64, t):
+    if t in ("e4m3", "e5m2"):
+        dt = torch.float8_e4m3fn if t == "e4m3" else torch.float8_e5m2
+        return torch.from_numpy(x64.astype(np.float32)).to(dt).view(torch.uint8).numpy()
     if t == "f16":
         return x64.astype(np.float32).astype(np.float16).view(np.uint16)
     if t == "bf16":
@@ -263,6 +267,35 @@ def test_split3_batched_and_integer_exact(any_handle):
     assert guards
     for got, D, R, AB, cdec in res:
         assert values_equal(got.astype(np.float64), R)
+
+
+FP8_SHAPES = [(1, 1, 1), (7, 17, 15), (129, 255, 257), (256, 384, 1000), (1000, 300, 129)]
+
+
+@pytest.mark.parametrize("m,n,k", FP8_SHAPES)
+@pytest.mark.parametrize("in_t", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("out_t", ["f32", "f16", "bf16"])
+def test_fp8_ragged(any_handle, m, n, k, in_t, out_t):
+    """FP8 (E4M3 / E5M2) inputs, exact products, FP32 accumulation: bit-exact on integer
+    data, within the bound on random data."""
+    res, guards = run_colmajor(any_handle, N, N, m, n, k, 1.0, 1.0, in_t, out_t,
+                               seed=m + 3 * n + k, dist="integer")
+    assert guards
+    _assert_results(res, k, 1.0, 1.0, out_t, exact=True)
+    res, guards = run_colmajor(any_handle, N, N, m, n, k, 0.5, -1.0, in_t, out_t,
+                               seed=5 + m + n + k, dist="uniform", extra_ld=1)
+    assert guards
+    _assert_results(res, k, 0.5, -1.0, out_t, exact=False)
+
+
+@pytest.mark.parametrize("m,n,k", [(256, 512, 320), (384, 128, 64), (300, 520, 200)])
+@pytest.mark.parametrize("transa,transb", [(N, N), (T, N), (N, T), (T, T)])
+@pytest.mark.parametrize("in_t", ["e4m3", "e5m2"])
+def test_fp8_op_combinations(any_handle, m, n, k, transa, transb, in_t):
+    res, guards = run_colmajor(any_handle, transa, transb, m, n, k, 1.0, 1.0, in_t, "f32",
+                               seed=11 + m + transa + 2 * transb, dist="integer", batch=2)
+    assert guards
+    _assert_results(res, k, 1.0, 1.0, "f32", exact=True)
 
 
 def test_degenerate_cases(handle):

@@ -38,6 +38,27 @@ def test_bf16_decode_all_patterns_match_torch():
     assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
 
 
+@pytest.mark.parametrize("name,fn,tdt", [("e4m3", "f8e4m3_to_f64", "float8_e4m3fn"),
+                                         ("e5m2", "f8e5m2_to_f64", "float8_e5m2")])
+def test_f8_decode_all_patterns_match_torch(name, fn, tdt):
+    bits = np.arange(256, dtype=np.uint8)
+    got = getattr(oracle, fn)(bits)
+    want = torch.from_numpy(bits).view(getattr(torch, tdt)).to(torch.float64).numpy()
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+
+
+def test_f8_closed_forms():
+    e4 = oracle.f8e4m3_to_f64(np.array([0x7E, 0x01, 0x08, 0x38, 0xFE, 0x7F], dtype=np.uint8))
+    assert e4[0] == 448.0 and e4[1] == 2.0 ** -9 and e4[2] == 2.0 ** -6 and e4[3] == 1.0
+    assert e4[4] == -448.0 and np.isnan(e4[5])
+    e5 = oracle.f8e5m2_to_f64(np.array([0x7B, 0x01, 0x3C, 0x7C, 0x7D], dtype=np.uint8))
+    assert e5[0] == 57344.0 and e5[1] == 2.0 ** -16 and e5[2] == 1.0
+    assert e5[3] == np.inf and np.isnan(e5[4])
+
+
 def _f16_edge_values():
     h = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16).view(np.float16)
     v = h.astype(np.float64)

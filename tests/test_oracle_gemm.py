@@ -20,6 +20,10 @@ from mixed_precision_tensor_gb300 import workloads as wl
 
 def _store(x64, t):
     """FP64 values that are exact in type t -> raw storage array."""
+    if t in ("e4m3", "e5m2"):
+        import torch
+        dt = torch.float8_e4m3fn if t == "e4m3" else torch.float8_e5m2
+        return torch.from_numpy(np.asarray(x64, dtype=np.float32)).to(dt).view(torch.uint8).numpy()
     if t == "f16":
         return x64.astype(np.float16).view(np.uint16)
     if t == "bf16":
@@ -86,7 +90,7 @@ def test_identity_gives_rounded_alpha_b_plus_beta_c(out):
 
 @pytest.mark.parametrize("transa", [oracle.OP_N, oracle.OP_T])
 @pytest.mark.parametrize("transb", [oracle.OP_N, oracle.OP_T])
-@pytest.mark.parametrize("t", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("t", ["f16", "bf16", "f32", "e4m3", "e5m2"])
 def test_small_integers_exact_against_int64_matmul(transa, transb, t):
     rng = np.random.default_rng(12 + 2 * transa + transb)
     m, n, k = 37, 29, 53
