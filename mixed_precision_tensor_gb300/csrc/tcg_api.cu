@@ -261,11 +261,11 @@ tcgStatus_t get_map(tcgContext *h, const void *ptr, tcgDataType_t t, int rank,
 }
 
 // Map for one operand as the kernel loads it (see OperandMode).  rows = M (for A) or
-// N (for B); box_rows = the rows one CTA loads per stage (128 for A; 256 or 128 for B).
+// N (for B); box_rows = the rows one CTA loads per stage (128 for A; 256 or 128 for B);
+// k_row = K elements per 128-byte row.
 tcgStatus_t operand_map(tcgContext *h, const void *ptr, tcgDataType_t t, bool kmajor,
                         int64_t rows, int64_t k, int64_t ld, int64_t stride, int64_t batch,
-                        int box_rows, int k_per_block, int mn_box, bool *bcast, int *mode,
-                        CUtensorMap *out)
+                        int box_rows, int k_row, bool *bcast, int *mode, CUtensorMap *out)
 {
     const int es = elem_size(t);
     const bool bc = (batch > 1 && stride == 0);
@@ -282,27 +282,15 @@ tcgStatus_t operand_map(tcgContext *h, const void *ptr, tcgDataType_t t, bool km
         *mode = kK;
         const uint64_t dims[3] = {static_cast<uint64_t>(k), static_cast<uint64_t>(rows), nb};
         const uint64_t str[2] = {ldb, bstride};
-        const uint32_t box[3] = {static_cast<uint32_t>(k_per_block),
-                                 static_cast<uint32_t>(box_rows), 1};
+        const uint32_t box[3] = {static_cast<uint32_t>(k_row), static_cast<uint32_t>(box_rows),
+                                 1};
         return get_map(h, ptr, t, 3, dims, str, box, out);
     }
-    const int64_t c = 128 / es;                 // elements per 128-byte chunk
-    if (rows % c == 0 && k % 8 == 0) {
-        // Element (r, p) = (c*c2 + c0, 8*c3 + c1): every coordinate TMA accepts maps
-        // inside the matrix, so zero fill covers exactly the ragged K tail.
-        *mode = kMNInter;
-        const uint64_t dims[5] = {static_cast<uint64_t>(c), 8, static_cast<uint64_t>(rows / c),
-                                  static_cast<uint64_t>(k / 8), nb};
-        const uint64_t str[4] = {ldb, 128ull, 8ull * ldb, bstride};
-        const uint32_t box[5] = {static_cast<uint32_t>(c), 8,
-                                 static_cast<uint32_t>(box_rows / c),
-                                 static_cast<uint32_t>(k_per_block / 8), 1};
-        return get_map(h, ptr, t, 5, dims, str, box, out);
-    }
-    *mode = kMNChunk;
+    // M/N-major: one box = one 128-byte chunk of rows over a stage's kDepth K rows.
+    *mode = kMN;
     const uint64_t dims[3] = {static_cast<uint64_t>(rows), static_cast<uint64_t>(k), nb};
     const uint64_t str[2] = {ldb, bstride};
-    const uint32_t box[3] = {static_cast<uint32_t>(mn_box), static_cast<uint32_t>(k_per_block),
+    const uint32_t box[3] = {static_cast<uint32_t>(128 / es), static_cast<uint32_t>(kDepth * k_row),
                              1};
     return get_map(h, ptr, t, 3, dims, str, box, out);
 }
@@ -451,12 +439,11 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
         a.num_m_tiles = (m + kBM * cg - 1) / (kBM * cg);
         a.num_n_tiles = (n + kBN - 1) / kBN;
         const int es = elem_size(at);
-        a.k_per_block = 128 / es;                     // one 128-byte swizzle row of K
-        a.num_k_blocks = (k + a.k_per_block - 1) / a.k_per_block;
+        a.k_row = 128 / es;                           // one 128-byte swizzle row of K
+        a.num_k_blocks = (k + kDepth * a.k_row - 1) / (kDepth * a.k_row);
         a.total_tiles = a.num_m_tiles * a.num_n_tiles * batch;
         a.group_m = h->group_m > 0 ? h->group_m : 8;
         a.kind = tf32 ? kKindTF32 : (fp8 ? kKindF8 : kKindF16);
-        a.mn_box = 128 / es;
         // operand format codes: kind::f16 F16 = 0, BF16 = 1; kind::tf32 TF32 = 2;
         // kind::f8f6f4 E4M3 = 0, E5M2 = 1
         const uint32_t fmt = tf32 ? 2u
@@ -470,6 +457,10 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
                   | (static_cast<uint32_t>((kBM * cg) >> 4) << 24);   // M = 128 or 256
         a.alpha = p.alpha;
         a.beta = beta;
+        // Four C buffers (one operand stage less) when the epilogue's C/D traffic
+        // outweighs the main loop: K bytes per row <= 1024 x D's element size.
+        a.c_bufs = beta == 0.0f ? 0
+                 : (cg == 2 && k * es <= 1024 * elem_size(p.Ctype) ? 4 : 2);
         a.C = p.C;
         a.D = p.C;
         a.ldc = p.ldc;
@@ -480,11 +471,11 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
         CUtensorMap tmA, tmB;
         bool abc = false, bbc = false;
         tcgStatus_t s2 = operand_map(h, opA, at, a_kmajor, p.m, p.k, lda, sA, p.batch, kBM,
-                                     a.k_per_block, a.mn_box, &abc, &a.a_mode, &tmA);
+                                     a.k_row, &abc, &a.a_mode, &tmA);
         if (s2 != TCG_STATUS_SUCCESS)
             return s2;
-        s2 = operand_map(h, opB, at, b_kmajor, p.n, p.k, ldb, sB, p.batch, kBN / cg,
-                         a.k_per_block, a.mn_box, &bbc, &a.b_mode, &tmB);
+        s2 = operand_map(h, opB, at, b_kmajor, p.n, p.k, ldb, sB, p.batch, kBN / cg, a.k_row,
+                         &bbc, &a.b_mode, &tmB);
         if (s2 != TCG_STATUS_SUCCESS)
             return s2;
         a.a_bcast = abc ? 1 : 0;
@@ -798,16 +789,16 @@ extern "C" tcgStatus_t tcg_gemm_tf32_noalloc(void *stream, tcgOp_t transa, tcgOp
     a.m = static_cast<int>(m); a.n = static_cast<int>(n); a.k = static_cast<int>(k); a.batch = 1;
     a.num_m_tiles = static_cast<int>((m + kBM * cg - 1) / (kBM * cg));
     a.num_n_tiles = static_cast<int>((n + kBN - 1) / kBN);
-    a.k_per_block = 32;
-    a.num_k_blocks = static_cast<int>((k + 31) / 32);
+    a.k_row = 32;
+    a.num_k_blocks = static_cast<int>((k + kDepth * 32 - 1) / (kDepth * 32));
     a.total_tiles = a.num_m_tiles * a.num_n_tiles;
     a.group_m = 8;
     a.kind = kKindTF32;
-    a.mn_box = 32;
     a.idesc = (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(kBN >> 3) << 17) |
               (static_cast<uint32_t>((kBM * cg) >> 4) << 24);
     a.alpha = alpha;
     a.beta = beta;
+    a.c_bufs = beta == 0.0f ? 0 : (k * 4 <= 1024 * 4 ? 4 : 2);
     a.C = C;
     a.D = C;
     a.ldc = ldc;
@@ -816,11 +807,11 @@ extern "C" tcgStatus_t tcg_gemm_tf32_noalloc(void *stream, tcgOp_t transa, tcgOp
     a.wait_limit_ns = kDefaultWaitNs;
     CUtensorMap tmA, tmB;
     bool bca = false, bcb = false;
-    st = operand_map(&ctx, Ak, TCG_R_32F, true, m, k, kp, m * kp, 1, kBM, a.k_per_block, a.mn_box,
-                     &bca, &a.a_mode, &tmA);
+    st = operand_map(&ctx, Ak, TCG_R_32F, true, m, k, kp, m * kp, 1, kBM, a.k_row, &bca,
+                     &a.a_mode, &tmA);
     if (st == TCG_STATUS_SUCCESS)
-        st = operand_map(&ctx, Bk, TCG_R_32F, true, n, k, kp, n * kp, 1, kBN / cg, a.k_per_block,
-                         a.mn_box, &bcb, &a.b_mode, &tmB);
+        st = operand_map(&ctx, Bk, TCG_R_32F, true, n, k, kp, n * kp, 1, kBN / cg, a.k_row, &bcb,
+                         &a.b_mode, &tmB);
     if (st != TCG_STATUS_SUCCESS)
         return st;
     CUtensorMap tmD;

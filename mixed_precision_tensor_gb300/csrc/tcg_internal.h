@@ -13,17 +13,20 @@ namespace tcg {
 // 128 x 256 and the CTA holds all 256 rows of B.
 constexpr int kBM = 128;               // rows of D per CTA (MMA M per CTA, TMEM lanes)
 constexpr int kBN = 256;               // columns of D per tile (MMA N, TMEM columns)
-constexpr int kRowBytes = 128;         // one 128-byte swizzle row of K per stage
-constexpr int kABytes = kBM * kRowBytes;           // 16 KiB per stage
+constexpr int kRowBytes = 128;         // one 128-byte swizzle row of K
+constexpr int kDepth = 2;              // 128-byte K rows per operand row and stage
+constexpr int kABytes = kBM * kRowBytes;           // 16 KiB: A for one K row
 constexpr int kAccBufs = 2;            // TMEM accumulator double buffer
 constexpr int kTmemCols = kAccBufs * kBN;          // 512 columns = all of TMEM
 constexpr int kEpiWarps = 8;           // two warps per TMEM lane quarter
 constexpr int kThreads = 32 * (2 + kEpiWarps);     // producer, MMA, 8 epilogue warps
 // Shared memory: operand ring + epilogue staging = kDataBytes.  Epilogue staging: each
-// half of the epilogue (4 warps, 128 rows) owns kEpiBufs buffers of one 128-row chunk
-// of D (16 FP32 or 32 16-bit columns: 8 KiB), loaded with C by TMA when beta != 0 and
-// written back by TMA.  With beta != 0 four buffers keep C three chunks ahead; without C
-// two suffice and the operand ring keeps the space.
+// half of the epilogue (4 warps, 128 rows) owns CBUF buffers (2 when C is not read) of
+// one 128-row chunk of D (16 FP32 or 32 16-bit columns: 8 KiB), loaded with C by TMA
+// CBUF - 1 chunks ahead when beta != 0 and written back by TMA.  Four buffers (and one
+// stage less) pay off when the epilogue's C/D traffic outweighs the main loop: K bytes
+// per operand row <= 1024 x D's element size (measured on 16384 x 4096 and batched
+// 256 x 256 problems).
 constexpr int kDataBytes = 224 * 1024;
 constexpr int kEpiChunkBytes = 8 * 1024;
 constexpr int kBarrierBytes = 256;
@@ -31,15 +34,22 @@ constexpr int kSmemBytes = kDataBytes + kBarrierBytes + 1024;  // + alignment sl
 // Columns of D per epilogue chunk for an output of `bytes` per element.
 __host__ __device__ constexpr int epi_cols(int out_bytes) { return kEpiChunkBytes / (kBM * out_bytes); }
 
-template <int CG, bool BETA>
+// One ring stage holds kDepth 128-byte rows of K for every operand row: K = 128 FP16/BF16,
+// 64 TF32 or 256 FP8 elements.  The depth is what lets an M/N-major operand arrive as one
+// TMA box of 2 x 64 K rows per 128-byte chunk of M/N: boxes that cover only 64 K rows
+// (or interleave chunks within K groups) starve the tensor core on GB300 (measured: 76%
+// of the issue rate against 90% for K-major boxes), one box per chunk over the stage's
+// whole K range does not.
+template <int CG, int CBUF>
 struct TileCfg {
-    static constexpr int kEpiBufs = BETA ? 4 : 2;
-    static constexpr int kEpiBytes = 2 * kEpiBufs * kEpiChunkBytes;   // 64 or 32 KiB
-    static constexpr int kRingBytes = kDataBytes - kEpiBytes;         // 160 or 192 KiB
+    static constexpr int kEpiBufs = CBUF ? CBUF : 2;
+    static constexpr int kEpiBytes = 2 * kEpiBufs * kEpiChunkBytes;   // 32 or 64 KiB
+    static constexpr int kRingBytes = kDataBytes - kEpiBytes;         // 192 or 160 KiB
     static constexpr int kBRows = kBN / CG;                  // B rows loaded per CTA
-    static constexpr int kBBytes = kBRows * kRowBytes;
-    static constexpr int kStageBytes = kABytes + kBBytes;    // 48 KiB (1 CTA), 32 KiB (pair)
-    static constexpr int kStages = kRingBytes / kStageBytes; // pair: 6 (5 with C); 1 CTA: 4 (3)
+    static constexpr int kAStage = kABytes * kDepth;         // 32 KiB
+    static constexpr int kBStage = kBRows * kRowBytes * kDepth;   // 32 KiB (pair), 64 KiB
+    static constexpr int kStageBytes = kAStage + kBStage;    // 64 KiB (pair), 96 KiB (1 CTA)
+    static constexpr int kStages = kRingBytes / kStageBytes; // pair: 3 (2 with CBUF 4); 1 CTA: 2
     static constexpr int kTileM = kBM * CG;                  // rows of D per tile
 };
 
@@ -57,30 +67,26 @@ enum OutKind { kOutF32 = 0, kOutF16 = 1, kOutBF16 = 2 };
 // of K per instruction.
 enum MmaKind { kKindF16 = 0, kKindTF32 = 1, kKindF8 = 2 };
 
-// How an operand tile sits in global and shared memory.
-//   kK:        K contiguous.  3-D map {K, rows, batch}; shared tile = rows of 128 B
-//              along K, 8-row groups 1 KiB apart.
-//   kMNChunk:  M/N contiguous.  3-D map {rows, K, batch}; one box per 64-element
-//              (128-byte) chunk of rows, each chunk holding all K rows of the stage.
-//   kMNInter:  M/N contiguous, rows % c == 0 and K % 8 == 0, with c = 128 bytes /
-//              element size (64 for 16-bit operands; TF32 operands are always K-major).
-//              5-D map
-//              {c, 8, rows/c, K/8, batch}; one box per stage that interleaves the
-//              chunks inside every 8-row K group (1 KiB core blocks), which is the
-//              layout the tensor core reads at full rate.
-enum OperandMode { kK = 0, kMNChunk = 1, kMNInter = 2 };
+// How an operand tile sits in global and shared memory (128-byte swizzle throughout).
+//   kK:   K contiguous.  3-D map {K, rows, batch}, box {one 128-byte row of K, rows};
+//         a stage holds kDepth such boxes one after the other (rows x 128 B each);
+//         inside a box, 8-row groups are 1 KiB apart.
+//   kMN:  M/N contiguous.  3-D map {rows, K, batch}, box {c, kDepth 128-byte rows of K}
+//         with c = 128 bytes / element size (64 for 16-bit operands, 128 for FP8; TF32
+//         operands are always made K-major); a stage holds one box per c-element chunk
+//         of rows, chunk after chunk, each covering the stage's whole K range.
+enum OperandMode { kK = 0, kMN = 1 };
 
 struct GemmArgs {
     int m, n, k;
     int batch;
-    int num_m_tiles, num_n_tiles, num_k_blocks;
+    int num_m_tiles, num_n_tiles, num_k_blocks;   // K blocks of kDepth * k_row elements
     int total_tiles;
     int group_m;               // tile rasterisation: group of m-tiles walked together
     int a_mode, b_mode;        // OperandMode of A and B
     int a_bcast, b_bcast;      // batch stride 0: always batch coordinate 0
     int kind;                  // MmaKind
-    int k_per_block;           // K elements per stage (128 bytes): 64, 32 (TF32), 128 (FP8)
-    int mn_box;                // M/N elements per 128-byte run: 64, 32 (TF32), 128 (FP8)
+    int k_row;                 // K elements per 128-byte row: 64, 32 (TF32), 128 (FP8)
     uint32_t idesc;            // tcgen05 instruction descriptor
     float alpha, beta;
     const void *C;
@@ -89,6 +95,7 @@ struct GemmArgs {
     uint32_t *err;
     unsigned long long wait_limit_ns;
     int fault_inject;
+    int c_bufs;                // 0 (beta == 0), 2 or 4: epilogue variant (see TileCfg)
 };
 
 // Launchers (tcg_kernels.cu).  Return the launch's cudaError_t.

@@ -7,20 +7,22 @@
 // accumulator elementwise; "CUDA Handbook, 17.5 Tensor Cores": one MMA instruction
 // is a rank-K slab of the outer-product sum over k).
 //
-//   warp 0 (one lane)   TMA producer: 128x(128 B) A tile and 256x(128 B) B tile per
-//                        stage into a 4-deep ring of 128-byte-swizzled shared memory;
-//                        out-of-range rows/columns/K are zero-filled by TMA, which
-//                        makes ragged m, n, k exact.
-//   warp 1 (one lane)   MMA issuer: tcgen05.mma (M=128, N=256, K=16 for FP16/BF16,
-//                        K=8 for TF32) into a TMEM accumulator; two accumulators
+//   warp 0 (one lane)   TMA producer: per stage, two 128-byte rows of K for every row of
+//                        the CTA's A (128 rows) and B (128 rows per CTA of a pair, 256
+//                        for a single CTA) into a ring of 128-byte-swizzled shared
+//                        memory (3 stages of 64 KiB for a pair); out-of-range
+//                        rows/columns/K are zero-filled by TMA, which makes ragged m, n,
+//                        k exact.
+//   warp 1 (one lane)   MMA issuer: tcgen05.mma (M=128 or 256 for a pair, N=256; K=16
+//                        FP16/BF16, 8 TF32, 32 FP8) into a TMEM accumulator; two accumulators
 //                        (2 x 256 columns) so the epilogue of tile t overlaps the
 //                        main loop of tile t+1.  The page's diagnosis -- a tensor-core
 //                        kernel that stalls waiting for the next slab ("CUDA Handbook,
 //                        17.5", after Listing 17-5) -- is what the ring and the
 //                        separate producer remove.
-//   warps 2-5           epilogue: tcgen05.ld TMEM -> registers, alpha*acc + beta*C in
-//                        FP32, round to the output type (nearest even), coalesced
-//                        column-major stores (a warp writes 32 consecutive rows).
+//   warps 2-9           epilogue: tcgen05.ld TMEM -> registers, alpha*acc + beta*C in
+//                        FP32 (C by TMA), round to the output type (nearest even) into a
+//                        staging buffer, TMA store of D.
 //
 // Every wait is bounded (globaltimer): a wait that runs out sets a bit in the device
 // error word and a shared abort flag, every role stops, in-flight copies and MMAs are
@@ -32,12 +34,14 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "tcg_internal.h"
 #include "tcg_ptx.cuh"
 
 namespace tcg {
 
-constexpr int kMaxStages = TileCfg<2, false>::kStages;
+constexpr int kMaxStages = TileCfg<2, 0>::kStages;
 constexpr int kMaxEpiBufs = 4;
 
 struct SmemCtl {
@@ -149,19 +153,21 @@ __device__ __forceinline__ float load_c(const void *C, int64_t idx)
 // and signal the even CTA's "full" barrier, the MMA completion is multicast to both
 // CTAs' "empty" and "accumulator full" barriers, and both CTAs' epilogues report to the
 // even CTA's "accumulator empty" barrier.
-template <int OUT, int CG, int KIND, bool BETA>
+template <int OUT, int CG, int KIND, int CBUF>
 __global__ void __launch_bounds__(kThreads, 1)
     tcg_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmD, const GemmArgs p)
 {
-    using Cfg = TileCfg<CG, BETA>;
+    using Cfg = TileCfg<CG, CBUF>;
+    constexpr bool BETA = CBUF != 0;                          // C is read
     constexpr int kStages = Cfg::kStages;
     constexpr int kRingBytes = Cfg::kRingBytes;
     constexpr int kEpiBufs = Cfg::kEpiBufs;
     constexpr int kEpiBytes = Cfg::kEpiBytes;
     constexpr int kBRows = Cfg::kBRows;
-    constexpr int kBBytes = Cfg::kBBytes;
+    constexpr int kAStage = Cfg::kAStage;
+    constexpr int kBStage = Cfg::kBStage;
     constexpr int kStageBytes = Cfg::kStageBytes;
     constexpr int kTileM = Cfg::kTileM;
 
@@ -171,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t base = (raw_u32 + 1023u) & ~1023u;
     uint8_t *base_ptr = smem_raw + (base - raw_u32);
     const uint32_t a_smem = base;
-    const uint32_t b_smem = base + kStages * kABytes;
+    const uint32_t b_smem = base + kStages * kAStage;
     const uint32_t epi_smem = base + kRingBytes;
     uint8_t *epi_ptr = base_ptr + kRingBytes;
     SmemCtl *ctl = reinterpret_cast<SmemCtl *>(base_ptr + kRingBytes + kEpiBytes);
@@ -220,35 +226,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
 
-    // Byte offsets of successive K slices (one MMA each) inside a stage, and the
-    // descriptor strides, per operand majorness.  The MMA kind is a template argument:
-    // the issuing thread's loop must stay branch-free, as its instruction rate is what
-    // keeps the tensor core fed.
+    // The MMA kind is a template argument and every per-slice descriptor offset is
+    // computed before the loop: the issuing thread's loop must stay branch-free and
+    // short, as its instruction rate is what keeps the tensor core fed.
     constexpr uint32_t kEsize = KIND == kKindTF32 ? 4u : (KIND == kKindF8 ? 1u : 2u);
     constexpr uint32_t kKmma = 32u / kEsize;                  // K per MMA instruction
-    constexpr int kMmasPerStage = kRowBytes / 32;             // 4
-    const uint32_t chunk_bytes = static_cast<uint32_t>(p.k_per_block) * kRowBytes;
-    // Per operand: byte step between successive K slices, and the descriptor's
-    // leading / stride byte offsets (see OperandMode).
-    auto layout = [&](int mode, int rows, uint32_t &kstep, uint32_t &lbo, uint32_t &sbo) {
-        if (mode == kK) {
-            kstep = 32u;                                      // 32 bytes further along K
-            lbo = 16u;                                        // unused for this layout
-            sbo = 8 * kRowBytes;
-        } else if (mode == kMNChunk) {
-            kstep = kKmma * kRowBytes;                        // kKmma rows of 128 B
-            lbo = chunk_bytes;                                // next 64-element chunk
-            sbo = 8 * kRowBytes;                              // next 8-row K group
-        } else {
-            const uint32_t nchunks = static_cast<uint32_t>(rows / p.mn_box);
-            kstep = (kKmma / 8u) * nchunks * 1024u;           // kKmma/8 K groups
-            lbo = 1024u;                                      // next chunk, same K group
-            sbo = nchunks * 1024u;                            // next K group
+    constexpr int kMmasPerRow = kRowBytes / 32;               // 4 MMAs per 128-byte K row
+    constexpr int kMmasPerStage = kMmasPerRow * kDepth;       // 8
+    constexpr int kKRow = kRowBytes / kEsize;                 // K elements per 128-byte row
+    constexpr int kMnBox = kRowBytes / kEsize;                // M/N elements per 128-byte chunk
+    // Bytes of one kMnBox-element chunk of an M/N-major operand: kDepth K rows each.
+    constexpr uint32_t kChunkBytes = kDepth * kKRow * kRowBytes;
+    // Per operand (see OperandMode): the descriptor's leading / stride byte offsets and
+    // the byte offset of K slice j (one MMA) inside a stage.
+    //   kK:  slice j = K row j / 4 (a box of rows x 128 B), 32 bytes per slice within it;
+    //        8-row groups 1 KiB apart (SBO); LBO unused.
+    //   kMN: kKmma K rows of 128 B per slice, all chunks at once: LBO = chunk stride,
+    //        SBO = next 8-row K group (1 KiB).
+    auto layout = [&](int mode, int rows, uint32_t &lbo, uint32_t &sbo, uint32_t *off) {
+        sbo = 8 * kRowBytes;
+        lbo = mode == kK ? 16u : kChunkBytes;
+#pragma unroll
+        for (int j = 0; j < kMmasPerStage; ++j) {
+            const uint32_t b = mode == kK
+                ? static_cast<uint32_t>((j / kMmasPerRow) * rows * kRowBytes + (j % kMmasPerRow) * 32)
+                : static_cast<uint32_t>(j) * kKmma * kRowBytes;
+            off[j] = b >> 4;                                   // descriptor address units
         }
     };
-    uint32_t a_kstep, a_lbo, a_sbo, b_kstep, b_lbo, b_sbo;
-    layout(p.a_mode, kBM, a_kstep, a_lbo, a_sbo);
-    layout(p.b_mode, kBRows, b_kstep, b_lbo, b_sbo);
+    uint32_t a_lbo, a_sbo, b_lbo, b_sbo, a_off[kMmasPerStage], b_off[kMmasPerStage];
+    layout(p.a_mode, kBM, a_lbo, a_sbo, a_off);
+    layout(p.b_mode, kBRows, b_lbo, b_sbo, b_off);
     // Descriptors of stage 0, K slice 0; other slices add (byte offset >> 4) to the
     // start-address field (bits 0-13), which cannot overflow in 227 KB of shared memory.
     const uint64_t a_desc0 = smem_desc_sw128(a_smem, a_lbo, a_sbo);
@@ -284,35 +292,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                             issued_mask |= 1u << stage;
                             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                         }
-                        const uint32_t sa = a_smem + stage * kABytes;
-                        const uint32_t sb = b_smem + stage * kBBytes;
-                        const int k0 = kb * p.k_per_block;
-                        // One operand tile: `rows` rows starting at row0, K slice k0.
-                        auto load = [&](uint32_t dst, const CUtensorMap *map, int mode, int rows,
+                        const uint32_t sa = a_smem + stage * kAStage;
+                        const uint32_t sb = b_smem + stage * kBStage;
+                        const int k0 = kb * kDepth * kKRow;
+                        // One operand tile: `rows` rows starting at row0, K from k0: kDepth
+                        // boxes of rows x 128 B (K-major) or one box per c-element chunk of
+                        // rows covering all kDepth K rows (M/N-major).
+                        auto box = [&](uint32_t d, const CUtensorMap *map, int x, int y, int z) {
+                            if constexpr (CG == 2)
+                                tma_load_3d_pair(d, map, fb, x, y, z);
+                            else
+                                tma_load_3d(d, map, fb, x, y, z);
+                        };
+                        auto load = [&](uint32_t dst, const CUtensorMap *map, int mode, auto rows_c,
                                         int row0, int z) {
+                            constexpr int kRows = decltype(rows_c)::value;
                             if (mode == kK) {
-                                if constexpr (CG == 2)
-                                    tma_load_3d_pair(dst, map, fb, k0, row0, z);
-                                else
-                                    tma_load_3d(dst, map, fb, k0, row0, z);
-                            } else if (mode == kMNChunk) {
-                                for (int h = 0; h < rows / p.mn_box; ++h) {
-                                    if constexpr (CG == 2)
-                                        tma_load_3d_pair(dst + h * chunk_bytes, map, fb,
-                                                         row0 + h * p.mn_box, k0, z);
-                                    else
-                                        tma_load_3d(dst + h * chunk_bytes, map, fb,
-                                                    row0 + h * p.mn_box, k0, z);
-                                }
+#pragma unroll
+                                for (int h = 0; h < kDepth; ++h)
+                                    box(dst + h * kRows * kRowBytes, map, k0 + h * kKRow, row0, z);
                             } else {
-                                if constexpr (CG == 2)
-                                    tma_load_5d_pair(dst, map, fb, 0, 0, row0 / p.mn_box, k0 / 8, z);
-                                else
-                                    tma_load_5d(dst, map, fb, 0, 0, row0 / p.mn_box, k0 / 8, z);
+#pragma unroll
+                                for (int h = 0; h < kRows / kMnBox; ++h)
+                                    box(dst + h * kChunkBytes, map, row0 + h * kMnBox, k0, z);
                             }
                         };
-                        load(sa, &tmA, p.a_mode, kBM, m0, za);
-                        load(sb, &tmB, p.b_mode, kBRows, n0, zb);
+                        load(sa, &tmA, p.a_mode, std::integral_constant<int, kBM>{}, m0, za);
+                        load(sb, &tmB, p.b_mode, std::integral_constant<int, kBRows>{}, n0, zb);
                     }
                     if (++stage == kStages) {
                         stage = 0;
@@ -345,12 +351,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad_s = a_desc0 + ((static_cast<uint32_t>(stage) * kABytes) >> 4);
-                    const uint64_t bd_s = b_desc0 + ((static_cast<uint32_t>(stage) * kBBytes) >> 4);
+                    const uint64_t ad_s = a_desc0 + ((static_cast<uint32_t>(stage) * kAStage) >> 4);
+                    const uint64_t bd_s = b_desc0 + ((static_cast<uint32_t>(stage) * kBStage) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < kMmasPerStage; ++kk) {
-                        const uint64_t ad = ad_s + ((kk * a_kstep) >> 4);
-                        const uint64_t bd = bd_s + ((kk * b_kstep) >> 4);
+                        const uint64_t ad = ad_s + a_off[kk];
+                        const uint64_t bd = bd_s + b_off[kk];
                         const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
                         if constexpr (CG == 2) {
                             if constexpr (KIND == kKindTF32)
@@ -648,30 +654,34 @@ __global__ void __launch_bounds__(256) tcg_tf32_pack_kernel(const uint32_t *__re
 typedef void (*GemmKernelFn)(const CUtensorMap, const CUtensorMap, const CUtensorMap,
                              const GemmArgs);
 
-template <int CG, bool BETA>
+template <int CG, int CBUF>
 static GemmKernelFn gemm_fn_cg(int out_kind, int kind)
 {
     if (kind == kKindTF32)   // TF32 inputs always produce FP32 output
-        return tcg_gemm_kernel<kOutF32, CG, kKindTF32, BETA>;
+        return tcg_gemm_kernel<kOutF32, CG, kKindTF32, CBUF>;
     if (kind == kKindF8) {
         switch (out_kind) {
-        case kOutF32: return tcg_gemm_kernel<kOutF32, CG, kKindF8, BETA>;
-        case kOutF16: return tcg_gemm_kernel<kOutF16, CG, kKindF8, BETA>;
-        default: return tcg_gemm_kernel<kOutBF16, CG, kKindF8, BETA>;
+        case kOutF32: return tcg_gemm_kernel<kOutF32, CG, kKindF8, CBUF>;
+        case kOutF16: return tcg_gemm_kernel<kOutF16, CG, kKindF8, CBUF>;
+        default: return tcg_gemm_kernel<kOutBF16, CG, kKindF8, CBUF>;
         }
     }
     switch (out_kind) {
-    case kOutF32: return tcg_gemm_kernel<kOutF32, CG, kKindF16, BETA>;
-    case kOutF16: return tcg_gemm_kernel<kOutF16, CG, kKindF16, BETA>;
-    default: return tcg_gemm_kernel<kOutBF16, CG, kKindF16, BETA>;
+    case kOutF32: return tcg_gemm_kernel<kOutF32, CG, kKindF16, CBUF>;
+    case kOutF16: return tcg_gemm_kernel<kOutF16, CG, kKindF16, CBUF>;
+    default: return tcg_gemm_kernel<kOutBF16, CG, kKindF16, CBUF>;
     }
 }
 
-static GemmKernelFn gemm_fn(int out_kind, int cta_group, int kind, bool beta)
+// c_bufs: 0 (beta == 0), 2 or 4 (C staging buffers per epilogue half; 4 only for pairs).
+static GemmKernelFn gemm_fn(int out_kind, int cta_group, int kind, int c_bufs)
 {
-    if (cta_group == 2)
-        return beta ? gemm_fn_cg<2, true>(out_kind, kind) : gemm_fn_cg<2, false>(out_kind, kind);
-    return beta ? gemm_fn_cg<1, true>(out_kind, kind) : gemm_fn_cg<1, false>(out_kind, kind);
+    if (cta_group == 2) {
+        if (c_bufs == 4)
+            return gemm_fn_cg<2, 4>(out_kind, kind);
+        return c_bufs ? gemm_fn_cg<2, 2>(out_kind, kind) : gemm_fn_cg<2, 0>(out_kind, kind);
+    }
+    return c_bufs ? gemm_fn_cg<1, 2>(out_kind, kind) : gemm_fn_cg<1, 0>(out_kind, kind);
 }
 
 static cudaError_t prepare(GemmKernelFn fn)
@@ -683,7 +693,7 @@ static cudaError_t prepare(GemmKernelFn fn)
 
 int gemm_max_resident_ctas(int cta_group, int num_sms)
 {
-    GemmKernelFn fn = gemm_fn(kOutF32, cta_group, kKindF16, false);
+    GemmKernelFn fn = gemm_fn(kOutF32, cta_group, kKindF16, 0);
     if (prepare(fn) != cudaSuccess) {
         cudaGetLastError();
         return num_sms / cta_group * cta_group;
@@ -850,7 +860,7 @@ cudaError_t launch_tf32_transpose_round(const void *in, int64_t ld, int64_t stri
 cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmD,
                         const GemmArgs &a, int out_kind, int cta_group, int grid, cudaStream_t s)
 {
-    GemmKernelFn fn = gemm_fn(out_kind, cta_group, a.kind, a.beta != 0.0f);
+    GemmKernelFn fn = gemm_fn(out_kind, cta_group, a.kind, a.c_bufs);
     cudaError_t e = prepare(fn);
     if (e != cudaSuccess)
         return e;

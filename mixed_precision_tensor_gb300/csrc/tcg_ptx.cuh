@@ -73,18 +73,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
-// 5-D tiled load (used for the interleaved M/N-major operand layout).
-__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                            int c0, int c1, int c2, int c3, int c4)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
-        "r"(bar)
-        : "memory");
-}
-
 // 3-D tiled store shared -> global (bulk-group completion); out-of-range parts of the
 // box are not written.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int x, int y,
@@ -141,12 +129,6 @@ __device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t count, bo
         : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(count)
         : "memory");
     return r != 0;
-}
-
-// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned address) into L2.
-__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // ----------------------------------------------------------------- tcgen05
@@ -321,18 +303,6 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
         "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar_cluster)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_5d_pair(uint32_t dst, const CUtensorMap *map,
-                                                 uint32_t bar_cluster, int c0, int c1, int c2,
-                                                 int c3, int c4)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.5d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
-        "r"(bar_cluster)
         : "memory");
 }
 
