@@ -28,6 +28,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "tcg_oracle.c")
+_SRC_MODEL = os.path.join(_HERE, "tc_model.c")
 _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
 
@@ -42,11 +43,12 @@ def build(force: bool = False) -> str:
     """Compile tcg_oracle.c into oracle/_build/liboracle.so with gcc."""
     os.makedirs(_OUT_DIR, exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(_SRC),
+                                                    os.path.getmtime(_SRC_MODEL))):
         return _LIB_PATH
     tmp = _LIB_PATH + f".{os.getpid()}.tmp"
-    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
-           "-shared", "-pthread", "-o", tmp, _SRC, "-lm"]
+    cmd = ["gcc", "-O2", "-std=gnu11", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+           "-shared", "-pthread", "-o", tmp, _SRC, _SRC_MODEL, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -72,6 +74,10 @@ def _load():
             fn.argtypes = [vp, vp, i64]
         lib.orc_tf32_round_bits.restype = ctypes.c_uint32
         lib.orc_tf32_round_bits.argtypes = [ctypes.c_uint32]
+        lib.orc_gemm_model.restype = ci
+        lib.orc_gemm_model.argtypes = [ci, ci, i64, i64, i64, dbl, vp, ci, i64, vp, ci, i64,
+                                       dbl, vp, ci, i64, ci, i64, i64, i64, i64, vp, i64,
+                                       ci, ci, ci, ci, ci]
         _lib = lib
         return lib
 
@@ -164,3 +170,53 @@ def gemm(transa, transb, m, n, k, alpha, A, atype, lda, B, btype, ldb, beta, C, 
     def shape(x):
         return None if x is None else x[: nr * nc].reshape(nc, nr).T
     return shape(D), shape(R), shape(AB)
+
+
+def gemm_model(transa, transb, m, n, k, alpha, A, atype, lda, B, btype, ldb, beta, C, ctype,
+               ldc, tf32=False, rows=None, cols=None, nthreads=None, block=16, frac=25,
+               norm_rne=False, exp_sum=True):
+    """Block of D = alpha*op(A)*op(B) + beta*C with the block-FMA model of ``tc_model.c``
+    as the accumulator and the library's FP32 epilogue (arguments as :func:`gemm`):
+    products in blocks of ``block``, terms cut toward zero ``frac`` bits below the
+    block's largest alignment exponent (input-exponent sums if ``exp_sum``), each block
+    sum rounded into the FP32 accumulator toward zero (to nearest even if
+    ``norm_rne``).  Returns D as an (i1-i0, j1-j0) array in the output storage type."""
+    i0, i1 = rows if rows is not None else (0, m)
+    j0, j1 = cols if cols is not None else (0, n)
+    nr, nc = i1 - i0, j1 - j0
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    A = np.ascontiguousarray(A) if A is not None else None
+    B = np.ascontiguousarray(B) if B is not None else None
+    C = np.ascontiguousarray(C) if C is not None else None
+    D = np.zeros(max(nr * nc, 1), dtype=_ELEM_DTYPE[ctype])
+    rc = _load().orc_gemm_model(int(transa), int(transb), int(m), int(n), int(k), float(alpha),
+                                _ptr(A), int(atype), int(lda), _ptr(B), int(btype), int(ldb),
+                                float(beta), _ptr(C), int(ctype), int(ldc), int(bool(tf32)),
+                                int(i0), int(i1), int(j0), int(j1), _ptr(D), int(max(nr, 1)),
+                                int(block), int(frac), int(bool(norm_rne)), int(bool(exp_sum)),
+                                int(nthreads))
+    if rc != 0:
+        raise ValueError(f"orc_gemm_model failed with code {rc}")
+    return D[: nr * nc].reshape(nc, nr).T
+
+
+def dot_model(A, atype, B, btype, m, n, k, tf32=False, **params):
+    """FP32 D = A*B (column-major, lda = m, ldb = k; alpha = 1, beta = 0) under the
+    block-FMA model; ``params`` as :func:`gemm_model`.  Returns an (m, n) float32 array."""
+    return gemm_model(OP_N, OP_N, m, n, k, 1.0, A, atype, m, B, btype, k, 0.0, None, F32, m,
+                      tf32=tf32, **params)
+
+
+# Block-FMA parameters of the pages' newest generation ("NVIDIA Tensor Core混合精度计算原理与应用解析",
+# sections 2.2.1 and 2.2.2: an accumulator of 2 + 23 + 2 bits, i.e. a cut 25 bits below the
+# block's largest exponent; N_FMA = 16 for FP16/BF16 and 8 for TF32; section 2.3: truncation
+# inside the accumulation; section 4.1: products aligned by their unnormalised exponents).
+# FP8 takes one block per 32-element instruction (see the readings in the design notes).
+PAGE_MODEL = {
+    F16: dict(block=16, frac=25, norm_rne=False, exp_sum=True),
+    BF16: dict(block=16, frac=25, norm_rne=False, exp_sum=True),
+    F32: dict(block=8, frac=25, norm_rne=False, exp_sum=True),       # TF32 compute
+    F8E4M3: dict(block=32, frac=25, norm_rne=False, exp_sum=True),
+    F8E5M2: dict(block=32, frac=25, norm_rne=False, exp_sum=True),
+}

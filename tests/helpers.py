@@ -67,6 +67,23 @@ def oracle_rowmajor(w, A, B, C, b=0, rows=None, cols=None, nthreads=None):
     return D.T, R.T, AB.T
 
 
+def model_rowmajor(w, A, B, C, b=0, rows=None, cols=None, nthreads=None):
+    """The block-FMA model (oracle.PAGE_MODEL parameters) for the same row-major problem
+    and block as :func:`oracle_rowmajor`.  Returns D as a row-major block."""
+    m, n, k = w.m, w.n, w.k
+    i0, i1 = rows if rows else (0, m)
+    j0, j1 = cols if cols else (0, n)
+    Ab = raw(A[b]).reshape(-1)
+    Bb = raw(B[b]).reshape(-1)
+    Cb = raw(C[b]).reshape(-1) if C is not None else None
+    t = TYPE_CODE[w.in_type]
+    D = oracle.gemm_model(oracle.OP_N, oracle.OP_N, n, m, k, w.alpha, Bb, t, n, Ab, t, k,
+                          w.beta, Cb, TYPE_CODE[w.out_type], n, tf32=(w.in_type == "f32"),
+                          rows=(j0, j1), cols=(i0, i1), nthreads=nthreads,
+                          **oracle.PAGE_MODEL[t])
+    return D.T
+
+
 def decode_out(x: np.ndarray, out_type: str) -> np.ndarray:
     if out_type == "f16":
         return x.view(np.float16).astype(np.float64) if x.dtype == np.uint16 else x.astype(np.float64)

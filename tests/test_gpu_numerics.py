@@ -1,0 +1,168 @@
+"""The tensor core's numeric features on this GPU (probe) and the block-FMA model's
+agreement with it on random inputs.
+
+"NVIDIA Tensor Core混合精度计算原理与应用解析", section 3: feature-detection vectors (GNFT,
+section 3.1) fix the parameters of a model of the hardware's accumulation, and random
+inputs (ISSM, section 3.2: normal and uniform samples plus directed special cases) check
+the model against the hardware; on disagreement the model is refined (section 3.3).
+
+Here the parameters come from this GPU (the probe), so agreement validates the model.
+The GEMM's parity tests (test_gpu_parity.py) use the parameters the page states for its
+newest generation (oracle.PAGE_MODEL), not these; test_probe_agrees_with_the_page below
+checks that the two sets coincide.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mixed_precision_tensor_gb300 as tcg
+import oracle
+from mixed_precision_tensor_gb300 import numerics
+
+pytestmark = pytest.mark.gpu
+
+KINDS = list(numerics.FORMATS)
+ORACLE_TYPE = {"f16": oracle.F16, "bf16": oracle.BF16, "tf32": oracle.F32, "e4m3": oracle.F8E4M3,
+               "e5m2": oracle.F8E5M2}
+
+
+@pytest.fixture(scope="module")
+def features(cuda_device):
+    return numerics.probe(tcg.Handle())
+
+
+def test_probe_determines_every_feature(features):
+    for kind, f in features.items():
+        assert not f.notes, (kind, f.notes)
+        assert f.block is not None and f.frac_bits is not None, (kind, f)
+        assert f.exponent is not None and f.accumulator_aligned is not None, (kind, f)
+        assert f.normalisation is not None and f.cut is not None, (kind, f)
+        assert f.subnormal_inputs is not None and f.specials_ieee is not None, (kind, f)
+        assert f.model_parameters() is not None, (kind, f)
+
+
+def test_probe_agrees_with_the_page(features):
+    # The page's newest-generation parameters (sections 2.2.1, 2.2.2, 2.3, 4.1) against
+    # what the probe measured on this GPU.
+    for kind, f in features.items():
+        assert f.model_parameters() == oracle.PAGE_MODEL[ORACLE_TYPE[kind]], (kind, f)
+
+
+def test_probe_matches_the_page_vectors(features):
+    # The page's accumulator example (section 2.2.1) through the library on this GPU: the
+    # result is 2.25 or 2.25 + 2^-22 depending on the window and the normalisation; the
+    # probe's features must predict which.
+    f = numerics.FORMATS["f16"]
+    run = numerics._Runner(tcg.Handle(), f, torch.device("cuda:0")).run
+    got = run([[(1.5, 1.5), (2.0 ** -23, 1.0), (2.0 ** -24, 1.0)]], f.k_instr)[0]
+    ft = features["f16"]
+    keeps_both = ft.frac_bits >= 24
+    want = 2.25 + 2.0 ** -22 if (keeps_both and ft.normalisation == "nearest-even") else 2.25
+    assert got == want
+
+
+# --- ISSM: random and directed inputs, GPU against the model ---------------------------
+
+def _cast(x64, kind):
+    """float64 values -> device tensor of the kind's storage type (RNE casts)."""
+    dt = numerics.FORMATS[kind].dtype
+    return torch.from_numpy(x64.astype(np.float32)).to(dt)
+
+
+def _raw(t, kind):
+    """Host raw storage of a tensor for the oracle."""
+    t = t.cpu().contiguous()
+    if kind in ("f16", "bf16"):
+        return t.view(torch.int16).numpy().view(np.uint16)
+    if kind in ("e4m3", "e5m2"):
+        return t.view(torch.uint8).numpy()
+    return t.numpy()
+
+
+def _draw(kind, dist, shape, rng):
+    f = numerics.FORMATS[kind]
+    if dist == "normal":
+        return rng.standard_normal(shape)
+    if dist == "uniform":
+        return rng.uniform(-1.0, 1.0, shape)
+    lo, hi = max(f.emin, -50), min(f.emax, 50)
+    sign = rng.integers(0, 2, shape) * 2 - 1
+    mant = 1.0 + rng.integers(0, 2 ** f.mbits, shape) / 2.0 ** f.mbits
+    if dist == "wide":               # every exponent of the format (BF16/TF32: +-50)
+        return sign * np.ldexp(mant, rng.integers(lo, hi, shape))
+    if dist == "subnormal":          # half subnormal inputs, half small normals
+        sub = rng.integers(1, 2 ** f.mbits, shape) * 2.0 ** (f.emin - f.mbits)
+        nrm = np.ldexp(mant, rng.integers(f.emin, f.emin + 4, shape))
+        return sign * np.where(rng.random(shape) < 0.5, sub, nrm)
+    raise ValueError(dist)
+
+
+def _case(kind, dist, m, n, k, seed):
+    """Inputs (column-major A m x k, B k x n) for one ISSM case, as device tensors."""
+    rng = np.random.default_rng(seed)
+    A = _draw(kind, dist if dist != "cancel" else "wide", (k, m), rng)   # A^T row-major
+    if dist == "subnormal":
+        f = numerics.FORMATS[kind]
+        # B scales the subnormal products into FP32's normal and subnormal range
+        B = np.ldexp(1.0 + rng.integers(0, 2 ** f.mbits, (n, k)) / 2.0 ** f.mbits,
+                     rng.integers(max(f.emax - 10, 0), f.emax, (n, k)))
+    else:
+        B = _draw(kind, dist if dist != "cancel" else "wide", (n, k), rng)
+    if dist == "cancel":
+        # every odd product cancels the even one before it, except where a perturbation
+        # of one input by a few units leaves a residual far below the pair
+        A[1::2, :] = -A[0::2, :]
+        B[:, 1::2] = B[:, 0::2]
+        f = numerics.FORMATS[kind]
+        pert = rng.random(A[1::2, :].shape) < 0.25
+        A[1::2, :] = np.where(pert, A[1::2, :] * (1 + 2.0 ** -f.mbits), A[1::2, :])
+    return _cast(A, kind), _cast(B, kind)
+
+
+DISTS = ["normal", "uniform", "wide", "cancel", "subnormal"]
+
+
+@pytest.mark.timeout(600)
+@pytest.mark.parametrize("dist", DISTS)
+@pytest.mark.parametrize("kind", KINDS)
+def test_issm_model_agreement(features, kind, dist):
+    params = features[kind].model_parameters()
+    assert params is not None
+    f = numerics.FORMATS[kind]
+    m = n = 128
+    k = 8 * f.k_instr
+    seed = 1000 + 17 * KINDS.index(kind) + DISTS.index(dist)
+    At, Bt = _case(kind, dist, m, n, k, seed)
+    D = torch.zeros((n, m), dtype=torch.float32, device="cuda:0")      # column-major m x n
+    h = tcg.Handle()
+    tcg.check(tcg.tcg_gemm_ex(h.h, tcg.TCG_OP_N, tcg.TCG_OP_N, m, n, k, 1.0, At.cuda(), f.code, m,
+                              Bt.cuda(), f.code, k, 0.0, D, tcg.TCG_R_32F, m, f.compute))
+    got = D.cpu().numpy().T                                          # (m, n)
+    want = oracle.dot_model(_raw(At, kind), ORACLE_TYPE[kind], _raw(Bt, kind),
+                            ORACLE_TYPE[kind], m, n, k, tf32=(kind == "tf32"), **params)
+    same = (got == want) | (np.isnan(got) & np.isnan(want))
+    bad = np.argwhere(~same)
+    assert bad.size == 0, (f"{len(bad)} of {m * n} differ; first (i, j, gpu, model): " +
+                           str([(int(i), int(j), float(got[i, j]), float(want[i, j]))
+                                for i, j in bad[:5]]))
+
+
+@pytest.mark.timeout(900)
+@pytest.mark.parametrize("kind", ["f16", "bf16"])
+def test_issm_large_uniform_sample(features, kind):
+    # ~6.6e4 dot products of length 1024 (the page's uniform sampling, section 3.2)
+    params = features[kind].model_parameters()
+    f = numerics.FORMATS[kind]
+    m = n = 256
+    k = 1024
+    rng = np.random.default_rng(77 + KINDS.index(kind))
+    At = _cast(rng.uniform(-1, 1, (k, m)), kind)
+    Bt = _cast(rng.uniform(-1, 1, (n, k)), kind)
+    D = torch.zeros((n, m), dtype=torch.float32, device="cuda:0")
+    h = tcg.Handle()
+    tcg.check(tcg.tcg_gemm_ex(h.h, tcg.TCG_OP_N, tcg.TCG_OP_N, m, n, k, 1.0, At.cuda(), f.code, m,
+                              Bt.cuda(), f.code, k, 0.0, D, tcg.TCG_R_32F, m, f.compute))
+    got = D.cpu().numpy().T
+    want = oracle.dot_model(_raw(At, kind), ORACLE_TYPE[kind], _raw(Bt, kind),
+                            ORACLE_TYPE[kind], m, n, k, **params)
+    assert np.array_equal(got, want)

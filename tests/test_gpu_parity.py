@@ -4,7 +4,10 @@ Bar (element by element): bit-exact (by value class) on integer-valued inputs
 whose sums stay exact in FP32; on random inputs
     |D - ref| <= k*2^-23*(|alpha|*(|A||B|) + |beta|*|C|)  (+ one output ulp for 16-bit out)
 the error model of "NVIDIA Tensor Core混合精度计算原理与应用解析" section 2.3 with
-p = 23 (FP32 accumulation).  Small cases are checked in full; the 8192^3,
+p = 23 (FP32 accumulation), against the exact oracle -- and, in addition, bit-exact
+(by value class) against the oracle's block-FMA model with the parameters that page
+gives for its newest generation (oracle.PAGE_MODEL: blocks of 16 FP16/BF16 or 8 TF32
+products, a cut 25 bits below the block's largest exponent, truncation).  Small cases are checked in full; the 8192^3,
 16384x4096x4096 and 4096x4096x16384 workloads are checked on 64 seeded 128x128
 output tiles (corners always included), in the launch configuration the
 benchmark times.  Output buffers carry canary guard bands (before, after, and in
@@ -16,7 +19,8 @@ import torch
 
 import mixed_precision_tensor_gb300 as tcg
 import oracle
-from helpers import TYPE_CODE, check_bound, decode_out, oracle_rowmajor, raw, values_equal
+from helpers import (TYPE_CODE, check_bound, decode_out, model_rowmajor, oracle_rowmajor, raw,
+                     values_equal)
 from mixed_precision_tensor_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -143,18 +147,21 @@ def run_colmajor(h, transa, transb, m, n, k, alpha, beta, in_t, out_t, seed, dis
                                              np.full_like(pad, canary).view(np.uint8))
     results = []
     for b in range(batch):
-        D, R, AB = oracle.gemm(transa, transb, m, n, k, alpha, Araw[b * sA:(b + 1) * sA],
-                               TYPE_CODE[in_t], lda, Braw[b * sB:(b + 1) * sB], TYPE_CODE[in_t],
-                               ldb, beta, Cin[b * sC:(b + 1) * sC], TYPE_CODE[out_t], ldc,
-                               tf32=(in_t == "f32" and not split3))
+        args = (transa, transb, m, n, k, alpha, Araw[b * sA:(b + 1) * sA], TYPE_CODE[in_t], lda,
+                Braw[b * sB:(b + 1) * sB], TYPE_CODE[in_t], ldb, beta,
+                Cin[b * sC:(b + 1) * sC], TYPE_CODE[out_t], ldc)
+        D, R, AB = oracle.gemm(*args, tf32=(in_t == "f32" and not split3))
+        # the three-product FP32 emulation is three GEMMs: not one block-FMA accumulation
+        Dm = None if split3 else oracle.gemm_model(*args, tf32=(in_t == "f32"),
+                                                   **oracle.PAGE_MODEL[TYPE_CODE[in_t]])
         got = body[b, : ldc * n].reshape(n, ldc)[:, :m].T
         cdec = _decode(Cin[b * sC:(b + 1) * sC][: ldc * n].reshape(n, ldc)[:, :m].T, out_t)
-        results.append((got, D, R, AB, cdec))
+        results.append((got, D, R, AB, cdec, Dm))
     return results, guards_ok
 
 
 def _assert_results(results, k, alpha, beta, out_t, exact):
-    for got, D, R, AB, cdec in results:
+    for got, D, R, AB, cdec, Dm in results:
         g = _decode(np.ascontiguousarray(got), out_t)
         ref = _decode(np.ascontiguousarray(D), out_t)
         if exact:
@@ -162,6 +169,18 @@ def _assert_results(results, k, alpha, beta, out_t, exact):
         else:
             ok, worst, idx = check_bound(g, ref, AB, cdec, k, alpha, beta, out_t)
             assert ok, f"bound exceeded: worst normalised error {worst} at {np.unravel_index(idx, g.shape)}"
+        if Dm is not None:
+            _assert_model_equal(g, _decode(np.ascontiguousarray(Dm), out_t))
+
+
+def _assert_model_equal(g, model):
+    """Bit-exact (by value class) against the block-FMA model."""
+    same = (g == model) | (np.isnan(g) & np.isnan(model))
+    bad = np.argwhere(~same)
+    assert bad.size == 0, (f"{len(bad)} of {g.size} differ from the block-FMA model; first "
+                           f"(index, gpu, model): " +
+                           str([(tuple(int(x) for x in i), float(g[tuple(i)]),
+                                 float(model[tuple(i)])) for i in bad[:4]]))
 
 
 RAGGED = [(1, 1, 1), (7, 17, 15), (129, 255, 257), (200, 127, 1000), (257, 513, 64),
@@ -248,7 +267,7 @@ def test_split3_tf32_recovers_fp32_accuracy(any_handle, m, n, k, transa, transb)
     assert guards
     res1, _ = run_colmajor(any_handle, transa, transb, m, n, k, 0.75, -0.5, "f32", "f32",
                            **kw)
-    (got3, D, R, AB, cdec), (got1, _, _, _, _) = res3[0], res1[0]
+    (got3, D, R, AB, cdec, _), (got1, _, _, _, _, _) = res3[0], res1[0]
     scale = 0.75 * AB + 0.5 * np.abs(cdec)
     bound = (k + 8) * 2.0 ** -23 * scale
     err3 = np.abs(got3.astype(np.float64) - R)
@@ -265,7 +284,7 @@ def test_split3_batched_and_integer_exact(any_handle):
     res, guards = run_colmajor(any_handle, N, T, 100, 72, 40, 1.0, 0.5, "f32", "f32", seed=91,
                                dist="integer", batch=3, split3=True)
     assert guards
-    for got, D, R, AB, cdec in res:
+    for got, D, R, AB, cdec, _ in res:
         assert values_equal(got.astype(np.float64), R)
 
 
@@ -331,8 +350,11 @@ def test_page_vectors_on_gpu(handle):
     tcg.gemm_rowmajor(handle, A.cuda(), B.cuda(), C)
     torch.cuda.synchronize()
     v = float(C[0, 0])
-    assert v in (2.25, 2.25 + 2.0 ** -22, 2.25 + 2.0 ** -23)
-    print(f"accumulation vector: GPU {v!r} (oracle 2.25 + 2^-22 = {2.25 + 2.0 ** -22!r})")
+    model = float(oracle.dot_model(A.T.contiguous().numpy().view(np.uint16), oracle.F16,
+                                   B.T.contiguous().numpy().view(np.uint16), oracle.F16, 16, 16,
+                                   16, **oracle.PAGE_MODEL[oracle.F16])[0, 0])
+    assert v == model          # 2.25: 3*2^-24 cut away when the sum is truncated into FP32
+    print(f"accumulation vector: GPU {v!r} (model {model!r}; exact-sum oracle 2.25 + 2^-22)")
     A = torch.zeros(16, 16, dtype=torch.bfloat16)
     B = torch.zeros(16, 16, dtype=torch.bfloat16)
     A[0, :2] = torch.tensor([127 * 2.0 ** -78, 2.0 ** -78], dtype=torch.float64).to(torch.bfloat16)
@@ -341,8 +363,12 @@ def test_page_vectors_on_gpu(handle):
     tcg.gemm_rowmajor(handle, A.cuda(), B.cuda(), C)
     torch.cuda.synchronize()
     v = float(C[0, 0])
-    print(f"subnormal vector: GPU {v!r} (oracle 2^-149 = {2.0 ** -149!r})")
-    assert 0.0 <= v <= 2.0 ** -148
+    model = float(oracle.dot_model(A.T.contiguous().view(torch.int16).numpy().view(np.uint16),
+                                   oracle.BF16,
+                                   B.T.contiguous().view(torch.int16).numpy().view(np.uint16),
+                                   oracle.BF16, 16, 16, 16, **oracle.PAGE_MODEL[oracle.BF16])[0, 0])
+    print(f"subnormal vector: GPU {v!r} (model {model!r}; exact-sum oracle 2^-149)")
+    assert v == model          # 2^-149 - 2^-157 truncated to the FP32 subnormal grid: 0
 
 
 # ------------------------------------------------------------ the five workloads
@@ -386,9 +412,10 @@ def _check_full(w, A, B, C, out, exact):
         else:
             ok, worst, idx = check_bound(g, ref, AB, cdec, w.k, w.alpha, w.beta, w.out_type)
             assert ok, f"batch {b}: worst normalised error {worst}"
+            _assert_model_equal(g, decode_out(raw(model_rowmajor(w, A, B, C, b=b)), w.out_type))
 
 
-def _check_sampled(w, A, B, C, out, exact, count=64):
+def _check_sampled(w, A, B, C, out, exact, count=64, model_tiles=8):
     tiles = wl.sample_tiles(w.m, w.n, count=count, tile=128, seed=w.seed)
     assert len(tiles) == min(count, (-(-w.m // 128)) * (-(-w.n // 128)))
     worst_all = 0.0
@@ -404,6 +431,13 @@ def _check_sampled(w, A, B, C, out, exact, count=64):
             ok, worst, idx = check_bound(g, ref, AB, cdec, w.k, w.alpha, w.beta, w.out_type)
             assert ok, f"tile {(i0, j0)}: worst normalised error {worst}"
             worst_all = max(worst_all, worst)
+    if not exact:
+        # bit-exact against the block-FMA model on the first model_tiles tiles (the four
+        # corners come first)
+        for (i0, i1, j0, j1) in tiles[:model_tiles]:
+            g = decode_out(raw(np.ascontiguousarray(out[0][i0:i1, j0:j1])), w.out_type)
+            Dm = model_rowmajor(w, A, B, C, rows=(i0, i1), cols=(j0, j1))
+            _assert_model_equal(g, decode_out(raw(np.ascontiguousarray(Dm)), w.out_type))
     return worst_all
 
 
