@@ -47,7 +47,8 @@
  * handle is not thread-safe: use one per host thread.  C must not overlap A or
  * B.  The first GEMM call on a handle binds it to the current device and
  * allocates a 4-byte device error word; make that call before any stream
- * capture.  The TF32 path needs a workspace (see tcg_set_workspace).
+ * capture.  The TF32 path and split-K calls need a workspace (see
+ * tcg_set_workspace).
  *
  * Pointers are device pointers (or memory the device can access, e.g. managed
  * memory) unless stated otherwise.
@@ -112,14 +113,17 @@ tcgStatus_t tcg_destroy(tcgHandle_t h);
 tcgStatus_t tcg_set_stream(tcgHandle_t h, void *stream);
 
 /* Give the handle caller-owned device scratch memory for the TF32 path (which
- * writes TF32-rounded, K-major copies of op(A) and op(B) before the product).
+ * writes TF32-rounded, K-major copies of op(A) and op(B) before the product) and for
+ * the FP32 partial sums of split-K calls (tcg_set_split_k).
  * ptr must be 256-byte aligned; bytes may be 0 to detach.  Without a caller
  * workspace the handle grows one of its own with cudaMalloc on the first TF32
  * call that needs more (not capture-safe).  Errors: INVALID_VALUE. */
 tcgStatus_t tcg_set_workspace(tcgHandle_t h, void *ptr, size_t bytes);
 
 /* Bytes of workspace a tcg_gemm_strided_batched call with these arguments
- * needs (0 for the 16-bit paths).  Errors: INVALID_VALUE (NULL bytes). */
+ * needs on the current device with the default kernel options: TF32 rounded copies,
+ * plus the FP32 partial sums when the call splits K (see tcg_set_split_k); 0 for an
+ * unsplit 16-bit or FP8 call.  Errors: INVALID_VALUE (NULL bytes). */
 tcgStatus_t tcg_gemm_workspace_size(tcgOp_t transa, tcgOp_t transb, int64_t m, int64_t n,
                                     int64_t k, tcgDataType_t Atype,
                                     tcgComputeType_t compute, int64_t batch_count,
@@ -241,6 +245,34 @@ tcgStatus_t tcg_set_debug(tcgHandle_t h, uint64_t wait_limit_ns, int fault_injec
  * 8).  Both variants meet the same accuracy bound.  INVALID_VALUE: NULL h,
  * cta_group outside 0..2, group_m outside 0..1024. */
 tcgStatus_t tcg_set_kernel_options(tcgHandle_t h, int cta_group, int group_m);
+
+/* K splitting ("split-K"; not a step the pages describe -- a scheduling choice of this
+ * library for problems with few output tiles): the K range of every output tile is cut
+ * into `splits` consecutive ranges, each range's products are accumulated on their own
+ * (FP32, from zero), the partial sums land in an FP32 workspace and a second kernel adds
+ * them in range order in FP32 before alpha, beta and the output rounding are applied.
+ * The result stays inside the accuracy bound of tcg_gemm_ex; it is not the unsplit
+ * accumulation bit for bit.
+ * tcg_set_split_k: 0 (default) splits automatically -- only when the tiles (times the
+ * batch) fill less than half of the GPU's SM pairs, into at most 64 ranges of at least
+ * four 2x128-byte K blocks each; 1 never splits; 2..64 forces that many ranges (fewer if
+ * K is short).  INVALID_VALUE: NULL h, splits outside 0..64. */
+tcgStatus_t tcg_set_split_k(tcgHandle_t h, int splits);
+
+/* The split a problem of tiles output tiles (times batch) and num_k_blocks K blocks gets
+ * on a GPU with `clusters` tile slots, with `forced` as in tcg_set_split_k: *splits
+ * ranges (1: none) of *kb_per_split K blocks, the last one possibly shorter, none empty.
+ * Pure host arithmetic, no device needed.  INVALID_VALUE: NULL outputs, negative
+ * arguments, forced > 64. */
+tcgStatus_t tcg_split_k_plan(int64_t tiles, int num_k_blocks, int clusters, int forced,
+                             int *splits, int *kb_per_split);
+
+/* The split the next call of this shape on h will use: *splits ranges of *k_per_split K
+ * elements (the last one possibly shorter).  Binds h to the current device like a GEMM
+ * call.  INVALID_VALUE: NULL h or outputs, negative sizes, unknown Atype. */
+tcgStatus_t tcg_gemm_split_k(tcgHandle_t h, int64_t m, int64_t n, int64_t k,
+                             tcgDataType_t Atype, tcgComputeType_t compute, int64_t batch_count,
+                             int *splits, int64_t *k_per_split);
 
 /* Number of GEMM-path kernel launches this handle has made (for the
  * benchmark's launch count).  Returns 0 for NULL. */

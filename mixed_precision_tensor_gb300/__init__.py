@@ -39,7 +39,8 @@ EXPORTS = ("tcg_create", "tcg_destroy", "tcg_set_stream", "tcg_set_workspace",
            "tcg_gemm_workspace_size", "tcg_gemm_ex", "tcg_gemm_strided_batched",
            "tcg_get_device_error", "tcg_last_device_error_bits", "tcg_status_string",
            "tcg_set_debug", "tcg_launch_count", "tcg_set_kernel_options",
-           "tcg_gemm_tf32_noalloc")
+           "tcg_gemm_tf32_noalloc", "tcg_set_split_k", "tcg_split_k_plan",
+           "tcg_gemm_split_k")
 
 _lock = threading.Lock()
 _lib = None
@@ -95,6 +96,13 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.tcg_launch_count.argtypes = [vp]
         lib.tcg_set_kernel_options.restype = st
         lib.tcg_set_kernel_options.argtypes = [vp, ci, ci]
+        lib.tcg_set_split_k.restype = st
+        lib.tcg_set_split_k.argtypes = [vp, ci]
+        lib.tcg_split_k_plan.restype = st
+        lib.tcg_split_k_plan.argtypes = [i64, ci, ci, ci, ctypes.POINTER(ci), ctypes.POINTER(ci)]
+        lib.tcg_gemm_split_k.restype = st
+        lib.tcg_gemm_split_k.argtypes = [vp, i64, i64, i64, ci, ci, i64, ctypes.POINTER(ci),
+                                         ctypes.POINTER(i64)]
         lib.tcg_gemm_tf32_noalloc.restype = st
         lib.tcg_gemm_tf32_noalloc.argtypes = [vp, ci, ci, i64, i64, i64, f32, vp, i64, vp, i64,
                                               f32, vp, i64]
@@ -179,6 +187,26 @@ def tcg_launch_count(h: int) -> int:
 
 def tcg_set_kernel_options(h: int, cta_group: int = 0, group_m: int = 0) -> int:
     return load_library().tcg_set_kernel_options(h, cta_group, group_m)
+
+
+def tcg_set_split_k(h: int, splits: int = 0) -> int:
+    return load_library().tcg_set_split_k(h, splits)
+
+
+def tcg_split_k_plan(tiles: int, num_k_blocks: int, clusters: int, forced: int = 0):
+    """(status, splits, kb_per_split) of the split-K rule (pure host arithmetic)."""
+    s, kb = ctypes.c_int(0), ctypes.c_int(0)
+    st = load_library().tcg_split_k_plan(tiles, num_k_blocks, clusters, forced, ctypes.byref(s),
+                                         ctypes.byref(kb))
+    return st, s.value, kb.value
+
+
+def tcg_gemm_split_k(h: int, m: int, n: int, k: int, Atype: int, compute: int, batch: int = 1):
+    """(status, splits, k_per_split) the next call of this shape on h will use."""
+    s, kps = ctypes.c_int(0), ctypes.c_int64(0)
+    st = load_library().tcg_gemm_split_k(h, m, n, k, Atype, compute, batch, ctypes.byref(s),
+                                         ctypes.byref(kps))
+    return st, s.value, kps.value
 
 
 def tcg_gemm_tf32_noalloc(stream, transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C,

@@ -65,6 +65,7 @@ struct tcgContext {
     uint32_t last_err_bits = 0;
     int cta_group = 2;
     int group_m = 0;           // 0: choose per problem
+    int split_k = 0;           // 0: choose per problem, 1: never split, >= 2: that many ranges
     int max_ctas[3] = {0, 0, 0};
     bool used = false;
     EncodeTiledFn encode = nullptr;
@@ -325,6 +326,53 @@ size_t tf32_ws_bytes(int64_t m, int64_t n, int64_t k, int64_t batch)
     return a + b;
 }
 
+// Partial-sum workspace of a split-K call: batch * splits slices of round_up(m, 4) x n
+// FP32 values.
+size_t splitk_ws_bytes(int64_t m, int64_t n, int64_t batch, int splits)
+{
+    const int64_t ldw = (m + 3) / 4 * 4;
+    return ((size_t)(batch * splits) * (size_t)(ldw * n) * 4 + 255) / 256 * 256;
+}
+
+// The K split the GEMM of this problem gets on handle h (see split_plan).
+SplitPlan plan_for(tcgContext *h, int64_t m, int64_t n, int64_t k, int64_t batch, int es, int cg)
+{
+    if (h->max_ctas[cg] == 0)
+        h->max_ctas[cg] = gemm_max_resident_ctas(cg, h->num_sms);
+    const int64_t k_block = static_cast<int64_t>(kDepth) * (128 / es);
+    const int nkb = static_cast<int>((k + k_block - 1) / k_block);
+    const int64_t tiles = ((m + kBM * cg - 1) / (kBM * cg)) * ((n + kBN - 1) / kBN) * batch;
+    return split_plan(tiles, nkb, h->max_ctas[cg] / cg, h->split_k);
+}
+
+// Device workspace of at least `need` bytes: the caller's (tcg_set_workspace) or one the
+// handle grows with cudaMalloc.
+tcgStatus_t acquire_ws(tcgContext *h, size_t need, void **ws)
+{
+    if (h->ws_user) {
+        if (h->ws_user_bytes < need)
+            return TCG_STATUS_INVALID_VALUE;
+        *ws = h->ws_user;
+        return TCG_STATUS_SUCCESS;
+    }
+    if (h->ws_own_bytes < need) {
+        if (h->ws_own) {
+            cudaStreamSynchronize(h->stream);
+            cudaFree(h->ws_own);
+            h->ws_own = nullptr;
+            h->ws_own_bytes = 0;
+        }
+        if (cudaMalloc(&h->ws_own, need) != cudaSuccess) {
+            cudaGetLastError();
+            h->ws_own = nullptr;
+            return TCG_STATUS_ALLOC_FAILED;
+        }
+        h->ws_own_bytes = need;
+    }
+    *ws = h->ws_own;
+    return TCG_STATUS_SUCCESS;
+}
+
 tcgStatus_t run(tcgContext *h, const Problem &p)
 {
     tcgStatus_t st = check_args(p);
@@ -355,6 +403,20 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
     // TF32 compute and the three-product split both run on rounded K-major copies.
     const bool split3 = p.compute == TCG_COMPUTE_32F_3XTF32;
     const bool tf32 = p.compute == TCG_COMPUTE_32F_FAST_TF32 || split3;
+    const int cg = h->cta_group;
+    const SplitPlan plan = plan_for(h, p.m, p.n, p.k, p.batch, tf32 ? 4 : elem_size(p.Atype), cg);
+    const size_t tf32_bytes = tf32 ? (split3 ? 2 : 1) * tf32_ws_bytes(p.m, p.n, p.k, p.batch) : 0;
+    const size_t splitk_bytes = plan.splits > 1 ? splitk_ws_bytes(p.m, p.n, p.batch, plan.splits)
+                                                : 0;
+    void *ws = nullptr;
+    if (tf32_bytes + splitk_bytes > 0) {
+        st = acquire_ws(h, tf32_bytes + splitk_bytes, &ws);
+        if (st != TCG_STATUS_SUCCESS)
+            return st;
+    }
+    float *W = splitk_bytes ? reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + tf32_bytes)
+                            : nullptr;
+    const int64_t ldw = (p.m + 3) / 4 * 4;
     const void *Aop = p.A, *Bop = p.B;
     const void *Alo = nullptr, *Blo = nullptr;
     bool a_kmajor = p.transa == TCG_OP_T;   // op(A) = A^T: K is A's contiguous dim
@@ -368,29 +430,6 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
         // 13 bits of FP32 input): K-major operands are rounded in place order, M/N-major
         // ones transposed on the way.  The split also writes the low words (x - hi).
         const size_t one = tf32_ws_bytes(p.m, p.n, p.k, p.batch);
-        const size_t need = split3 ? 2 * one : one;
-        void *ws = nullptr;
-        if (h->ws_user) {
-            if (h->ws_user_bytes < need)
-                return TCG_STATUS_INVALID_VALUE;
-            ws = h->ws_user;
-        } else {
-            if (h->ws_own_bytes < need) {
-                if (h->ws_own) {
-                    cudaStreamSynchronize(h->stream);
-                    cudaFree(h->ws_own);
-                    h->ws_own = nullptr;
-                    h->ws_own_bytes = 0;
-                }
-                if (cudaMalloc(&h->ws_own, need) != cudaSuccess) {
-                    cudaGetLastError();
-                    h->ws_own = nullptr;
-                    return TCG_STATUS_ALLOC_FAILED;
-                }
-                h->ws_own_bytes = need;
-            }
-            ws = h->ws_own;
-        }
         const int64_t kp = (p.k + 3) / 4 * 4;
         uint8_t *Ak = static_cast<uint8_t *>(ws);
         uint8_t *Bk = Ak + ((size_t)(p.batch * p.m * kp) * 4 + 255) / 256 * 256;
@@ -421,15 +460,16 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
         sB = sB == 0 ? 0 : p.n * kp;
     }
 
-    const int cg = h->cta_group;
     const bool fp8 = is_fp8(p.Atype);
     const tcgDataType_t at = tf32 ? TCG_R_32F : p.Atype;
+    const bool splitk = plan.splits > 1;
+    // The GEMM kernel writes D -- or, split, the FP32 partial sums (slice b * splits + s).
     CUtensorMap tmD;
-    st = output_map(h, p.C, p.Ctype, p.m, p.n, p.ldc, strideC, p.batch, &tmD);
+    st = splitk ? output_map(h, W, TCG_R_32F, p.m, p.n, ldw, ldw * p.n, p.batch * plan.splits,
+                             &tmD)
+                : output_map(h, p.C, p.Ctype, p.m, p.n, p.ldc, strideC, p.batch, &tmD);
     if (st != TCG_STATUS_SUCCESS)
         return st;
-    if (h->max_ctas[cg] == 0)
-        h->max_ctas[cg] = gemm_max_resident_ctas(cg, h->num_sms);
 
     // One launch of the GEMM kernel: D = alpha * opA * opB + beta * C.
     auto gemm_launch = [&](const void *opA, const void *opB, float beta) -> tcgStatus_t {
@@ -441,7 +481,9 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
         const int es = elem_size(at);
         a.k_row = 128 / es;                           // one 128-byte swizzle row of K
         a.num_k_blocks = (k + kDepth * a.k_row - 1) / (kDepth * a.k_row);
-        a.total_tiles = a.num_m_tiles * a.num_n_tiles * batch;
+        a.k_splits = plan.splits;
+        a.kb_per_split = plan.kb_per_split;
+        a.total_tiles = a.num_m_tiles * a.num_n_tiles * batch * plan.splits;
         a.group_m = h->group_m > 0 ? h->group_m : 8;
         a.kind = tf32 ? kKindTF32 : (fp8 ? kKindF8 : kKindF16);
         // operand format codes: kind::f16 F16 = 0, BF16 = 1; kind::tf32 TF32 = 2;
@@ -455,16 +497,18 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
                   | ((b_kmajor ? 0u : 1u) << 16)          // B: 0 = K-major, 1 = N-major
                   | (static_cast<uint32_t>(kBN >> 3) << 17)
                   | (static_cast<uint32_t>((kBM * cg) >> 4) << 24);   // M = 128 or 256
-        a.alpha = p.alpha;
-        a.beta = beta;
+        // Split, the kernel writes the raw FP32 accumulators (alpha 1, beta 0) into the
+        // partial-sum slices and the reduction applies alpha and beta.
+        a.alpha = splitk ? 1.0f : p.alpha;
+        a.beta = splitk ? 0.0f : beta;
         // Four C buffers (one operand stage less) when the epilogue's C/D traffic
         // outweighs the main loop: K bytes per row <= 1024 x D's element size.
-        a.c_bufs = beta == 0.0f ? 0
+        a.c_bufs = a.beta == 0.0f ? 0
                  : (cg == 2 && k * es <= 1024 * elem_size(p.Ctype) ? 4 : 2);
-        a.C = p.C;
-        a.D = p.C;
-        a.ldc = p.ldc;
-        a.strideC = strideC;
+        a.C = splitk ? static_cast<const void *>(W) : p.C;
+        a.D = splitk ? static_cast<void *>(W) : p.C;
+        a.ldc = splitk ? ldw : p.ldc;
+        a.strideC = splitk ? ldw * p.n : strideC;
         a.err = h->d_err;
         a.wait_limit_ns = h->wait_limit_ns;
         a.fault_inject = h->fault_inject;
@@ -482,8 +526,19 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
         a.b_bcast = bbc ? 1 : 0;
         const int64_t want = static_cast<int64_t>(a.total_tiles) * cg;
         const int grid = static_cast<int>(want < h->max_ctas[cg] ? want : h->max_ctas[cg]);
-        cudaError_t e = launch_gemm(tmA, tmB, tmD, a, ok, cg, grid, h->stream);
+        cudaError_t e = launch_gemm(tmA, tmB, tmD, a, splitk ? static_cast<int>(kOutF32) : ok,
+                                    cg, grid, h->stream);
         h->launches += 1;
+        if (e == cudaSuccess && splitk) {
+            const int64_t total = p.m * p.n * p.batch;
+            int64_t blocks = (total + 255) / 256;
+            const int64_t cap = static_cast<int64_t>(h->num_sms) * 8;
+            if (blocks > cap)
+                blocks = cap;
+            e = launch_splitk_reduce(W, ldw, plan.splits, m, n, batch, p.alpha, beta, p.C,
+                                     p.ldc, strideC, ok, static_cast<int>(blocks), h->stream);
+            h->launches += 1;
+        }
         return e == cudaSuccess ? TCG_STATUS_SUCCESS : TCG_STATUS_EXECUTION_FAILED;
     };
 
@@ -559,6 +614,23 @@ tcgStatus_t tcg_gemm_workspace_size(tcgOp_t transa, tcgOp_t transb, int64_t m, i
             *bytes = tf32_ws_bytes(m, n, k, batch_count);
         else if (compute == TCG_COMPUTE_32F_3XTF32)
             *bytes = 2 * tf32_ws_bytes(m, n, k, batch_count);
+    }
+    // Split-K partial sums, as a handle with default options would split on the current
+    // device (its SM count; at most kMaxSplits slices).
+    if (k > 0 && m > 0 && n > 0 && batch_count > 0) {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();          // no device: no GEMM can run, nothing to split
+            return TCG_STATUS_SUCCESS;
+        }
+        const int es = Atype == TCG_R_32F ? 4 : elem_size(Atype);
+        const int64_t k_block = static_cast<int64_t>(kDepth) * (128 / es);
+        const int nkb = static_cast<int>((k + k_block - 1) / k_block);
+        const int64_t tiles = ((m + 2 * kBM - 1) / (2 * kBM)) * ((n + kBN - 1) / kBN) * batch_count;
+        const SplitPlan pl = split_plan(tiles, nkb, sms / 2, 0);
+        if (pl.splits > 1)
+            *bytes += splitk_ws_bytes(m, n, batch_count, pl.splits);
     }
     return TCG_STATUS_SUCCESS;
 }
@@ -642,6 +714,44 @@ tcgStatus_t tcg_set_kernel_options(tcgHandle_t h, int cta_group, int group_m)
         return TCG_STATUS_INVALID_VALUE;
     h->cta_group = cta_group ? cta_group : 2;
     h->group_m = group_m;
+    return TCG_STATUS_SUCCESS;
+}
+
+tcgStatus_t tcg_set_split_k(tcgHandle_t h, int splits)
+{
+    if (!h || splits < 0 || splits > kMaxSplits)
+        return TCG_STATUS_INVALID_VALUE;
+    h->split_k = splits;
+    return TCG_STATUS_SUCCESS;
+}
+
+tcgStatus_t tcg_split_k_plan(int64_t tiles, int num_k_blocks, int clusters, int forced,
+                             int *splits, int *kb_per_split)
+{
+    if (!splits || !kb_per_split || tiles < 0 || num_k_blocks < 0 || clusters < 0 ||
+        forced < 0 || forced > kMaxSplits)
+        return TCG_STATUS_INVALID_VALUE;
+    const SplitPlan pl = split_plan(tiles, num_k_blocks, clusters, forced);
+    *splits = pl.splits;
+    *kb_per_split = pl.kb_per_split;
+    return TCG_STATUS_SUCCESS;
+}
+
+tcgStatus_t tcg_gemm_split_k(tcgHandle_t h, int64_t m, int64_t n, int64_t k,
+                             tcgDataType_t Atype, tcgComputeType_t compute, int64_t batch_count,
+                             int *splits, int64_t *k_per_split)
+{
+    if (!h || !splits || !k_per_split || m < 0 || n < 0 || k < 0 || batch_count < 0 ||
+        !valid_type(Atype))
+        return TCG_STATUS_INVALID_VALUE;
+    tcgStatus_t st = bind_device(h);
+    if (st != TCG_STATUS_SUCCESS)
+        return st;
+    const bool tf32 = compute == TCG_COMPUTE_32F_FAST_TF32 || compute == TCG_COMPUTE_32F_3XTF32;
+    const int es = tf32 ? 4 : elem_size(Atype);
+    const SplitPlan pl = plan_for(h, m, n, k, batch_count, es, h->cta_group);
+    *splits = pl.splits;
+    *k_per_split = static_cast<int64_t>(pl.kb_per_split) * kDepth * (128 / es);
     return TCG_STATUS_SUCCESS;
 }
 
@@ -791,6 +901,8 @@ extern "C" tcgStatus_t tcg_gemm_tf32_noalloc(void *stream, tcgOp_t transa, tcgOp
     a.num_n_tiles = static_cast<int>((n + kBN - 1) / kBN);
     a.k_row = 32;
     a.num_k_blocks = static_cast<int>((k + kDepth * 32 - 1) / (kDepth * 32));
+    a.k_splits = 1;                              // never split: no partial-sum workspace
+    a.kb_per_split = a.num_k_blocks;
     a.total_tiles = a.num_m_tiles * a.num_n_tiles;
     a.group_m = 8;
     a.kind = kKindTF32;

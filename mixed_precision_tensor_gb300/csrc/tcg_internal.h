@@ -81,7 +81,9 @@ struct GemmArgs {
     int m, n, k;
     int batch;
     int num_m_tiles, num_n_tiles, num_k_blocks;   // K blocks of kDepth * k_row elements
-    int total_tiles;
+    int total_tiles;           // work units: tiles x k_splits
+    int k_splits;              // K ranges per tile (1: no split)
+    int kb_per_split;          // K blocks per range (the last one may be shorter)
     int group_m;               // tile rasterisation: group of m-tiles walked together
     int a_mode, b_mode;        // OperandMode of A and B
     int a_bcast, b_bcast;      // batch stride 0: always batch coordinate 0
@@ -98,6 +100,43 @@ struct GemmArgs {
     int c_bufs;                // 0 (beta == 0), 2 or 4: epilogue variant (see TileCfg)
 };
 
+// K splitting for problems with few tiles ("split-K"): each tile's K blocks are cut into
+// k_splits ranges of kb_per_split blocks, every (tile, range) is a work unit whose FP32
+// accumulator goes to a partial-sum workspace (slice b * k_splits + s), and
+// launch_splitk_reduce adds the slices in range order and applies alpha, beta and the
+// output rounding.  Split only when the tiles fill less than half of the clusters, with
+// at least kMinSplitBlocks K blocks per range and at most kMaxSplits ranges; none of the
+// ranges is empty.
+constexpr int kMinSplitBlocks = 4;
+constexpr int kMaxSplits = 64;
+struct SplitPlan {
+    int splits;
+    int kb_per_split;
+};
+inline SplitPlan split_plan(int64_t tiles, int num_k_blocks, int clusters, int forced)
+{
+    SplitPlan pl{1, num_k_blocks};
+    int s;
+    if (forced >= 1) {
+        s = forced;
+    } else {
+        if (tiles <= 0 || tiles * 2 > clusters)
+            return pl;
+        s = static_cast<int>(clusters / tiles);
+        if (s > num_k_blocks / kMinSplitBlocks)
+            s = num_k_blocks / kMinSplitBlocks;
+    }
+    if (s > kMaxSplits)
+        s = kMaxSplits;
+    if (s > num_k_blocks)
+        s = num_k_blocks;
+    if (s < 2)
+        return pl;
+    pl.kb_per_split = (num_k_blocks + s - 1) / s;
+    pl.splits = (num_k_blocks + pl.kb_per_split - 1) / pl.kb_per_split;
+    return pl;
+}
+
 // Launchers (tcg_kernels.cu).  Return the launch's cudaError_t.
 // cta_group: 1 (128x256 tiles, one CTA) or 2 (256x256 tiles, CTA pairs; grid even).
 // tmD maps D (= C) as {m, n, batch} with box {128, epi_cols(out bytes), 1}, no swizzle.
@@ -107,6 +146,12 @@ cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
 int gemm_max_resident_ctas(int cta_group, int num_sms);
 cudaError_t launch_scale(void *D, const void *C, int m, int n, int64_t ldc, int64_t strideC,
                          int batch, float beta, int out_kind, int grid, cudaStream_t s);
+// D[b] = alpha * (W[b*splits] + W[b*splits + 1] + ... in that order, FP32) + beta * C[b]
+// (fma in FP32 when beta != 0), rounded to the output type; W slices are m x n FP32,
+// column-major with leading dimension ldw and slice stride ldw * n.  C is D (in place).
+cudaError_t launch_splitk_reduce(const float *W, int64_t ldw, int splits, int m, int n, int batch,
+                                 float alpha, float beta, void *D, int64_t ldc, int64_t strideC,
+                                 int out_kind, int grid, cudaStream_t s);
 // Round FP32 -> TF32 (nearest even).  The tensor core takes TF32 operands K-major only
 // and truncates the low 13 bits of FP32 input, so every TF32 operand gets a rounded,
 // K-major copy: launch_tf32_round keeps an operand that is already K-major (rows = K,

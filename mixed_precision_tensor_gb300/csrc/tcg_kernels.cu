@@ -90,8 +90,13 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, Smem
     }
 }
 
-__device__ __forceinline__ void tile_coords(const GemmArgs &p, int t, int &b, int &mt, int &nt)
+// Work unit u -> (batch b, m-tile mt, n-tile nt) with grouped rasterisation, and its
+// K split s (u = tile * k_splits + s; K blocks [s, s + 1) * kb_per_split).
+__device__ __forceinline__ void tile_coords(const GemmArgs &p, int u, int &b, int &mt, int &nt,
+                                            int &s)
 {
+    const int t = u / p.k_splits;
+    s = u - t * p.k_splits;
     const int per_batch = p.num_m_tiles * p.num_n_tiles;
     b = t / per_batch;
     const int r = t - b * per_batch;
@@ -271,12 +276,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool skip_once = p.fault_inject != 0 && leader;
             bool ok = true;
             for (int t = cluster_id; ok && t < p.total_tiles; t += num_clusters) {
-                int b, mt, nt;
-                tile_coords(p, t, b, mt, nt);
+                int b, mt, nt, ks;
+                tile_coords(p, t, b, mt, nt, ks);
+                const int kb_begin = ks * p.kb_per_split;
+                const int kb_end = min(kb_begin + p.kb_per_split, p.num_k_blocks);
                 const int m0 = mt * kTileM + static_cast<int>(rank) * kBM;
                 const int n0 = nt * kBN + static_cast<int>(rank) * kBRows;
                 const int za = p.a_bcast ? 0 : b, zb = p.b_bcast ? 0 : b;
-                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                for (int kb = kb_begin; kb < kb_end; ++kb) {
                     const uint32_t fb_local = smem_u32(&ctl->full[stage]);
                     const uint32_t fb = (CG == 2) ? mapa_shared(fb_local, 0) : fb_local;
                     if (!wait_bounded<CG>(smem_u32(&ctl->empty[stage]), phase ^ 1u, ctl, p,
@@ -335,6 +342,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             int it = 0;
             bool ok = true;
             for (int t = cluster_id; ok && t < p.total_tiles; t += num_clusters, ++it) {
+                const int ks = t % p.k_splits;
+                const int kb_begin = ks * p.kb_per_split;
+                const int kb_end = min(kb_begin + p.kb_per_split, p.num_k_blocks);
                 const int acc = it & 1;
                 const uint32_t acc_phase = (it >> 1) & 1;
                 if (!wait_bounded<CG>(smem_u32(&ctl->acc_empty[acc]), acc_phase ^ 1u, ctl, p,
@@ -344,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
-                for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+                for (int kb = kb_begin; kb < kb_end; ++kb) {
                     if (!wait_bounded<CG>(smem_u32(&ctl->full[stage]), phase, ctl, p,
                                           kErrMmaFull)) {
                         ok = false;
@@ -357,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int kk = 0; kk < kMmasPerStage; ++kk) {
                         const uint64_t ad = ad_s + a_off[kk];
                         const uint64_t bd = bd_s + b_off[kk];
-                        const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+                        const uint32_t accum = (kb > kb_begin || kk > 0) ? 1u : 0u;
                         if constexpr (CG == 2) {
                             if constexpr (KIND == kKindTF32)
                                 mma_tf32_pair(d_tmem, ad, bd, p.idesc, accum);
@@ -423,17 +433,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t *stage0_ptr = epi_ptr + half * kEpiBufs * kEpiChunkBytes;
         const int rl = q * 32 + lane;                           // row within the CTA's 128
 
-        // Origin (first row, first column, batch) of chunk number gg of this half.
+        // Origin (first row, first column, slice) of chunk number gg of this half.  With
+        // K splits, D is the partial-sum workspace and unit (b, s) goes to slice
+        // b * k_splits + s.
         auto chunk_origin = [&](uint32_t gg, int &x, int &y, int &z) -> bool {
             const int tile = cluster_id + static_cast<int>(gg / kChunks) * num_clusters;
             if (tile >= p.total_tiles)
                 return false;
             const int c = static_cast<int>(gg % kChunks);
-            int b, mt, nt;
-            tile_coords(p, tile, b, mt, nt);
+            int b, mt, nt, ks;
+            tile_coords(p, tile, b, mt, nt, ks);
             x = mt * kTileM + static_cast<int>(rank) * kBM;
             y = nt * kBN + half * (kBN / 2) + c * kCols;
-            z = b;
+            z = b * p.k_splits + ks;
             return true;
         };
         // Leader: start the C load of chunk gg (if it exists) into buffer gg % kEpiBufs.
@@ -594,6 +606,39 @@ __global__ void tcg_scale_kernel(void *D, const void *C, int m, int n, int64_t l
         const int64_t i = r - j * m;
         const int64_t idx = b * strideC + i + j * ldc;
         const float v = (beta == 0.0f) ? 0.0f : beta * load_c<OUT>(C, idx);
+        store_out<OUT>(D, idx, v);
+    }
+}
+
+// Split-K reduction: D = alpha * sum_s W_s + beta * C, the partial sums W_s (FP32, one
+// slice per K range of every batch entry) added in range order in FP32, then the same
+// epilogue arithmetic as the GEMM kernel (alpha * acc, fma with beta * C, one rounding to
+// the output type).  Grid-stride over the m x n x batch elements, consecutive threads on
+// consecutive rows (coalesced in every slice and in C/D).
+template <int OUT>
+__global__ void __launch_bounds__(256) tcg_splitk_reduce_kernel(const float *__restrict__ W,
+                                                                int64_t ldw, int splits, int m,
+                                                                int n, int batch, float alpha,
+                                                                float beta, void *D, int64_t ldc,
+                                                                int64_t strideC)
+{
+    const int64_t per = static_cast<int64_t>(m) * n;
+    const int64_t total = per * batch;
+    const int64_t slice = ldw * n;
+    for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t b = e / per;
+        const int64_t r = e - b * per;
+        const int64_t j = r / m;
+        const int64_t i = r - j * m;
+        const float *w = W + b * splits * slice + i + j * ldw;
+        float acc = w[0];
+        for (int s = 1; s < splits; ++s)
+            acc = __fadd_rn(acc, w[s * slice]);
+        const int64_t idx = b * strideC + i + j * ldc;
+        float v = __fmul_rn(alpha, acc);
+        if (beta != 0.0f)
+            v = __fmaf_rn(beta, load_c<OUT>(D, idx), v);
         store_out<OUT>(D, idx, v);
     }
 }
@@ -889,6 +934,27 @@ cudaError_t launch_scale(void *D, const void *C, int m, int n, int64_t ldc, int6
     case kOutF32: tcg_scale_kernel<kOutF32><<<grid, 256, 0, s>>>(D, C, m, n, ldc, strideC, batch, beta); break;
     case kOutF16: tcg_scale_kernel<kOutF16><<<grid, 256, 0, s>>>(D, C, m, n, ldc, strideC, batch, beta); break;
     default: tcg_scale_kernel<kOutBF16><<<grid, 256, 0, s>>>(D, C, m, n, ldc, strideC, batch, beta); break;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_splitk_reduce(const float *W, int64_t ldw, int splits, int m, int n, int batch,
+                                 float alpha, float beta, void *D, int64_t ldc, int64_t strideC,
+                                 int out_kind, int grid, cudaStream_t s)
+{
+    switch (out_kind) {
+    case kOutF32:
+        tcg_splitk_reduce_kernel<kOutF32><<<grid, 256, 0, s>>>(W, ldw, splits, m, n, batch, alpha,
+                                                               beta, D, ldc, strideC);
+        break;
+    case kOutF16:
+        tcg_splitk_reduce_kernel<kOutF16><<<grid, 256, 0, s>>>(W, ldw, splits, m, n, batch, alpha,
+                                                               beta, D, ldc, strideC);
+        break;
+    default:
+        tcg_splitk_reduce_kernel<kOutBF16><<<grid, 256, 0, s>>>(W, ldw, splits, m, n, batch, alpha,
+                                                                beta, D, ldc, strideC);
+        break;
     }
     return cudaGetLastError();
 }

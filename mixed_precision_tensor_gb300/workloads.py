@@ -61,13 +61,16 @@ WORKLOADS = {
                                           "f32", "f32", 1.0, 0.0, 1, 3, "uniform"),
     "fp16_batched_512x256": Workload("fp16_batched_512x256", 256, 256, 256, "f16", "f16", 1.0,
                                      0.5, 512, 4, "pow2"),
-    # not one of the five above: FP8 inputs on the headline shape, and the multi-word
-    # (3xTF32) variant of the TF32 workload
+    # not one of the five above: FP8 inputs on the headline shape, the multi-word (3xTF32)
+    # variant of the TF32 workload, and a split-K shape
     "fp8e4m3_gemm_8192": Workload("fp8e4m3_gemm_8192", 8192, 8192, 8192, "e4m3", "f32", 1.0,
                                   0.0, 1, 1, "uniform"),
     "fp32_3xtf32_4096x4096x16384": Workload("fp32_3xtf32_4096x4096x16384", 4096, 4096, 16384,
                                             "f32", "f32", 1.0, 0.0, 1, 3, "uniform",
                                             "3xtf32"),
+    # one 256 x 256 output tile with a long K: the split-K case
+    "fp16_splitk_256x256x65536": Workload("fp16_splitk_256x256x65536", 256, 256, 65536, "f16",
+                                          "f32", 1.0, 0.0, 1, 5, "uniform"),
 }
 # Canonical order: small check case first, the headline case second.
 WORKLOAD_ORDER = list(WORKLOADS)[:5]

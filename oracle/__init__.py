@@ -77,7 +77,7 @@ def _load():
         lib.orc_gemm_model.restype = ci
         lib.orc_gemm_model.argtypes = [ci, ci, i64, i64, i64, dbl, vp, ci, i64, vp, ci, i64,
                                        dbl, vp, ci, i64, ci, i64, i64, i64, i64, vp, i64,
-                                       ci, ci, ci, ci, ci]
+                                       ci, ci, ci, ci, ci, i64, ci]
         _lib = lib
         return lib
 
@@ -174,13 +174,15 @@ def gemm(transa, transb, m, n, k, alpha, A, atype, lda, B, btype, ldb, beta, C, 
 
 def gemm_model(transa, transb, m, n, k, alpha, A, atype, lda, B, btype, ldb, beta, C, ctype,
                ldc, tf32=False, rows=None, cols=None, nthreads=None, block=16, frac=25,
-               norm_rne=False, exp_sum=True):
+               norm_rne=False, exp_sum=True, splits=1, k_per_split=0):
     """Block of D = alpha*op(A)*op(B) + beta*C with the block-FMA model of ``tc_model.c``
     as the accumulator and the library's FP32 epilogue (arguments as :func:`gemm`):
     products in blocks of ``block``, terms cut toward zero ``frac`` bits below the
     block's largest alignment exponent (input-exponent sums if ``exp_sum``), each block
     sum rounded into the FP32 accumulator toward zero (to nearest even if
-    ``norm_rne``).  Returns D as an (i1-i0, j1-j0) array in the output storage type."""
+    ``norm_rne``).  ``splits`` > 1 accumulates K in ranges of ``k_per_split`` that are
+    added in order in FP32 (the library's split-K).  Returns D as an (i1-i0, j1-j0)
+    array in the output storage type."""
     i0, i1 = rows if rows is not None else (0, m)
     j0, j1 = cols if cols is not None else (0, n)
     nr, nc = i1 - i0, j1 - j0
@@ -195,7 +197,7 @@ def gemm_model(transa, transb, m, n, k, alpha, A, atype, lda, B, btype, ldb, bet
                                 float(beta), _ptr(C), int(ctype), int(ldc), int(bool(tf32)),
                                 int(i0), int(i1), int(j0), int(j1), _ptr(D), int(max(nr, 1)),
                                 int(block), int(frac), int(bool(norm_rne)), int(bool(exp_sum)),
-                                int(nthreads))
+                                int(splits), int(k_per_split), int(nthreads))
     if rc != 0:
         raise ValueError(f"orc_gemm_model failed with code {rc}")
     return D[: nr * nc].reshape(nc, nr).T

@@ -25,6 +25,10 @@
  *      * the cut terms are added exactly and the sum becomes the new FP32 accumulator,
  *        rounded toward zero (norm_rne = 0) or to nearest even (norm_rne = 1), FP32
  *        subnormals kept.
+ *  - With K split into ranges (the library's split-K scheduling, not a step of the pages)
+ *    every range of k_per_split products is accumulated on its own, from zero and with
+ *    blocks counted from the range's start, and the range results are added in range
+ *    order in FP32 (nearest even); that sum is the accumulator below.
  *  - The accumulator after the last block enters the GEMM's epilogue in FP32, as the
  *    library computes it: r = alpha * acc, then r = fma(beta, c, r) when beta != 0 (each
  *    rounded to nearest even in FP32; the order of these two roundings is the library's
@@ -198,7 +202,8 @@ typedef struct {
     void *D; int64_t ldd;
     const double *opA, *opB;                          /* decoded rows of op(A), columns of op(B) */
     const int *expA, *expB;
-    int block, frac, norm_rne, exp_sum;
+    int block, frac, norm_rne, exp_sum, splits;
+    int64_t k_per_split;
     int64_t jstart, jstop;                            /* this worker's columns (relative) */
 } model_job;
 
@@ -233,9 +238,16 @@ static void *model_worker(void *arg)
             if (no_product) {
                 r = g->beta == 0.0f ? 0.0f : g->beta * load_c32(g->C, g->ctype, i + j * g->ldc);
             } else {
-                float acc = model_dot(g->opA + ii * g->k, g->expA + ii * g->k,
-                                      g->opB + jj * g->k, g->expB + jj * g->k, g->k, g->block,
-                                      g->frac, g->norm_rne, g->exp_sum);
+                float acc = 0.0f;
+                for (int s = 0; s < g->splits; ++s) {
+                    int64_t p0 = s * g->k_per_split;
+                    int64_t p1 = p0 + g->k_per_split < g->k ? p0 + g->k_per_split : g->k;
+                    float part = model_dot(g->opA + ii * g->k + p0, g->expA + ii * g->k + p0,
+                                           g->opB + jj * g->k + p0, g->expB + jj * g->k + p0,
+                                           p1 - p0, g->block, g->frac, g->norm_rne,
+                                           g->exp_sum);
+                    acc = s == 0 ? part : acc + part;        /* FP32, nearest even */
+                }
                 r = g->alpha * acc;                                   /* FP32, nearest even */
                 if (g->beta != 0.0f)
                     r = fmaf(g->beta, load_c32(g->C, g->ctype, i + j * g->ldc), r);
@@ -249,7 +261,8 @@ static void *model_worker(void *arg)
 /*
  * orc_gemm_model: block [i0,i1) x [j0,j1) of D = alpha*op(A)*op(B) + beta*C with the
  * accumulator of the block-FMA model and the epilogue described at the top; arguments as
- * orc_gemm (column-major, BLAS style).  frac must be at most 60 and block at most 1023
+ * orc_gemm (column-major, BLAS style), plus the model's parameters and the K split
+ * (splits = 1: none; else ranges of k_per_split, the last one non-empty).  frac must be at most 60 and block at most 1023
  * (the cut terms of a block are summed as 128-bit integers).  Returns 0, -1 on bad
  * arguments, -2 on allocation failure.
  */
@@ -257,11 +270,14 @@ int orc_gemm_model(int transa, int transb, int64_t m, int64_t n, int64_t k, doub
                    const void *A, int atype, int64_t lda, const void *B, int btype, int64_t ldb,
                    double beta, const void *C, int ctype, int64_t ldc, int tf32, int64_t i0,
                    int64_t i1, int64_t j0, int64_t j1, void *D, int64_t ldd, int block, int frac,
-                   int norm_rne, int exp_sum, int nthreads)
+                   int norm_rne, int exp_sum, int splits, int64_t k_per_split, int nthreads)
 {
     if (m < 0 || n < 0 || k < 0 || i0 < 0 || i1 > m || i0 > i1 || j0 < 0 || j1 > n ||
-        j0 > j1 || ldd < i1 - i0 || block < 1 || block > 1023 || frac < 0 || frac > 60)
+        j0 > j1 || ldd < i1 - i0 || block < 1 || block > 1023 || frac < 0 || frac > 60 ||
+        splits < 1 || (splits > 1 && (k_per_split < 1 || (splits - 1) * k_per_split >= k)))
         return -1;
+    if (splits == 1)
+        k_per_split = k;
     int64_t rows = i1 - i0, cols = j1 - j0;
     if (rows == 0 || cols == 0)
         return 0;
@@ -311,6 +327,7 @@ int orc_gemm_model(int transa, int transb, int64_t m, int64_t n, int64_t k, doub
         g->D = D; g->ldd = ldd;
         g->opA = opA; g->opB = opB; g->expA = expA; g->expB = expB;
         g->block = block; g->frac = frac; g->norm_rne = norm_rne; g->exp_sum = exp_sum;
+        g->splits = splits; g->k_per_split = k_per_split;
         g->jstart = cols * t / nthreads;
         g->jstop = cols * (t + 1) / nthreads;
     }

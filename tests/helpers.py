@@ -67,7 +67,8 @@ def oracle_rowmajor(w, A, B, C, b=0, rows=None, cols=None, nthreads=None):
     return D.T, R.T, AB.T
 
 
-def model_rowmajor(w, A, B, C, b=0, rows=None, cols=None, nthreads=None):
+def model_rowmajor(w, A, B, C, b=0, rows=None, cols=None, nthreads=None, splits=1,
+                   k_per_split=0):
     """The block-FMA model (oracle.PAGE_MODEL parameters) for the same row-major problem
     and block as :func:`oracle_rowmajor`.  Returns D as a row-major block."""
     m, n, k = w.m, w.n, w.k
@@ -79,8 +80,8 @@ def model_rowmajor(w, A, B, C, b=0, rows=None, cols=None, nthreads=None):
     t = TYPE_CODE[w.in_type]
     D = oracle.gemm_model(oracle.OP_N, oracle.OP_N, n, m, k, w.alpha, Bb, t, n, Ab, t, k,
                           w.beta, Cb, TYPE_CODE[w.out_type], n, tf32=(w.in_type == "f32"),
-                          rows=(j0, j1), cols=(i0, i1), nthreads=nthreads,
-                          **oracle.PAGE_MODEL[t])
+                          rows=(j0, j1), cols=(i0, i1), nthreads=nthreads, splits=splits,
+                          k_per_split=k_per_split, **oracle.PAGE_MODEL[t])
     return D.T
 
 

@@ -158,3 +158,34 @@ def test_product_path_has_no_oracle_dependency():
                 text = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "tcg_oracle" not in text and "liboracle" not in text, f
+
+
+def test_split_k_plan_rule():
+    # Split only when the tiles fill less than half of the clusters; at least 4 K blocks
+    # per range; at most 64 ranges; no empty range.
+    plan = lambda *a: tcg.tcg_split_k_plan(*a)
+    assert plan(1, 512, 76) == (0, 64, 8)
+    assert plan(40, 512, 76)[1:] == (1, 512)            # 80 > 76: the GPU is busy enough
+    assert plan(10, 512, 76)[1] == 7                     # 76 // 10
+    assert plan(10, 12, 76)[1] == 3                      # at most 12 // 4 ranges
+    assert plan(1, 7, 76)[1:] == (1, 7)                  # too short to split
+    assert plan(500, 64, 76, 3)[1:] == (3, 22)           # forced
+    assert plan(1, 2, 76, 8)[1:] == (2, 1)               # forced, capped by the K blocks
+    for tiles in (1, 2, 5, 19, 37):
+        for nkb in (1, 4, 9, 33, 100, 1000):
+            for forced in (0, 2, 7, 64):
+                st, s, kb = plan(tiles, nkb, 76, forced)
+                assert st == 0 and 1 <= s <= 64
+                assert (s - 1) * kb < nkb <= s * kb          # every range non-empty
+                if s == 1:
+                    assert kb == nkb
+
+
+def test_split_k_argument_checks():
+    INV = tcg.TCG_STATUS_INVALID_VALUE
+    assert tcg.tcg_split_k_plan(-1, 4, 76)[0] == INV
+    assert tcg.tcg_split_k_plan(1, 4, 76, 65)[0] == INV
+    assert tcg.load_library().tcg_split_k_plan(1, 4, 76, 0, None, None) == INV
+    assert tcg.tcg_set_split_k(None, 2) == INV
+    assert tcg.tcg_gemm_split_k(None, 1, 1, 1, tcg.TCG_R_16F, tcg.TCG_COMPUTE_32F)[0] == INV
+

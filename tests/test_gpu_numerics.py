@@ -135,6 +135,7 @@ def test_issm_model_agreement(features, kind, dist):
     At, Bt = _case(kind, dist, m, n, k, seed)
     D = torch.zeros((n, m), dtype=torch.float32, device="cuda:0")      # column-major m x n
     h = tcg.Handle()
+    tcg.check(tcg.tcg_set_split_k(h.h, 1))        # one accumulation per output, no K split
     tcg.check(tcg.tcg_gemm_ex(h.h, tcg.TCG_OP_N, tcg.TCG_OP_N, m, n, k, 1.0, At.cuda(), f.code, m,
                               Bt.cuda(), f.code, k, 0.0, D, tcg.TCG_R_32F, m, f.compute))
     got = D.cpu().numpy().T                                          # (m, n)
@@ -160,6 +161,7 @@ def test_issm_large_uniform_sample(features, kind):
     Bt = _cast(rng.uniform(-1, 1, (n, k)), kind)
     D = torch.zeros((n, m), dtype=torch.float32, device="cuda:0")
     h = tcg.Handle()
+    tcg.check(tcg.tcg_set_split_k(h.h, 1))        # one accumulation per output, no K split
     tcg.check(tcg.tcg_gemm_ex(h.h, tcg.TCG_OP_N, tcg.TCG_OP_N, m, n, k, 1.0, At.cuda(), f.code, m,
                               Bt.cuda(), f.code, k, 0.0, D, tcg.TCG_R_32F, m, f.compute))
     got = D.cpu().numpy().T

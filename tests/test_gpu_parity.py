@@ -145,6 +145,9 @@ def run_colmajor(h, transa, transb, m, n, k, alpha, beta, in_t, out_t, seed, dis
     pad = body[:, : ldc * n].reshape(batch, n, ldc)[:, :, m:]
     guards_ok = guards_ok and np.array_equal(pad.view(np.uint8),
                                              np.full_like(pad, canary).view(np.uint8))
+    # the K split this call used (the model accumulates the same ranges)
+    st, splits, kps = tcg.tcg_gemm_split_k(h.h, m, n, k, CODE[in_t], comp, batch)
+    tcg.check(st, "split plan")
     results = []
     for b in range(batch):
         args = (transa, transb, m, n, k, alpha, Araw[b * sA:(b + 1) * sA], TYPE_CODE[in_t], lda,
@@ -152,7 +155,8 @@ def run_colmajor(h, transa, transb, m, n, k, alpha, beta, in_t, out_t, seed, dis
                 Cin[b * sC:(b + 1) * sC], TYPE_CODE[out_t], ldc)
         D, R, AB = oracle.gemm(*args, tf32=(in_t == "f32" and not split3))
         # the three-product FP32 emulation is three GEMMs: not one block-FMA accumulation
-        Dm = None if split3 else oracle.gemm_model(*args, tf32=(in_t == "f32"),
+        Dm = None if split3 else oracle.gemm_model(*args, tf32=(in_t == "f32"), splits=splits,
+                                                   k_per_split=kps,
                                                    **oracle.PAGE_MODEL[TYPE_CODE[in_t]])
         got = body[b, : ldc * n].reshape(n, ldc)[:, :m].T
         cdec = _decode(Cin[b * sC:(b + 1) * sC][: ldc * n].reshape(n, ldc)[:, :m].T, out_t)
@@ -371,6 +375,38 @@ def test_page_vectors_on_gpu(handle):
     assert v == model          # 2^-149 - 2^-157 truncated to the FP32 subnormal grid: 0
 
 
+# ------------------------------------------------------------ split-K
+SPLITK_CASES = [
+    # (m, n, k, in, out, alpha, beta, batch, forced splits)
+    (256, 256, 65536, "f16", "f32", 1.0, 0.0, 1, 0),
+    (100, 300, 20000, "bf16", "bf16", 0.5, 1.0, 1, 0),
+    (257, 129, 10000, "f32", "f32", 1.0, 0.0, 1, 0),
+    (128, 128, 16384, "f16", "f16", 1.0, 0.5, 3, 0),
+    (256, 256, 32768, "e4m3", "f32", 1.0, 0.0, 1, 0),
+    (300, 700, 5000, "f16", "f32", -1.0, 0.25, 1, 3),
+    (64, 64, 1000, "f16", "f32", 1.0, 0.0, 1, 64),
+]
+
+
+@pytest.mark.timeout(900)
+@pytest.mark.parametrize("m,n,k,in_t,out_t,alpha,beta,batch,forced", SPLITK_CASES)
+def test_split_k(cuda_device, m, n, k, in_t, out_t, alpha, beta, batch, forced):
+    """Few output tiles, long K: the K range is split (automatically, or forced), the
+    partial sums reduced in range order.  Within the bound of the exact oracle and bit-exact
+    against the block-FMA model with the same split."""
+    h = tcg.Handle()
+    tcg.check(tcg.tcg_set_split_k(h.h, forced))
+    comp = tcg.TCG_COMPUTE_32F_FAST_TF32 if in_t == "f32" else tcg.TCG_COMPUTE_32F
+    st, splits, kps = tcg.tcg_gemm_split_k(h.h, m, n, k, CODE[in_t], comp, batch)
+    assert st == 0 and splits > 1, (splits, kps)
+    for dist in ("uniform", "integer"):
+        res, guards = run_colmajor(h, N, N, m, n, k, alpha, beta, in_t, out_t,
+                                   seed=m + n + k + batch, dist=dist, batch=batch)
+        assert guards
+        _assert_results(res, k, alpha, beta, out_t, exact=(dist == "integer"))
+    h.close()
+
+
 # ------------------------------------------------------------ the five workloads
 def _device_inputs(w, A, B, C):
     dev = torch.device("cuda:0")
@@ -401,7 +437,15 @@ def _run_workload(handle, w, A, B, C):
     return out if w.batch > 1 else out[None]
 
 
-def _check_full(w, A, B, C, out, exact):
+def _plan(handle, w):
+    comp = tcg.TCG_COMPUTE_32F_FAST_TF32 if w.in_type == "f32" else tcg.TCG_COMPUTE_32F
+    st, splits, kps = tcg.tcg_gemm_split_k(handle.h, w.n, w.m, w.k, CODE[w.in_type], comp,
+                                           w.batch)
+    tcg.check(st, "split plan")
+    return dict(splits=splits, k_per_split=kps)
+
+
+def _check_full(w, A, B, C, out, exact, plan=None):
     for b in range(w.batch):
         D, R, AB = oracle_rowmajor(w, A, B, C, b=b)
         g = decode_out(raw(out[b]), w.out_type)
@@ -412,10 +456,11 @@ def _check_full(w, A, B, C, out, exact):
         else:
             ok, worst, idx = check_bound(g, ref, AB, cdec, w.k, w.alpha, w.beta, w.out_type)
             assert ok, f"batch {b}: worst normalised error {worst}"
-            _assert_model_equal(g, decode_out(raw(model_rowmajor(w, A, B, C, b=b)), w.out_type))
+            Dm = model_rowmajor(w, A, B, C, b=b, **(plan or {}))
+            _assert_model_equal(g, decode_out(raw(Dm), w.out_type))
 
 
-def _check_sampled(w, A, B, C, out, exact, count=64, model_tiles=8):
+def _check_sampled(w, A, B, C, out, exact, count=64, model_tiles=8, plan=None):
     tiles = wl.sample_tiles(w.m, w.n, count=count, tile=128, seed=w.seed)
     assert len(tiles) == min(count, (-(-w.m // 128)) * (-(-w.n // 128)))
     worst_all = 0.0
@@ -436,7 +481,7 @@ def _check_sampled(w, A, B, C, out, exact, count=64, model_tiles=8):
         # corners come first)
         for (i0, i1, j0, j1) in tiles[:model_tiles]:
             g = decode_out(raw(np.ascontiguousarray(out[0][i0:i1, j0:j1])), w.out_type)
-            Dm = model_rowmajor(w, A, B, C, rows=(i0, i1), cols=(j0, j1))
+            Dm = model_rowmajor(w, A, B, C, rows=(i0, i1), cols=(j0, j1), **(plan or {}))
             _assert_model_equal(g, decode_out(raw(np.ascontiguousarray(Dm)), w.out_type))
     return worst_all
 
@@ -450,7 +495,7 @@ def test_small_workload_full_random(handle, name):
     w = wl.WORKLOADS[name]
     A, B, C = wl.draw(w)
     out = _run_workload(handle, w, A, B, C)
-    _check_full(w, A, B, C, out, exact=False)
+    _check_full(w, A, B, C, out, exact=False, plan=_plan(handle, w))
 
 
 @pytest.mark.parametrize("name", SMALL)
@@ -467,7 +512,7 @@ def test_large_workload_sampled_random(handle, name):
     w = wl.WORKLOADS[name]
     A, B, C = wl.draw(w)
     out = _run_workload(handle, w, A, B, C)
-    worst = _check_sampled(w, A, B, C, out, exact=False)
+    worst = _check_sampled(w, A, B, C, out, exact=False, plan=_plan(handle, w))
     print(f"{name}: worst normalised error over 64 tiles = {worst:.3e}")
 
 

@@ -200,3 +200,32 @@ def test_truncation_error_stays_inside_the_bound():
     exact = Af @ Bf
     bound = k * 2.0 ** -23 * (np.abs(Af) @ np.abs(Bf))
     assert np.all(np.abs(D - exact) <= bound)
+
+
+def test_split_k_partials_are_added_in_fp32():
+    # K = 32 in two ranges of 16: range 0 = [1, 2^-23] -> 1 + 2^-23, range 1 = [1.5 * 2^-24]
+    # kept exactly on its own; their FP32 sum (nearest even) is 1 + 2^-22.  Unsplit, the
+    # second block meets the accumulator 1 + 2^-23 and the truncated sum stays 1 + 2^-23.
+    a = [1.0, 2.0 ** -23] + [0.0] * 14 + [1.5 * 2.0 ** -24] + [0.0] * 15
+    b = [1.0] * 32
+    assert dot(a, b, fmt=BF16, block=16, frac=25) == 1 + 2.0 ** -23
+    assert dot(a, b, fmt=BF16, block=16, frac=25, splits=2, k_per_split=16) == 1 + 2.0 ** -22
+
+
+def test_split_k_integer_data_is_exact():
+    # small integers: every partial and their sum are exact, whatever the split
+    rng = np.random.default_rng(6)
+    m, n, k = 12, 10, 300
+    A = rng.integers(-2, 3, (k, m)).astype(np.float16)
+    B = rng.integers(-2, 3, (n, k)).astype(np.float16)
+    ref = A.astype(np.float64).reshape(k, m).T @ B.astype(np.float64).reshape(n, k).T
+    for splits, kps in ((1, 0), (2, 256), (3, 128), (5, 64)):
+        D = oracle.dot_model(A.view(np.uint16), F16, B.view(np.uint16), F16, m, n, k,
+                             splits=splits, k_per_split=kps)
+        assert np.array_equal(D.astype(np.float64), ref), (splits, kps)
+
+
+def test_split_k_rejects_empty_ranges():
+    A = np.zeros(64, dtype=np.uint16)
+    with pytest.raises(ValueError):
+        oracle.dot_model(A, F16, A, F16, 1, 1, 64, splits=3, k_per_split=32)
