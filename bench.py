@@ -337,41 +337,36 @@ def run_ours(args, w):
     step_ms_max = max_over_ranks(step_ms, world)
     value = w.flops * world / (step_ms_max * 1e-3) / 1e12
 
-    # End to end through the C ABI: pinned host inputs -> device -> GEMM -> host result.
-    hA = host(A).pin_memory()
-    hB = host(B).pin_memory()
-    hC = host(C).pin_memory() if C is not None else None
-    hD = torch.empty(oshape, dtype=tdt[w.out_type] if w.out_type != "bf16" else torch.int16
-                     ).pin_memory()
+    # End to end through the C ABI's host-buffer call (tcg_gemm_ex_host /
+    # tcg_gemm_strided_batched_host): pinned host inputs, the copies in, the GEMM and the
+    # copy of D back into host memory all inside the timed region; the library pipelines
+    # the copies against the product.  Each call returns when D is in host memory.
+    views = {"bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+
+    def pinned(x, t):
+        tt = host(x).pin_memory()
+        return tt.view(views[t]) if t in views else tt
+    hA, hB = pinned(A, w.in_type), pinned(B, w.in_type)
+    hD = (pinned(C, w.out_type) if C is not None else
+          torch.zeros(oshape, dtype=torch.int16 if w.out_type == "bf16" else tdt[w.out_type]
+                      ).pin_memory())
+    if w.out_type == "bf16" and hD.dtype == torch.int16:
+        hD = hD.view(torch.bfloat16)
     e2e_steps = max(3, min(20, args.steps // 10))
-    h2d = hA.nbytes + hB.nbytes + (hC.nbytes if hC is not None else 0)
+    h2d = hA.nbytes + hB.nbytes + (hD.nbytes if C is not None else 0)
     d2h = hD.nbytes
 
-    in_views = {"bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
-
     def e2e_step():
-        dA.copy_(hA.view(in_views[w.in_type]) if w.in_type in in_views else hA,
-                 non_blocking=True)
-        dB.copy_(hB.view(in_views[w.in_type]) if w.in_type in in_views else hB,
-                 non_blocking=True)
-        if hC is not None:
-            dC.copy_(hC.view(torch.bfloat16) if w.out_type == "bf16" else hC, non_blocking=True)
-        step()
-        hD.copy_(dC.view(torch.int16) if w.out_type == "bf16" else dC, non_blocking=True)
+        tcg.gemm_rowmajor(h, hA, hB, hD, alpha=w.alpha, beta=w.beta, tf32=tf32,
+                          split3=w.compute == "3xtf32", host=True)
 
-    with torch.cuda.stream(stream):
-        e2e_step()
+    e2e_step()                                  # grows the handle's staging buffers
     torch.cuda.synchronize()
     barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / e2e_steps, world)
     e2e_value = w.flops * world / (e2e_ms * 1e-3) / 1e12
     tcg.check(tcg.tcg_get_device_error(h.h), "e2e")
 

@@ -177,6 +177,30 @@ tcgStatus_t tcg_gemm_strided_batched(tcgHandle_t h, tcgOp_t transa, tcgOp_t tran
                                      tcgDataType_t Ctype, int64_t ldc, int64_t strideC,
                                      int64_t batch_count, tcgComputeType_t compute);
 
+/* The same two calls with A, B and C in HOST memory (pinned memory gives the full copy
+ * bandwidth; pageable memory works).  The handle copies the operands into device buffers
+ * it keeps (grown with cudaMalloc on demand, freed by tcg_destroy; not capture-safe), runs
+ * the GEMM on its stream, copies D back into C and returns when C holds D.  The copies in
+ * and out are pipelined against the product: column panels of B/C (tcg_gemm_ex_host) or
+ * groups of batch entries (batched), up to four, each at least one wave of output tiles,
+ * copies in on one internal stream, copies out on another.  Arguments, layout rules
+ * (leading dimensions and strides; no alignment needed for the host pointers), accuracy
+ * and status codes as tcg_gemm_ex / tcg_gemm_strided_batched -- the result is theirs bit
+ * for bit -- plus ALLOC_FAILED when the device buffers cannot be had.  Rows >= m inside
+ * ldc and the gaps between batch entries of C are not written. */
+tcgStatus_t tcg_gemm_ex_host(tcgHandle_t h, tcgOp_t transa, tcgOp_t transb, int64_t m, int64_t n,
+                             int64_t k, float alpha, const void *A, tcgDataType_t Atype,
+                             int64_t lda, const void *B, tcgDataType_t Btype, int64_t ldb,
+                             float beta, void *C, tcgDataType_t Ctype, int64_t ldc,
+                             tcgComputeType_t compute);
+tcgStatus_t tcg_gemm_strided_batched_host(tcgHandle_t h, tcgOp_t transa, tcgOp_t transb,
+                                          int64_t m, int64_t n, int64_t k, float alpha,
+                                          const void *A, tcgDataType_t Atype, int64_t lda,
+                                          int64_t strideA, const void *B, tcgDataType_t Btype,
+                                          int64_t ldb, int64_t strideB, float beta, void *C,
+                                          tcgDataType_t Ctype, int64_t ldc, int64_t strideC,
+                                          int64_t batch_count, tcgComputeType_t compute);
+
 /*
  * TF32 GEMM that allocates nothing.  The pages have no counterpart to this entry
  * point: it exists for callers that cannot allocate device memory when they call

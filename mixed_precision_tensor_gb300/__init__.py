@@ -40,7 +40,7 @@ EXPORTS = ("tcg_create", "tcg_destroy", "tcg_set_stream", "tcg_set_workspace",
            "tcg_get_device_error", "tcg_last_device_error_bits", "tcg_status_string",
            "tcg_set_debug", "tcg_launch_count", "tcg_set_kernel_options",
            "tcg_gemm_tf32_noalloc", "tcg_set_split_k", "tcg_split_k_plan",
-           "tcg_gemm_split_k")
+           "tcg_gemm_split_k", "tcg_gemm_ex_host", "tcg_gemm_strided_batched_host")
 
 _lock = threading.Lock()
 _lib = None
@@ -84,6 +84,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.tcg_gemm_strided_batched.argtypes = [vp, ci, ci, i64, i64, i64, f32, vp, ci, i64,
                                                  i64, vp, ci, i64, i64, f32, vp, ci, i64, i64,
                                                  i64, ci]
+        lib.tcg_gemm_ex_host.restype = st
+        lib.tcg_gemm_ex_host.argtypes = lib.tcg_gemm_ex.argtypes
+        lib.tcg_gemm_strided_batched_host.restype = st
+        lib.tcg_gemm_strided_batched_host.argtypes = lib.tcg_gemm_strided_batched.argtypes
         lib.tcg_get_device_error.restype = st
         lib.tcg_get_device_error.argtypes = [vp]
         lib.tcg_last_device_error_bits.restype = ctypes.c_uint32
@@ -161,6 +165,23 @@ def tcg_gemm_strided_batched(h, transa, transb, m, n, k, alpha, A, Atype, lda, s
                              Btype, ldb, strideB, beta, C, Ctype, ldc, strideC, batch_count,
                              compute) -> int:
     return load_library().tcg_gemm_strided_batched(
+        h, transa, transb, m, n, k, float(alpha), _ptr(A), Atype, lda, strideA, _ptr(B), Btype,
+        ldb, strideB, float(beta), _ptr(C), Ctype, ldc, strideC, batch_count, compute)
+
+
+def tcg_gemm_ex_host(h, transa, transb, m, n, k, alpha, A, Atype, lda, B, Btype, ldb, beta, C,
+                     Ctype, ldc, compute) -> int:
+    """tcg_gemm_ex with A, B, C in host memory (CPU torch tensors or host addresses);
+    returns when C holds D."""
+    return load_library().tcg_gemm_ex_host(h, transa, transb, m, n, k, float(alpha), _ptr(A),
+                                           Atype, lda, _ptr(B), Btype, ldb, float(beta), _ptr(C),
+                                           Ctype, ldc, compute)
+
+
+def tcg_gemm_strided_batched_host(h, transa, transb, m, n, k, alpha, A, Atype, lda, strideA, B,
+                                  Btype, ldb, strideB, beta, C, Ctype, ldc, strideC,
+                                  batch_count, compute) -> int:
+    return load_library().tcg_gemm_strided_batched_host(
         h, transa, transb, m, n, k, float(alpha), _ptr(A), Atype, lda, strideA, _ptr(B), Btype,
         ldb, strideB, float(beta), _ptr(C), Ctype, ldc, strideC, batch_count, compute)
 
@@ -264,8 +285,9 @@ def check(status: int, what: str = "") -> None:
 
 
 def gemm_rowmajor(handle: Handle, A, B, C, alpha=1.0, beta=0.0, tf32=False,
-                  split3=False) -> None:
-    """Row-major D = alpha*A@B + beta*C in place in C (torch CUDA tensors).
+                  split3=False, host=False) -> None:
+    """Row-major D = alpha*A@B + beta*C in place in C (torch CUDA tensors; CPU tensors,
+    preferably pinned, with ``host=True``, through the host-buffer entry points).
 
     A: (m, k) or (batch, m, k); B: (k, n) or (batch, k, n); C: (m, n) or
     (batch, m, n), all contiguous row-major.  Issued as the column-major call
@@ -279,11 +301,13 @@ def gemm_rowmajor(handle: Handle, A, B, C, alpha=1.0, beta=0.0, tf32=False,
                                          at == TCG_R_32F) else TCG_COMPUTE_32F
     if split3:
         comp = TCG_COMPUTE_32F_3XTF32
+    one = tcg_gemm_ex_host if host else tcg_gemm_ex
+    many = tcg_gemm_strided_batched_host if host else tcg_gemm_strided_batched
     if not batched:
-        s = tcg_gemm_ex(handle.h, TCG_OP_N, TCG_OP_N, n, m, k, alpha, B, at, n, A, at, k, beta,
-                        C, ct, n, comp)
+        s = one(handle.h, TCG_OP_N, TCG_OP_N, n, m, k, alpha, B, at, n, A, at, k, beta, C, ct, n,
+                comp)
     else:
         batch = A.shape[0]
-        s = tcg_gemm_strided_batched(handle.h, TCG_OP_N, TCG_OP_N, n, m, k, alpha, B, at, n,
-                                     k * n, A, at, k, m * k, beta, C, ct, n, m * n, batch, comp)
+        s = many(handle.h, TCG_OP_N, TCG_OP_N, n, m, k, alpha, B, at, n, k * n, A, at, k, m * k,
+                 beta, C, ct, n, m * n, batch, comp)
     check(s, "gemm_rowmajor")

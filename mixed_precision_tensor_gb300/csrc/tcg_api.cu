@@ -42,6 +42,8 @@ struct MapKey {
     bool operator==(const MapKey &o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
 };
 
+constexpr int kHostChunks = 4;      // pipeline depth of the host-buffer calls
+
 struct MapEntry {
     MapKey key;
     CUtensorMap map;
@@ -66,6 +68,11 @@ struct tcgContext {
     int cta_group = 2;
     int group_m = 0;           // 0: choose per problem
     int split_k = 0;           // 0: choose per problem, 1: never split, >= 2: that many ranges
+    // Host-buffer calls: device copies of A, B, C (grown on demand) and two copy streams.
+    void *stage_buf[3] = {nullptr, nullptr, nullptr};
+    size_t stage_bytes[3] = {0, 0, 0};
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t ev_in[kHostChunks] = {}, ev_out[kHostChunks] = {};
     int max_ctas[3] = {0, 0, 0};
     bool used = false;
     EncodeTiledFn encode = nullptr;
@@ -554,6 +561,244 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
     return st;
 }
 
+
+// ---------------------------------------------------------------- host-buffer calls
+//
+// The same GEMM with A, B and C in host memory: the operands are copied to device
+// buffers the handle keeps (same leading dimensions and strides as on the host), the
+// product runs on the handle's stream, and D is copied back into C.  The work is cut into
+// up to kHostChunks chunks -- column panels of B/C, or groups of batch entries -- so that
+// the copies of one chunk overlap the product of another (copies in on one stream, copies
+// out on another).  Every chunk still fills at least one wave of the GPU, so no chunk
+// makes a K-split decision the whole problem would not make: the result is the device
+// call's, bit for bit.
+
+// Elements spanned by a column-major rows x cols matrix with leading dimension ld, and
+// by `batch` of them stride elements apart (stride 0: one shared matrix).
+int64_t span(int64_t rows, int64_t cols, int64_t ld, int64_t batch, int64_t stride)
+{
+    if (rows == 0 || cols == 0 || batch == 0)
+        return 0;
+    const int64_t one = (cols - 1) * ld + rows;
+    return stride == 0 ? one : (batch - 1) * stride + one;
+}
+
+tcgStatus_t stage_buffer(tcgContext *h, int i, size_t bytes, void **out)
+{
+    if (h->stage_bytes[i] < bytes) {
+        if (h->stage_buf[i]) {
+            cudaDeviceSynchronize();
+            cudaFree(h->stage_buf[i]);
+            h->stage_buf[i] = nullptr;
+            h->stage_bytes[i] = 0;
+        }
+        if (cudaMalloc(&h->stage_buf[i], bytes ? bytes : 16) != cudaSuccess) {
+            cudaGetLastError();
+            h->stage_buf[i] = nullptr;
+            return TCG_STATUS_ALLOC_FAILED;
+        }
+        h->stage_bytes[i] = bytes;
+    }
+    *out = h->stage_buf[i];
+    return TCG_STATUS_SUCCESS;
+}
+
+tcgStatus_t host_streams(tcgContext *h)
+{
+    if (!h->h2d && cudaStreamCreateWithFlags(&h->h2d, cudaStreamNonBlocking) != cudaSuccess)
+        return TCG_STATUS_EXECUTION_FAILED;
+    if (!h->d2h && cudaStreamCreateWithFlags(&h->d2h, cudaStreamNonBlocking) != cudaSuccess)
+        return TCG_STATUS_EXECUTION_FAILED;
+    for (int i = 0; i < kHostChunks; ++i) {
+        if (!h->ev_in[i] && cudaEventCreateWithFlags(&h->ev_in[i], cudaEventDisableTiming) != cudaSuccess)
+            return TCG_STATUS_EXECUTION_FAILED;
+        if (!h->ev_out[i] && cudaEventCreateWithFlags(&h->ev_out[i], cudaEventDisableTiming) != cudaSuccess)
+            return TCG_STATUS_EXECUTION_FAILED;
+    }
+    return TCG_STATUS_SUCCESS;
+}
+
+tcgStatus_t run_host(tcgContext *h, const Problem &hp)
+{
+    // Host memory needs no particular alignment (the device copies get cudaMalloc's): check
+    // the arguments with stand-in aligned addresses where pointers were given.
+    Problem cp = hp;
+    static const uint4 stand_in = {0, 0, 0, 0};
+    if (cp.A) cp.A = &stand_in;
+    if (cp.B) cp.B = &stand_in;
+    if (cp.C) cp.C = const_cast<uint4 *>(&stand_in);
+    tcgStatus_t st = check_args(cp);
+    if (st != TCG_STATUS_SUCCESS)
+        return st;
+    if (hp.m == 0 || hp.n == 0 || hp.batch == 0)
+        return TCG_STATUS_SUCCESS;
+    st = bind_device(h);
+    if (st != TCG_STATUS_SUCCESS)
+        return st;
+    st = host_streams(h);
+    if (st != TCG_STATUS_SUCCESS) {
+        cudaGetLastError();
+        return st;
+    }
+    h->used = true;
+    const bool product = hp.k > 0 && hp.alpha != 0.0f;
+    const bool read_c = hp.beta != 0.0f;
+    const int64_t esa = elem_size(hp.Atype), esc = elem_size(hp.Ctype);
+    const int64_t a_rows = hp.transa == TCG_OP_N ? hp.m : hp.k;
+    const int64_t a_cols = hp.transa == TCG_OP_N ? hp.k : hp.m;
+    const int64_t b_rows = hp.transb == TCG_OP_N ? hp.k : hp.n;
+    const int64_t b_cols = hp.transb == TCG_OP_N ? hp.n : hp.k;
+    const int64_t sA = hp.batched ? hp.strideA : 0, sB = hp.batched ? hp.strideB : 0;
+    const int64_t sC = hp.batched ? hp.strideC : 0;
+    const int64_t nA = product ? span(a_rows, a_cols, hp.lda, hp.batch, sA) : 0;
+    const int64_t nB = product ? span(b_rows, b_cols, hp.ldb, hp.batch, sB) : 0;
+    const int64_t nC = span(hp.m, hp.n, hp.ldc, hp.batch, sC);
+    void *dA = nullptr, *dB = nullptr, *dC = nullptr;
+    if ((st = stage_buffer(h, 0, (size_t)(nA * esa), &dA)) != TCG_STATUS_SUCCESS ||
+        (st = stage_buffer(h, 1, (size_t)(nB * esa), &dB)) != TCG_STATUS_SUCCESS ||
+        (st = stage_buffer(h, 2, (size_t)(nC * esc), &dC)) != TCG_STATUS_SUCCESS)
+        return st;
+
+    // Chunks: column panels (one matrix) or batch groups, each at least one wave of tiles.
+    if (h->max_ctas[h->cta_group] == 0)
+        h->max_ctas[h->cta_group] = gemm_max_resident_ctas(h->cta_group, h->num_sms);
+    const int64_t clusters = h->max_ctas[h->cta_group] / h->cta_group;
+    const int64_t tile_m = kBM * h->cta_group;
+    const int64_t m_tiles = (hp.m + tile_m - 1) / tile_m, n_tiles = (hp.n + kBN - 1) / kBN;
+    const int64_t units = hp.batched ? hp.batch : n_tiles;        // what chunks split
+    const int64_t per_unit = hp.batched ? m_tiles * n_tiles : m_tiles;
+    int64_t chunks = clusters > 0 ? per_unit * units / clusters : 1;
+    chunks = chunks < 1 ? 1 : (chunks > kHostChunks ? kHostChunks : chunks);
+    if (chunks > units)
+        chunks = units;
+    const int64_t per_chunk = (units + chunks - 1) / chunks;      // units per chunk
+    chunks = (units + per_chunk - 1) / per_chunk;
+    // A problem of several waves is never split along K (see split_plan); its chunks, some
+    // smaller than a wave, must not be either.  A forced split applies to every chunk alike.
+    const int saved_split = h->split_k;
+    if (chunks > 1 && saved_split == 0)
+        h->split_k = 1;
+    struct Restore {
+        tcgContext *h;
+        int v;
+        ~Restore() { h->split_k = v; }
+    } restore{h, saved_split};
+
+    auto fail = [&]() {
+        cudaGetLastError();
+        cudaStreamSynchronize(h->h2d);
+        cudaStreamSynchronize(h->d2h);
+        cudaStreamSynchronize(h->stream);
+        cudaGetLastError();
+        return TCG_STATUS_EXECUTION_FAILED;
+    };
+    auto h2d = [&](void *dst, const void *src, int64_t bytes) {
+        return bytes <= 0 ||
+               cudaMemcpyAsync(dst, src, (size_t)bytes, cudaMemcpyHostToDevice, h->h2d) == cudaSuccess;
+    };
+    const char *A = static_cast<const char *>(hp.A);
+    const char *B = static_cast<const char *>(hp.B);
+    char *C = static_cast<char *>(hp.C);
+    char *dAc = static_cast<char *>(dA), *dBc = static_cast<char *>(dB), *dCc = static_cast<char *>(dC);
+    // Work on the handle's stream issued before this call must not see the staging
+    // buffers change under it: copies start after it.
+    if (cudaEventRecord(h->ev_out[0], h->stream) != cudaSuccess ||
+        cudaStreamWaitEvent(h->h2d, h->ev_out[0], 0) != cudaSuccess)
+        return fail();
+    // A whole (or, batched, per group below when it has a stride).
+    const bool a_per_group = hp.batched && sA != 0;
+    if (product && !a_per_group && !h2d(dAc, A, nA * esa))
+        return fail();
+    for (int64_t c = 0; c < chunks; ++c) {
+        const int64_t u0 = c * per_chunk, u1 = u0 + per_chunk < units ? u0 + per_chunk : units;
+        Problem dp = hp;
+        dp.A = dA;
+        dp.B = dB;
+        dp.C = dC;
+        // element ranges of this chunk (in the host/device layouts, which are the same)
+        int64_t c_off, c_len;
+        if (hp.batched) {
+            const int64_t b0 = u0, b1 = u1;
+            dp.batch = b1 - b0;
+            if (product) {
+                if (a_per_group) {
+                    const int64_t off = b0 * sA, len = span(a_rows, a_cols, hp.lda, b1 - b0, sA);
+                    if (!h2d(dAc + off * esa, A + off * esa, len * esa))
+                        return fail();
+                    dp.A = dAc + off * esa;
+                }
+                if (sB != 0) {
+                    const int64_t off = b0 * sB, len = span(b_rows, b_cols, hp.ldb, b1 - b0, sB);
+                    if (!h2d(dBc + off * esa, B + off * esa, len * esa))
+                        return fail();
+                    dp.B = dBc + off * esa;
+                } else if (c == 0 && !h2d(dBc, B, nB * esa)) {
+                    return fail();
+                }
+            }
+            c_off = b0 * sC;
+            c_len = span(hp.m, hp.n, hp.ldc, b1 - b0, sC);
+            dp.C = dCc + c_off * esc;
+        } else {
+            const int64_t j0 = u0 * kBN, j1 = u1 * kBN < hp.n ? u1 * kBN : hp.n;
+            dp.n = j1 - j0;
+            if (product) {
+                if (hp.transb == TCG_OP_N) {           // columns j0..j1 of a k x n matrix
+                    const int64_t off = j0 * hp.ldb, len = span(hp.k, j1 - j0, hp.ldb, 1, 0);
+                    if (!h2d(dBc + off * esa, B + off * esa, len * esa))
+                        return fail();
+                    dp.B = dBc + off * esa;
+                } else {                               // rows j0..j1 of an n x k matrix
+                    if (cudaMemcpy2DAsync(dBc + j0 * esa, (size_t)(hp.ldb * esa), B + j0 * esa,
+                                          (size_t)(hp.ldb * esa), (size_t)((j1 - j0) * esa),
+                                          (size_t)hp.k, cudaMemcpyHostToDevice, h->h2d) != cudaSuccess)
+                        return fail();
+                    dp.B = dBc + j0 * esa;
+                }
+            }
+            c_off = j0 * hp.ldc;
+            c_len = span(hp.m, j1 - j0, hp.ldc, 1, 0);
+            dp.C = dCc + c_off * esc;
+        }
+        if (read_c && !h2d(dCc + c_off * esc, C + c_off * esc, c_len * esc))
+            return fail();
+        if (cudaEventRecord(h->ev_in[c], h->h2d) != cudaSuccess ||
+            cudaStreamWaitEvent(h->stream, h->ev_in[c], 0) != cudaSuccess)
+            return fail();
+        st = run(h, dp);
+        if (st != TCG_STATUS_SUCCESS) {
+            fail();
+            return st;
+        }
+        if (cudaEventRecord(h->ev_out[c], h->stream) != cudaSuccess ||
+            cudaStreamWaitEvent(h->d2h, h->ev_out[c], 0) != cudaSuccess)
+            return fail();
+        // D back into C, leaving the ldc padding and the gaps between batch entries alone.
+        cudaError_t e = cudaSuccess;
+        const int64_t cols = hp.batched ? hp.n : dp.n;
+        const int64_t nb = hp.batched ? dp.batch : 1;
+        if (hp.ldc == hp.m && (nb == 1 || sC == hp.m * hp.n)) {
+            e = cudaMemcpyAsync(C + c_off * esc, dCc + c_off * esc, (size_t)(hp.m * cols * nb * esc),
+                                cudaMemcpyDeviceToHost, h->d2h);
+        } else if (hp.ldc == hp.m) {
+            e = cudaMemcpy2DAsync(C + c_off * esc, (size_t)(sC * esc), dCc + c_off * esc,
+                                  (size_t)(sC * esc), (size_t)(hp.m * cols * esc), (size_t)nb,
+                                  cudaMemcpyDeviceToHost, h->d2h);
+        } else {
+            for (int64_t b = 0; b < nb && e == cudaSuccess; ++b)
+                e = cudaMemcpy2DAsync(C + (c_off + b * sC) * esc, (size_t)(hp.ldc * esc),
+                                      dCc + (c_off + b * sC) * esc, (size_t)(hp.ldc * esc),
+                                      (size_t)(hp.m * esc), (size_t)cols, cudaMemcpyDeviceToHost,
+                                      h->d2h);
+        }
+        if (e != cudaSuccess)
+            return fail();
+    }
+    if (cudaStreamSynchronize(h->d2h) != cudaSuccess || cudaStreamSynchronize(h->h2d) != cudaSuccess)
+        return fail();
+    return TCG_STATUS_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" {
@@ -579,6 +824,23 @@ tcgStatus_t tcg_destroy(tcgHandle_t h)
         cudaFree(h->d_err);
     if (h->ws_own)
         cudaFree(h->ws_own);
+    for (int i = 0; i < 3; ++i)
+        if (h->stage_buf[i])
+            cudaFree(h->stage_buf[i]);
+    if (h->h2d) {
+        cudaStreamSynchronize(h->h2d);
+        cudaStreamDestroy(h->h2d);
+    }
+    if (h->d2h) {
+        cudaStreamSynchronize(h->d2h);
+        cudaStreamDestroy(h->d2h);
+    }
+    for (int i = 0; i < kHostChunks; ++i) {
+        if (h->ev_in[i])
+            cudaEventDestroy(h->ev_in[i]);
+        if (h->ev_out[i])
+            cudaEventDestroy(h->ev_out[i]);
+    }
     delete h;
     return TCG_STATUS_SUCCESS;
 }
@@ -661,6 +923,34 @@ tcgStatus_t tcg_gemm_strided_batched(tcgHandle_t h, tcgOp_t transa, tcgOp_t tran
     Problem p{transa, transb, m, n, k, alpha, beta, A, Atype, lda, strideA, B, Btype, ldb,
               strideB, C, Ctype, ldc, strideC, batch_count, compute, true};
     return run(h, p);
+}
+
+tcgStatus_t tcg_gemm_ex_host(tcgHandle_t h, tcgOp_t transa, tcgOp_t transb, int64_t m, int64_t n,
+                             int64_t k, float alpha, const void *A, tcgDataType_t Atype,
+                             int64_t lda, const void *B, tcgDataType_t Btype, int64_t ldb,
+                             float beta, void *C, tcgDataType_t Ctype, int64_t ldc,
+                             tcgComputeType_t compute)
+{
+    if (!h)
+        return TCG_STATUS_INVALID_VALUE;
+    Problem p{transa, transb, m, n, k, alpha, beta, A, Atype, lda, 0, B, Btype, ldb, 0,
+              C, Ctype, ldc, 0, 1, compute, false};
+    return run_host(h, p);
+}
+
+tcgStatus_t tcg_gemm_strided_batched_host(tcgHandle_t h, tcgOp_t transa, tcgOp_t transb,
+                                          int64_t m, int64_t n, int64_t k, float alpha,
+                                          const void *A, tcgDataType_t Atype, int64_t lda,
+                                          int64_t strideA, const void *B, tcgDataType_t Btype,
+                                          int64_t ldb, int64_t strideB, float beta, void *C,
+                                          tcgDataType_t Ctype, int64_t ldc, int64_t strideC,
+                                          int64_t batch_count, tcgComputeType_t compute)
+{
+    if (!h)
+        return TCG_STATUS_INVALID_VALUE;
+    Problem p{transa, transb, m, n, k, alpha, beta, A, Atype, lda, strideA, B, Btype, ldb,
+              strideB, C, Ctype, ldc, strideC, batch_count, compute, true};
+    return run_host(h, p);
 }
 
 tcgStatus_t tcg_get_device_error(tcgHandle_t h)

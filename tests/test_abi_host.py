@@ -189,3 +189,14 @@ def test_split_k_argument_checks():
     assert tcg.tcg_set_split_k(None, 2) == INV
     assert tcg.tcg_gemm_split_k(None, 1, 1, 1, tcg.TCG_R_16F, tcg.TCG_COMPUTE_32F)[0] == INV
 
+
+
+def test_host_buffer_calls_check_arguments_without_a_gpu():
+    INV = tcg.TCG_STATUS_INVALID_VALUE
+    lib = tcg.load_library()
+    args = (N, N, 16, 16, 16, 1.0, None, tcg.TCG_R_16F, 16, None, tcg.TCG_R_16F, 16, 0.0, None,
+            tcg.TCG_R_32F, 16, tcg.TCG_COMPUTE_32F)
+    assert lib.tcg_gemm_ex_host(None, *args) == INV
+    bargs = (N, N, 16, 16, 16, 1.0, None, tcg.TCG_R_16F, 16, 256, None, tcg.TCG_R_16F, 16, 256,
+             0.0, None, tcg.TCG_R_32F, 16, 256, 2, tcg.TCG_COMPUTE_32F)
+    assert lib.tcg_gemm_strided_batched_host(None, *bargs) == INV

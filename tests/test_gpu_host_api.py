@@ -1,0 +1,139 @@
+"""The host-buffer entry points (tcg_gemm_ex_host, tcg_gemm_strided_batched_host) against
+the device entry points on the same inputs: bit-identical results, untouched ldc padding
+and batch gaps in the host C, chunked (pipelined) and single-chunk problems."""
+import numpy as np
+import pytest
+import torch
+
+import mixed_precision_tensor_gb300 as tcg
+
+pytestmark = pytest.mark.gpu
+
+N, T = tcg.TCG_OP_N, tcg.TCG_OP_T
+DT = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32,
+      "e4m3": torch.float8_e4m3fn}
+CODE = {"f16": tcg.TCG_R_16F, "bf16": tcg.TCG_R_16BF, "f32": tcg.TCG_R_32F,
+        "e4m3": tcg.TCG_R_8F_E4M3}
+
+
+def _rand(n, t, gen):
+    return (torch.rand(n, generator=gen, dtype=torch.float32) * 2 - 1).to(DT[t])
+
+
+def _bits(x):
+    """Raw bits of a tensor for bit-for-bit comparison."""
+    x = x.contiguous().cpu()
+    return x.view(torch.uint8) if x.element_size() == 1 else (
+        x.view(torch.int16) if x.element_size() == 2 else x.view(torch.int32))
+
+
+CASES = [
+    # m, n, k, transa, transb, in, out, alpha, beta, extra ld (elements)
+    (4096, 4096, 2048, N, N, "f16", "f32", 1.0, 0.0, 0),       # several chunks
+    (3000, 2600, 1000, T, T, "bf16", "bf16", 0.5, 1.0, 8),     # 2-D copies of B, ldc padding
+    (200, 300, 500, N, T, "f16", "f16", 1.0, 0.5, 8),          # one chunk
+    (2048, 4096, 1024, T, N, "f32", "f32", 1.0, -1.0, 0),      # TF32 pre-pass on the device
+    (1024, 5120, 512, N, N, "e4m3", "f32", 2.0, 0.0, 16),      # FP8
+    (256, 256, 32768, N, N, "f16", "f32", 1.0, 0.0, 0),        # split K, one chunk
+]
+
+
+@pytest.mark.timeout(600)
+@pytest.mark.parametrize("m,n,k,ta,tb,in_t,out_t,alpha,beta,xld", CASES)
+def test_host_call_matches_device_call(cuda_device, m, n, k, ta, tb, in_t, out_t, alpha, beta,
+                                       xld):
+    gen = torch.Generator().manual_seed(m + 3 * n + k)
+    al = 16 // torch.tensor([], dtype=DT[in_t]).element_size()
+    cl = 16 // torch.tensor([], dtype=DT[out_t]).element_size()
+    a_rows, a_cols = (m, k) if ta == N else (k, m)
+    b_rows, b_cols = (k, n) if tb == N else (n, k)
+    lda = -(-a_rows // al) * al + (xld if in_t != "e4m3" else 0)
+    ldb = -(-b_rows // al) * al
+    ldc = -(-m // cl) * cl + xld
+    A = _rand(lda * a_cols, in_t, gen)
+    B = _rand(ldb * b_cols, in_t, gen)
+    C0 = _rand(ldc * n, out_t, gen)
+    comp = tcg.TCG_COMPUTE_32F_FAST_TF32 if in_t == "f32" else tcg.TCG_COMPUTE_32F
+    h = tcg.Handle()
+    # device call
+    dC = C0.clone().cuda()
+    tcg.check(tcg.tcg_gemm_ex(h.h, ta, tb, m, n, k, alpha, A.cuda(), CODE[in_t], lda, B.cuda(),
+                              CODE[in_t], ldb, beta, dC, CODE[out_t], ldc, comp))
+    want = dC.cpu()
+    # host call on pinned memory
+    hA, hB, hC = A.pin_memory(), B.pin_memory(), C0.clone().pin_memory()
+    tcg.check(tcg.tcg_gemm_ex_host(h.h, ta, tb, m, n, k, alpha, hA, CODE[in_t], lda, hB,
+                                   CODE[in_t], ldb, beta, hC, CODE[out_t], ldc, comp))
+    tcg.check(tcg.tcg_get_device_error(h.h))
+    got = hC.clone()
+    g = _bits(got).view(n, ldc)
+    w = _bits(want).view(n, ldc)
+    assert torch.equal(g[:, :m], w[:, :m]), "host call differs from the device call"
+    # the ldc padding of the host C holds what it held
+    assert torch.equal(g[:, m:], _bits(C0).view(n, ldc)[:, m:])
+    # pageable host memory works too
+    pC = C0.clone()
+    tcg.check(tcg.tcg_gemm_ex_host(h.h, ta, tb, m, n, k, alpha, A, CODE[in_t], lda, B,
+                                   CODE[in_t], ldb, beta, pC, CODE[out_t], ldc, comp))
+    assert torch.equal(_bits(pC), _bits(got))
+    h.close()
+
+
+BATCHED = [
+    # m, n, k, batch, in, out, alpha, beta, gap between batch entries (elements), xld
+    (256, 256, 256, 512, "f16", "f16", 1.0, 0.5, 0, 0),          # the batched workload shape
+    (130, 200, 96, 40, "bf16", "f32", 1.0, 1.0, 64, 4),          # gaps and ldc padding
+    (256, 512, 128, 300, "f16", "f32", 1.0, 0.0, 32, 0),         # gaps, ldc == m
+]
+
+
+@pytest.mark.timeout(600)
+@pytest.mark.parametrize("m,n,k,batch,in_t,out_t,alpha,beta,gap,xld", BATCHED)
+def test_batched_host_call_matches_device_call(cuda_device, m, n, k, batch, in_t, out_t, alpha,
+                                               beta, gap, xld):
+    gen = torch.Generator().manual_seed(m + n + k + batch)
+    al = 16 // torch.tensor([], dtype=DT[in_t]).element_size()
+    cl = 16 // torch.tensor([], dtype=DT[out_t]).element_size()
+    lda, ldb = -(-m // al) * al, -(-k // al) * al
+    ldc = -(-m // cl) * cl + xld
+    sA, sB, sC = lda * k + gap, ldb * n + gap, ldc * n + gap
+    A = _rand(sA * batch, in_t, gen)
+    B = _rand(sB * batch, in_t, gen)
+    C0 = _rand(sC * batch, out_t, gen)
+    h = tcg.Handle()
+    dC = C0.clone().cuda()
+    tcg.check(tcg.tcg_gemm_strided_batched(h.h, N, N, m, n, k, alpha, A.cuda(), CODE[in_t], lda,
+                                           sA, B.cuda(), CODE[in_t], ldb, sB, beta, dC,
+                                           CODE[out_t], ldc, sC, batch, tcg.TCG_COMPUTE_32F))
+    want = dC.cpu()
+    hC = C0.clone().pin_memory()
+    tcg.check(tcg.tcg_gemm_strided_batched_host(h.h, N, N, m, n, k, alpha, A.pin_memory(),
+                                                CODE[in_t], lda, sA, B.pin_memory(),
+                                                CODE[in_t], ldb, sB, beta, hC, CODE[out_t], ldc,
+                                                sC, batch,
+                                                tcg.TCG_COMPUTE_32F))
+    tcg.check(tcg.tcg_get_device_error(h.h))
+    g, w, c0 = _bits(hC), _bits(want), _bits(C0)
+    for b in range(batch):
+        blk = slice(b * sC, b * sC + ldc * n)
+        gb, wb = g[blk].view(n, ldc), w[blk].view(n, ldc)
+        assert torch.equal(gb[:, :m], wb[:, :m]), f"batch entry {b} differs"
+        assert torch.equal(gb[:, m:], c0[blk].view(n, ldc)[:, m:])
+        if gap:
+            gap_blk = slice(b * sC + ldc * n, (b + 1) * sC)
+            assert torch.equal(g[gap_blk], c0[gap_blk])
+    h.close()
+
+
+def test_host_call_degenerate_cases(cuda_device):
+    h = tcg.Handle()
+    C = torch.randn(40, 72).pin_memory()              # column-major 70 x 40, ldc 72
+    want = (-1.5 * C[:, :70].double()).float()
+    tcg.check(tcg.tcg_gemm_ex_host(h.h, N, N, 70, 40, 0, 1.0, None, tcg.TCG_R_16F, 72, None,
+                                   tcg.TCG_R_16F, 64, -1.5, C, tcg.TCG_R_32F, 72,
+                                   tcg.TCG_COMPUTE_32F))
+    assert torch.equal(C[:, :70], want)
+    assert tcg.tcg_gemm_ex_host(h.h, N, N, 0, 40, 8, 1.0, None, tcg.TCG_R_16F, 8, None,
+                                tcg.TCG_R_16F, 8, 0.0, C, tcg.TCG_R_32F, 72,
+                                tcg.TCG_COMPUTE_32F) == 0
+    h.close()
