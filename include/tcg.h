@@ -291,9 +291,34 @@ tcgStatus_t tcg_set_split_k(tcgHandle_t h, int splits);
 tcgStatus_t tcg_split_k_plan(int64_t tiles, int num_k_blocks, int clusters, int forced,
                              int *splits, int *kb_per_split);
 
-/* The split the next call of this shape on h will use: *splits ranges of *k_per_split K
- * elements (the last one possibly shorter).  Binds h to the current device like a GEMM
- * call.  INVALID_VALUE: NULL h or outputs, negative sizes, unknown Atype. */
+/* Tail split (FP32 output, no split-K, automatic mode only): when the output tiles fill
+ * whole waves of the GPU's SM pairs plus a partial one, the tiles after
+ * (tiles / clusters - 1) full waves are cut into 2..4 K ranges whose FP32 partial sums
+ * land in tile-sized workspace slices and are added in range order by a second kernel,
+ * which then applies alpha and beta -- so the last wave takes a fraction of a tile's time.
+ * Chosen when the tensor time it saves is over twice the partial sums' round trip.
+ * tcg_tail_split_plan is the rule, pure host arithmetic: tiles, K blocks (2 x 128 bytes of
+ * K each), tile slots (clusters), one tile's time in microseconds, one tile's FP32 bytes
+ * -> the number of whole tiles, the ranges (1: no tail split) and K blocks per range.
+ * INVALID_VALUE: NULL outputs or negative counts. */
+tcgStatus_t tcg_tail_split_plan(int64_t tiles, int num_k_blocks, int clusters, double tile_us,
+                                double tile_bytes, int64_t *full_tiles, int *splits,
+                                int *kb_per_split);
+
+/* The K ranges of every output tile of the next call of this shape on h: *tile_m x *tile_n
+ * tiles (column-major D), tile (b, mt, nt) at entry (b * tiles_m + mt) * tiles_n + nt of
+ * splits[] (1: one accumulation over all of K) and k_per_split[] (K elements per range, the
+ * last range possibly shorter).  max_tiles is the arrays' length (at least batch_count x
+ * tiles_m x tiles_n).  Binds h to the current device.  INVALID_VALUE: NULL h or outputs,
+ * negative sizes, unknown types, arrays too short. */
+tcgStatus_t tcg_gemm_tile_plan(tcgHandle_t h, int64_t m, int64_t n, int64_t k,
+                               tcgDataType_t Atype, tcgComputeType_t compute, tcgDataType_t Ctype,
+                               int64_t batch_count, int64_t max_tiles, int *tile_m, int *tile_n,
+                               int *splits, int64_t *k_per_split);
+
+/* The split-K the next call of this shape on h will use (not the tail split; see
+ * tcg_gemm_tile_plan): *splits ranges of *k_per_split K elements (the last one possibly
+ * shorter).  Binds h to the current device like a GEMM call.  INVALID_VALUE: NULL h or outputs, negative sizes, unknown Atype. */
 tcgStatus_t tcg_gemm_split_k(tcgHandle_t h, int64_t m, int64_t n, int64_t k,
                              tcgDataType_t Atype, tcgComputeType_t compute, int64_t batch_count,
                              int *splits, int64_t *k_per_split);

@@ -40,7 +40,8 @@ EXPORTS = ("tcg_create", "tcg_destroy", "tcg_set_stream", "tcg_set_workspace",
            "tcg_get_device_error", "tcg_last_device_error_bits", "tcg_status_string",
            "tcg_set_debug", "tcg_launch_count", "tcg_set_kernel_options",
            "tcg_gemm_tf32_noalloc", "tcg_set_split_k", "tcg_split_k_plan",
-           "tcg_gemm_split_k", "tcg_gemm_ex_host", "tcg_gemm_strided_batched_host")
+           "tcg_gemm_split_k", "tcg_gemm_ex_host", "tcg_gemm_strided_batched_host",
+           "tcg_tail_split_plan", "tcg_gemm_tile_plan")
 
 _lock = threading.Lock()
 _lib = None
@@ -84,6 +85,13 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.tcg_gemm_strided_batched.argtypes = [vp, ci, ci, i64, i64, i64, f32, vp, ci, i64,
                                                  i64, vp, ci, i64, i64, f32, vp, ci, i64, i64,
                                                  i64, ci]
+        lib.tcg_tail_split_plan.restype = st
+        lib.tcg_tail_split_plan.argtypes = [i64, ci, ci, ctypes.c_double, ctypes.c_double,
+                                            ctypes.POINTER(i64), ctypes.POINTER(ci),
+                                            ctypes.POINTER(ci)]
+        lib.tcg_gemm_tile_plan.restype = st
+        lib.tcg_gemm_tile_plan.argtypes = [vp, i64, i64, i64, ci, ci, ci, i64, i64,
+                                           ctypes.POINTER(ci), ctypes.POINTER(ci), vp, vp]
         lib.tcg_gemm_ex_host.restype = st
         lib.tcg_gemm_ex_host.argtypes = lib.tcg_gemm_ex.argtypes
         lib.tcg_gemm_strided_batched_host.restype = st
@@ -220,6 +228,37 @@ def tcg_split_k_plan(tiles: int, num_k_blocks: int, clusters: int, forced: int =
     st = load_library().tcg_split_k_plan(tiles, num_k_blocks, clusters, forced, ctypes.byref(s),
                                          ctypes.byref(kb))
     return st, s.value, kb.value
+
+
+def tcg_tail_split_plan(tiles: int, num_k_blocks: int, clusters: int, tile_us: float,
+                        tile_bytes: float):
+    """(status, full_tiles, splits, kb_per_split) of the tail-split rule (host arithmetic)."""
+    f, s, kb = ctypes.c_int64(0), ctypes.c_int(0), ctypes.c_int(0)
+    st = load_library().tcg_tail_split_plan(tiles, num_k_blocks, clusters, tile_us, tile_bytes,
+                                            ctypes.byref(f), ctypes.byref(s), ctypes.byref(kb))
+    return st, f.value, s.value, kb.value
+
+
+def tcg_gemm_tile_plan(h: int, m: int, n: int, k: int, Atype: int, compute: int, Ctype: int,
+                       batch: int = 1):
+    """(status, tile_m, tile_n, splits, k_per_split): per-tile K ranges of the next call of
+    this shape; splits/k_per_split are numpy arrays of shape (batch, tiles_m, tiles_n)."""
+    import numpy as np
+    lib = load_library()
+    tm, tn = ctypes.c_int(0), ctypes.c_int(0)
+    # first call for the tile sizes (the arrays' length is only known after it)
+    st = lib.tcg_gemm_tile_plan(h, m, n, k, Atype, compute, Ctype, batch, 1 << 62,
+                                ctypes.byref(tm), ctypes.byref(tn), None, None)
+    if st != 0 and st != 2:
+        return st, 0, 0, None, None
+    mt = -(-m // tm.value) if tm.value else 0
+    nt = -(-n // tn.value) if tn.value else 0
+    splits = np.zeros((batch, mt, nt), dtype=np.int32)
+    kps = np.zeros((batch, mt, nt), dtype=np.int64)
+    st = lib.tcg_gemm_tile_plan(h, m, n, k, Atype, compute, Ctype, batch, splits.size,
+                                ctypes.byref(tm), ctypes.byref(tn), splits.ctypes.data,
+                                kps.ctypes.data)
+    return st, tm.value, tn.value, splits, kps
 
 
 def tcg_gemm_split_k(h: int, m: int, n: int, k: int, Atype: int, compute: int, batch: int = 1):

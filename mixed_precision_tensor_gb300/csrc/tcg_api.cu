@@ -352,6 +352,21 @@ SplitPlan plan_for(tcgContext *h, int64_t m, int64_t n, int64_t k, int64_t batch
     return split_plan(tiles, nkb, h->max_ctas[cg] / cg, h->split_k);
 }
 
+// The tail split of an unsplit problem with FP32 output (see tail_plan); none otherwise.
+// A K block (2 x 128 bytes of K for every row) keeps the tensor pipe 1024 cycles busy on
+// either kernel variant; ~1.8 GHz is taken for the tile time.
+TailPlan tail_for(tcgContext *h, int64_t m, int64_t n, int64_t k, int64_t batch, int es, int cg,
+                  bool fp32_out, const SplitPlan &split)
+{
+    const int64_t k_block = static_cast<int64_t>(kDepth) * (128 / es);
+    const int nkb = static_cast<int>((k + k_block - 1) / k_block);
+    const int64_t tiles = ((m + kBM * cg - 1) / (kBM * cg)) * ((n + kBN - 1) / kBN) * batch;
+    if (!fp32_out || split.splits > 1 || h->split_k != 0)
+        return TailPlan{tiles, 1, nkb};
+    const double tile_us = nkb * 1024.0 / 1.8e3;
+    return tail_plan(tiles, nkb, h->max_ctas[cg] / cg, tile_us, 4.0 * kBM * cg * kBN);
+}
+
 // Device workspace of at least `need` bytes: the caller's (tcg_set_workspace) or one the
 // handle grows with cudaMalloc.
 tcgStatus_t acquire_ws(tcgContext *h, size_t need, void **ws)
@@ -411,10 +426,18 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
     const bool split3 = p.compute == TCG_COMPUTE_32F_3XTF32;
     const bool tf32 = p.compute == TCG_COMPUTE_32F_FAST_TF32 || split3;
     const int cg = h->cta_group;
-    const SplitPlan plan = plan_for(h, p.m, p.n, p.k, p.batch, tf32 ? 4 : elem_size(p.Atype), cg);
+    const int es_k = tf32 ? 4 : elem_size(p.Atype);
+    const SplitPlan plan = plan_for(h, p.m, p.n, p.k, p.batch, es_k, cg);
+    const TailPlan tail = tail_for(h, p.m, p.n, p.k, p.batch, es_k, cg, p.Ctype == TCG_R_32F,
+                                   plan);
+    const int64_t n_tiles_total = ((p.m + kBM * cg - 1) / (kBM * cg)) * ((p.n + kBN - 1) / kBN) *
+                                  p.batch;
+    const int64_t tail_tiles = tail.splits > 1 ? n_tiles_total - tail.full_tiles : 0;
     const size_t tf32_bytes = tf32 ? (split3 ? 2 : 1) * tf32_ws_bytes(p.m, p.n, p.k, p.batch) : 0;
     const size_t splitk_bytes = plan.splits > 1 ? splitk_ws_bytes(p.m, p.n, p.batch, plan.splits)
-                                                : 0;
+                                                : (tail_tiles ? (size_t)(tail_tiles * tail.splits) *
+                                                                    (size_t)(kBM * cg * kBN) * 4
+                                                              : 0);
     void *ws = nullptr;
     if (tf32_bytes + splitk_bytes > 0) {
         st = acquire_ws(h, tf32_bytes + splitk_bytes, &ws);
@@ -477,6 +500,15 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
                 : output_map(h, p.C, p.Ctype, p.m, p.n, p.ldc, strideC, p.batch, &tmD);
     if (st != TCG_STATUS_SUCCESS)
         return st;
+    // Split tail tiles write their partial sums to tile-sized FP32 slices of W.
+    const int tile_m = kBM * cg;
+    CUtensorMap tmW = tmD;
+    if (tail_tiles) {
+        st = output_map(h, W, TCG_R_32F, tile_m, kBN, tile_m, (int64_t)tile_m * kBN,
+                        tail_tiles * tail.splits, &tmW);
+        if (st != TCG_STATUS_SUCCESS)
+            return st;
+    }
 
     // One launch of the GEMM kernel: D = alpha * opA * opB + beta * C.
     auto gemm_launch = [&](const void *opA, const void *opB, float beta) -> tcgStatus_t {
@@ -490,7 +522,17 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
         a.num_k_blocks = (k + kDepth * a.k_row - 1) / (kDepth * a.k_row);
         a.k_splits = plan.splits;
         a.kb_per_split = plan.kb_per_split;
-        a.total_tiles = a.num_m_tiles * a.num_n_tiles * batch * plan.splits;
+        if (tail_tiles) {
+            a.full_units = static_cast<int>(tail.full_tiles);
+            a.tail_splits = tail.splits;
+            a.tail_kb_per_split = tail.kb_per_split;
+            a.total_tiles = a.full_units + static_cast<int>(tail_tiles) * tail.splits;
+        } else {
+            a.total_tiles = a.num_m_tiles * a.num_n_tiles * batch * plan.splits;
+            a.full_units = a.total_tiles;
+            a.tail_splits = 1;
+            a.tail_kb_per_split = a.num_k_blocks;
+        }
         a.group_m = h->group_m > 0 ? h->group_m : 8;
         a.kind = tf32 ? kKindTF32 : (fp8 ? kKindF8 : kKindF16);
         // operand format codes: kind::f16 F16 = 0, BF16 = 1; kind::tf32 TF32 = 2;
@@ -533,9 +575,19 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
         a.b_bcast = bbc ? 1 : 0;
         const int64_t want = static_cast<int64_t>(a.total_tiles) * cg;
         const int grid = static_cast<int>(want < h->max_ctas[cg] ? want : h->max_ctas[cg]);
-        cudaError_t e = launch_gemm(tmA, tmB, tmD, a, splitk ? static_cast<int>(kOutF32) : ok,
-                                    cg, grid, h->stream);
+        cudaError_t e = launch_gemm(tmA, tmB, tmD, tmW, a,
+                                    splitk ? static_cast<int>(kOutF32) : ok, cg, grid, h->stream);
         h->launches += 1;
+        if (e == cudaSuccess && tail_tiles) {
+            const int64_t total = tail_tiles * tile_m * kBN;
+            int64_t blocks = (total + 255) / 256;
+            const int64_t cap = static_cast<int64_t>(h->num_sms) * 8;
+            if (blocks > cap)
+                blocks = cap;
+            e = launch_tail_reduce(W, static_cast<int>(tail_tiles), tile_m, a,
+                                   static_cast<int>(blocks), h->stream);
+            h->launches += 1;
+        }
         if (e == cudaSuccess && splitk) {
             const int64_t total = p.m * p.n * p.batch;
             int64_t blocks = (total + 255) / 256;
@@ -669,6 +721,14 @@ tcgStatus_t run_host(tcgContext *h, const Problem &hp)
     const int64_t per_unit = hp.batched ? m_tiles * n_tiles : m_tiles;
     int64_t chunks = clusters > 0 ? per_unit * units / clusters : 1;
     chunks = chunks < 1 ? 1 : (chunks > kHostChunks ? kHostChunks : chunks);
+    {   // a problem whose last tiles are K-split is run whole (chunks would tile differently)
+        const bool tf32c = hp.compute != TCG_COMPUTE_32F;
+        const int es_k = tf32c ? 4 : elem_size(hp.Atype);
+        const SplitPlan sp = plan_for(h, hp.m, hp.n, hp.k, hp.batch, es_k, h->cta_group);
+        if (tail_for(h, hp.m, hp.n, hp.k, hp.batch, es_k, h->cta_group,
+                     hp.Ctype == TCG_R_32F, sp).splits > 1)
+            chunks = 1;
+    }
     if (chunks > units)
         chunks = units;
     const int64_t per_chunk = (units + chunks - 1) / chunks;      // units per chunk
@@ -891,8 +951,14 @@ tcgStatus_t tcg_gemm_workspace_size(tcgOp_t transa, tcgOp_t transb, int64_t m, i
         const int nkb = static_cast<int>((k + k_block - 1) / k_block);
         const int64_t tiles = ((m + 2 * kBM - 1) / (2 * kBM)) * ((n + kBN - 1) / kBN) * batch_count;
         const SplitPlan pl = split_plan(tiles, nkb, sms / 2, 0);
-        if (pl.splits > 1)
+        if (pl.splits > 1) {
             *bytes += splitk_ws_bytes(m, n, batch_count, pl.splits);
+        } else {        // tail split of an FP32-output call
+            const TailPlan tp = tail_plan(tiles, nkb, sms / 2, nkb * 1024.0 / 1.8e3,
+                                          4.0 * 2 * kBM * kBN);
+            if (tp.splits > 1)
+                *bytes += (size_t)((tiles - tp.full_tiles) * tp.splits) * (size_t)(2 * kBM * kBN) * 4;
+        }
     }
     return TCG_STATUS_SUCCESS;
 }
@@ -1024,6 +1090,64 @@ tcgStatus_t tcg_split_k_plan(int64_t tiles, int num_k_blocks, int clusters, int 
     const SplitPlan pl = split_plan(tiles, num_k_blocks, clusters, forced);
     *splits = pl.splits;
     *kb_per_split = pl.kb_per_split;
+    return TCG_STATUS_SUCCESS;
+}
+
+tcgStatus_t tcg_tail_split_plan(int64_t tiles, int num_k_blocks, int clusters, double tile_us,
+                                double tile_bytes, int64_t *full_tiles, int *splits,
+                                int *kb_per_split)
+{
+    if (!full_tiles || !splits || !kb_per_split || tiles < 0 || num_k_blocks < 0 || clusters < 0)
+        return TCG_STATUS_INVALID_VALUE;
+    const TailPlan pl = tail_plan(tiles, num_k_blocks, clusters, tile_us, tile_bytes);
+    *full_tiles = pl.full_tiles;
+    *splits = pl.splits;
+    *kb_per_split = pl.kb_per_split;
+    return TCG_STATUS_SUCCESS;
+}
+
+tcgStatus_t tcg_gemm_tile_plan(tcgHandle_t h, int64_t m, int64_t n, int64_t k,
+                               tcgDataType_t Atype, tcgComputeType_t compute, tcgDataType_t Ctype,
+                               int64_t batch_count, int64_t max_tiles, int *tile_m, int *tile_n,
+                               int *splits, int64_t *k_per_split)
+{
+    if (!h || !tile_m || !tile_n || m < 0 || n < 0 || k < 0 || batch_count < 0 ||
+        !valid_type(Atype) || !valid_type(Ctype))
+        return TCG_STATUS_INVALID_VALUE;
+    tcgStatus_t st = bind_device(h);
+    if (st != TCG_STATUS_SUCCESS)
+        return st;
+    const int cg = h->cta_group;
+    *tile_m = kBM * cg;
+    *tile_n = kBN;
+    const bool tf32 = compute == TCG_COMPUTE_32F_FAST_TF32 || compute == TCG_COMPUTE_32F_3XTF32;
+    const int es = tf32 ? 4 : elem_size(Atype);
+    const int64_t k_row = 128 / es, k_block = kDepth * k_row;
+    GemmArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.num_m_tiles = static_cast<int>((m + kBM * cg - 1) / (kBM * cg));
+    a.num_n_tiles = static_cast<int>((n + kBN - 1) / kBN);
+    a.group_m = h->group_m > 0 ? h->group_m : 8;
+    const int64_t tiles = static_cast<int64_t>(a.num_m_tiles) * a.num_n_tiles * batch_count;
+    if (max_tiles < tiles || (tiles > 0 && (!splits || !k_per_split)))
+        return TCG_STATUS_INVALID_VALUE;
+    if (tiles == 0 || k == 0)
+        return TCG_STATUS_SUCCESS;
+    const SplitPlan sp = plan_for(h, m, n, k, batch_count, es, cg);
+    const TailPlan tp = tail_for(h, m, n, k, batch_count, es, cg, Ctype == TCG_R_32F, sp);
+    // tiles in raster order -> (b, mt, nt); entry b * mt_count * nt_count + mt * nt_count + nt
+    for (int64_t t = 0; t < tiles; ++t) {
+        int b, mt, nt;
+        raster(a, static_cast<int>(t), b, mt, nt);
+        const int64_t e = (static_cast<int64_t>(b) * a.num_m_tiles + mt) * a.num_n_tiles + nt;
+        if (tp.splits > 1 && t >= tp.full_tiles) {
+            splits[e] = tp.splits;
+            k_per_split[e] = static_cast<int64_t>(tp.kb_per_split) * k_block;
+        } else {
+            splits[e] = sp.splits;
+            k_per_split[e] = sp.splits > 1 ? static_cast<int64_t>(sp.kb_per_split) * k_block : k;
+        }
+    }
     return TCG_STATUS_SUCCESS;
 }
 
@@ -1194,6 +1318,9 @@ extern "C" tcgStatus_t tcg_gemm_tf32_noalloc(void *stream, tcgOp_t transa, tcgOp
     a.k_splits = 1;                              // never split: no partial-sum workspace
     a.kb_per_split = a.num_k_blocks;
     a.total_tiles = a.num_m_tiles * a.num_n_tiles;
+    a.full_units = a.total_tiles;
+    a.tail_splits = 1;
+    a.tail_kb_per_split = a.num_k_blocks;
     a.group_m = 8;
     a.kind = kKindTF32;
     a.idesc = (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(kBN >> 3) << 17) |
@@ -1222,7 +1349,7 @@ extern "C" tcgStatus_t tcg_gemm_tf32_noalloc(void *stream, tcgOp_t transa, tcgOp
         return st;
     const int64_t want = static_cast<int64_t>(a.total_tiles) * cg;
     const int grid = static_cast<int>(want < d->max_ctas ? want : d->max_ctas);
-    if (launch_gemm(tmA, tmB, tmD, a, kOutF32, cg, grid, s) != cudaSuccess) {
+    if (launch_gemm(tmA, tmB, tmD, tmD, a, kOutF32, cg, grid, s) != cudaSuccess) {
         cudaGetLastError();
         return TCG_STATUS_EXECUTION_FAILED;
     }

@@ -84,6 +84,9 @@ struct GemmArgs {
     int total_tiles;           // work units: tiles x k_splits
     int k_splits;              // K ranges per tile (1: no split)
     int kb_per_split;          // K blocks per range (the last one may be shorter)
+    int full_units;            // units [0, full_units) as above; then the split tail tiles
+    int tail_splits;           // K ranges of each tail tile (1: no tail tiles)
+    int tail_kb_per_split;     // K blocks per tail range
     int group_m;               // tile rasterisation: group of m-tiles walked together
     int a_mode, b_mode;        // OperandMode of A and B
     int a_bcast, b_bcast;      // batch stride 0: always batch coordinate 0
@@ -99,6 +102,64 @@ struct GemmArgs {
     int fault_inject;
     int c_bufs;                // 0 (beta == 0), 2 or 4: epilogue variant (see TileCfg)
 };
+
+// Tile t -> (batch b, m-tile mt, n-tile nt) with grouped rasterisation.
+__host__ __device__ inline void raster(const GemmArgs &p, int t, int &b, int &mt, int &nt)
+{
+    const int per_batch = p.num_m_tiles * p.num_n_tiles;
+    b = t / per_batch;
+    const int r = t - b * per_batch;
+    const int span = p.group_m * p.num_n_tiles;
+    const int g = r / span;
+    const int first_m = g * p.group_m;
+    const int gsize = p.num_m_tiles - first_m < p.group_m ? p.num_m_tiles - first_m : p.group_m;
+    const int in_g = r - g * span;
+    mt = first_m + in_g % gsize;
+    nt = in_g / gsize;
+}
+
+
+// Tail split (FP32 output only): when the tiles fill whole waves of the SM pairs plus a
+// partial last wave, the last tiles (all but (tiles / clusters - 1) waves of them) are cut
+// into `splits` K ranges whose partial sums go to tile-sized FP32 slices, and
+// launch_tail_reduce adds them in range order and applies alpha and beta.  Chosen when
+// the estimated time saved on the tensor cores exceeds twice the partial-sum round trip
+// (write, read: 2 x tail tiles x splits x tile bytes at ~5 TB/s) plus a launch (~5 us);
+// tile_us is the time of one whole tile.
+struct TailPlan {
+    int64_t full_tiles;        // tiles [0, full_tiles) whole
+    int splits;                // 1: no tail split
+    int kb_per_split;
+};
+inline TailPlan tail_plan(int64_t tiles, int num_k_blocks, int clusters, double tile_us,
+                          double tile_bytes)
+{
+    TailPlan pl{tiles, 1, num_k_blocks};
+    if (clusters <= 0 || tiles <= clusters || tiles % clusters == 0)
+        return pl;
+    const int64_t waves = (tiles + clusters - 1) / clusters;
+    const int64_t full = (tiles / clusters - 1) * clusters;
+    const int64_t rest = tiles - full;
+    double best = static_cast<double>(waves);
+    for (int s = 2; s <= 4; ++s) {
+        if (num_k_blocks < 2 * s)
+            break;
+        const int64_t tail_waves = (rest * s + clusters - 1) / clusters;
+        const double t = static_cast<double>(full / clusters) + static_cast<double>(tail_waves) / s;
+        const double saved_us = (static_cast<double>(waves) - t) * tile_us;
+        const double cost_us = 5.0 + 2.0 * static_cast<double>(rest * s) * tile_bytes / 5.0e6;
+        if (t < best && saved_us > 2.0 * cost_us) {
+            best = t;
+            pl.splits = s;
+        }
+    }
+    if (pl.splits > 1) {
+        pl.full_tiles = full;
+        pl.kb_per_split = (num_k_blocks + pl.splits - 1) / pl.splits;
+        pl.splits = (num_k_blocks + pl.kb_per_split - 1) / pl.kb_per_split;
+    }
+    return pl;
+}
 
 // K splitting for problems with few tiles ("split-K"): each tile's K blocks are cut into
 // k_splits ranges of kb_per_split blocks, every (tile, range) is a work unit whose FP32
@@ -140,8 +201,14 @@ inline SplitPlan split_plan(int64_t tiles, int num_k_blocks, int clusters, int f
 // Launchers (tcg_kernels.cu).  Return the launch's cudaError_t.
 // cta_group: 1 (128x256 tiles, one CTA) or 2 (256x256 tiles, CTA pairs; grid even).
 // tmD maps D (= C) as {m, n, batch} with box {128, epi_cols(out bytes), 1}, no swizzle.
+// tmW maps the tail partial sums (tile_m x 256 x slices FP32), used only when
+// a.tail_splits > 1 (any valid map otherwise).
 cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmD,
-                        const GemmArgs &a, int out_kind, int cta_group, int grid, cudaStream_t s);
+                        const CUtensorMap &tmW, const GemmArgs &a, int out_kind, int cta_group,
+                        int grid, cudaStream_t s);
+// D (FP32) of the split tail tiles from their partial sums W (see tcg_tail_reduce_kernel).
+cudaError_t launch_tail_reduce(const float *W, int tail_tiles, int tile_m, const GemmArgs &a,
+                               int grid, cudaStream_t s);
 // Largest number of CTAs of the GEMM kernel that can be resident at once.
 int gemm_max_resident_ctas(int cta_group, int num_sms);
 cudaError_t launch_scale(void *D, const void *C, int m, int n, int64_t ldc, int64_t strideC,

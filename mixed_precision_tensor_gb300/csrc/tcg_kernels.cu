@@ -90,23 +90,36 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, Smem
     }
 }
 
-// Work unit u -> (batch b, m-tile mt, n-tile nt) with grouped rasterisation, and its
-// K split s (u = tile * k_splits + s; K blocks [s, s + 1) * kb_per_split).
-__device__ __forceinline__ void tile_coords(const GemmArgs &p, int u, int &b, int &mt, int &nt,
-                                            int &s)
+
+// Work unit u -> its tile (b, mt, nt), its K blocks [kb0, kb1), and -- for a unit of a
+// split tail tile -- its partial-sum slice (-1 otherwise).  Units [0, full_units) are
+// tiles u / k_splits with K range u % k_splits (k_splits = 1: whole tiles); the units
+// after them are the tail tiles full_units, full_units + 1, ..., tail_splits units each.
+struct UnitInfo {
+    int b, mt, nt, kb0, kb1, ks, tail_slice;
+};
+__device__ __forceinline__ UnitInfo unit_info(const GemmArgs &p, int u)
 {
-    const int t = u / p.k_splits;
-    s = u - t * p.k_splits;
-    const int per_batch = p.num_m_tiles * p.num_n_tiles;
-    b = t / per_batch;
-    const int r = t - b * per_batch;
-    const int span = p.group_m * p.num_n_tiles;
-    const int g = r / span;
-    const int first_m = g * p.group_m;
-    const int gsize = min(p.num_m_tiles - first_m, p.group_m);
-    const int in_g = r - g * span;
-    mt = first_m + in_g % gsize;
-    nt = in_g / gsize;
+    UnitInfo w;
+    int t, s, kbps;
+    if (u < p.full_units) {
+        t = u / p.k_splits;
+        s = u - t * p.k_splits;
+        kbps = p.kb_per_split;
+        w.tail_slice = -1;
+    } else {
+        const int v = u - p.full_units;
+        const int r = v / p.tail_splits;
+        s = v - r * p.tail_splits;
+        t = p.full_units + r;
+        kbps = p.tail_kb_per_split;
+        w.tail_slice = v;
+    }
+    raster(p, t, w.b, w.mt, w.nt);
+    w.ks = s;
+    w.kb0 = s * kbps;
+    w.kb1 = min(w.kb0 + kbps, p.num_k_blocks);
+    return w;
 }
 
 template <int OUT>
@@ -162,7 +175,8 @@ template <int OUT, int CG, int KIND, int CBUF>
 __global__ void __launch_bounds__(kThreads, 1)
     tcg_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmD, const GemmArgs p)
+                    const __grid_constant__ CUtensorMap tmD,
+                    const __grid_constant__ CUtensorMap tmW, const GemmArgs p)
 {
     using Cfg = TileCfg<CG, CBUF>;
     constexpr bool BETA = CBUF != 0;                          // C is read
@@ -212,6 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB);
         tma_prefetch_map(&tmD);
+        if (p.tail_splits > 1)
+            tma_prefetch_map(&tmW);
     }
     __syncwarp();
     if (warp == 1) {
@@ -276,13 +292,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool skip_once = p.fault_inject != 0 && leader;
             bool ok = true;
             for (int t = cluster_id; ok && t < p.total_tiles; t += num_clusters) {
-                int b, mt, nt, ks;
-                tile_coords(p, t, b, mt, nt, ks);
-                const int kb_begin = ks * p.kb_per_split;
-                const int kb_end = min(kb_begin + p.kb_per_split, p.num_k_blocks);
-                const int m0 = mt * kTileM + static_cast<int>(rank) * kBM;
-                const int n0 = nt * kBN + static_cast<int>(rank) * kBRows;
-                const int za = p.a_bcast ? 0 : b, zb = p.b_bcast ? 0 : b;
+                const UnitInfo w = unit_info(p, t);
+                const int kb_begin = w.kb0, kb_end = w.kb1;
+                const int m0 = w.mt * kTileM + static_cast<int>(rank) * kBM;
+                const int n0 = w.nt * kBN + static_cast<int>(rank) * kBRows;
+                const int za = p.a_bcast ? 0 : w.b, zb = p.b_bcast ? 0 : w.b;
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
                     const uint32_t fb_local = smem_u32(&ctl->full[stage]);
                     const uint32_t fb = (CG == 2) ? mapa_shared(fb_local, 0) : fb_local;
@@ -342,9 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int it = 0;
             bool ok = true;
             for (int t = cluster_id; ok && t < p.total_tiles; t += num_clusters, ++it) {
-                const int ks = t % p.k_splits;
-                const int kb_begin = ks * p.kb_per_split;
-                const int kb_end = min(kb_begin + p.kb_per_split, p.num_k_blocks);
+                const UnitInfo w = unit_info(p, t);
+                const int kb_begin = w.kb0, kb_end = w.kb1;
                 const int acc = it & 1;
                 const uint32_t acc_phase = (it >> 1) & 1;
                 if (!wait_bounded<CG>(smem_u32(&ctl->acc_empty[acc]), acc_phase ^ 1u, ctl, p,
@@ -435,28 +448,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // Origin (first row, first column, slice) of chunk number gg of this half.  With
         // K splits, D is the partial-sum workspace and unit (b, s) goes to slice
-        // b * k_splits + s.
-        auto chunk_origin = [&](uint32_t gg, int &x, int &y, int &z) -> bool {
+        // b * k_splits + s.  A split tail tile's unit goes to its own tile-sized slice of
+        // tmW instead (tail = true; rows and columns relative to the tile).
+        auto chunk_origin = [&](uint32_t gg, int &x, int &y, int &z, bool &tail) -> bool {
             const int tile = cluster_id + static_cast<int>(gg / kChunks) * num_clusters;
             if (tile >= p.total_tiles)
                 return false;
             const int c = static_cast<int>(gg % kChunks);
-            int b, mt, nt, ks;
-            tile_coords(p, tile, b, mt, nt, ks);
-            x = mt * kTileM + static_cast<int>(rank) * kBM;
-            y = nt * kBN + half * (kBN / 2) + c * kCols;
-            z = b * p.k_splits + ks;
+            const UnitInfo w = unit_info(p, tile);
+            tail = w.tail_slice >= 0;
+            const int xr = static_cast<int>(rank) * kBM, yr = half * (kBN / 2) + c * kCols;
+            x = tail ? xr : w.mt * kTileM + xr;
+            y = tail ? yr : w.nt * kBN + yr;
+            z = tail ? w.tail_slice : w.b * p.k_splits + w.ks;
             return true;
         };
         // Leader: start the C load of chunk gg (if it exists) into buffer gg % kEpiBufs.
         uint32_t issued = 0;          // C loads issued: chunks [0, issued)
         auto load_c_chunk = [&](uint32_t gg) {
             int x, y, z;
-            if (!chunk_origin(gg, x, y, z))
+            bool tail;
+            if (!chunk_origin(gg, x, y, z, tail))
                 return;
             const uint32_t buf = gg % kEpiBufs;
             const uint32_t bar = smem_u32(&ctl->c_full[half][buf]);
-            if (x < p.m && y < p.n) {
+            if (!tail && x < p.m && y < p.n) {
                 mbar_arrive_expect_tx(bar, kEpiChunkBytes);
                 tma_load_3d(stage0 + buf * kEpiChunkBytes, &tmD, bar, x, y, z);
             } else {
@@ -509,18 +525,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 int cx, cy, cz;
-                chunk_origin(g, cx, cy, cz);
+                bool tail_unit = false;
+                chunk_origin(g, cx, cy, cz, tail_unit);
                 // A TMA store writes the last row run of a column in whole 16-byte units,
                 // which would touch rows >= m inside the ldc padding: a chunk that crosses
-                // row m at a non-16-byte boundary is stored by the threads instead.
-                const bool thread_store =
-                    cx + kBM > p.m && (static_cast<int64_t>(p.m) * kOutBytes) % 16 != 0;
+                // row m at a non-16-byte boundary is stored by the threads instead.  (Tail
+                // partial sums go to whole tile-sized slices and never need that.)
+                const bool thread_store = !tail_unit && cx + kBM > p.m &&
+                                          (static_cast<int64_t>(p.m) * kOutBytes) % 16 != 0;
                 float r[kCols];
+                if (OUT == kOutF32 && tail_unit) {
+                    // the raw FP32 accumulator; the tail reduction applies alpha and beta
 #pragma unroll
-                for (int j = 0; j < kCols; ++j) {
-                    r[j] = p.alpha * __uint_as_float(v[j]);
-                    if constexpr (BETA)
-                        r[j] = fmaf(p.beta, load_smem<OUT>(sbuf, j * kBM + rl), r[j]);
+                    for (int j = 0; j < kCols; ++j)
+                        r[j] = __uint_as_float(v[j]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < kCols; ++j) {
+                        r[j] = p.alpha * __uint_as_float(v[j]);
+                        if constexpr (BETA)
+                            r[j] = fmaf(p.beta, load_smem<OUT>(sbuf, j * kBM + rl), r[j]);
+                    }
                 }
                 if (!thread_store) {
 #pragma unroll
@@ -537,7 +562,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_shared();
                 named_barrier_sync(bar_id, 128);               // the block is complete
                 if (half_leader) {
-                    if (!thread_store && cx < p.m && cy < p.n)
+                    if (tail_unit)
+                        tma_store_3d(&tmW, stage0 + buf * kEpiChunkBytes, cx, cy, cz);
+                    else if (!thread_store && cx < p.m && cy < p.n)
                         tma_store_3d(&tmD, stage0 + buf * kEpiChunkBytes, cx, cy, cz);
                     bulk_commit_group();
                     // The buffer of chunk g + 1 (no C) or g + kAhead (C) was last stored
@@ -643,6 +670,41 @@ __global__ void __launch_bounds__(256) tcg_splitk_reduce_kernel(const float *__r
     }
 }
 
+// Tail reduction (FP32 output only): for each split tail tile r (tiles full_units + r),
+// D = alpha * (W[r*S] + W[r*S + 1] + ... in that order, FP32) + beta * C over the tile's
+// elements inside the matrix.  W slices are tile-sized (tile_m x 256 FP32, leading
+// dimension tile_m).  Grid-stride over tail tiles x tile elements, consecutive threads on
+// consecutive rows.
+__global__ void __launch_bounds__(256) tcg_tail_reduce_kernel(const float *__restrict__ W,
+                                                              int tail_tiles, int tile_m,
+                                                              const GemmArgs p)
+{
+    const int64_t per_tile = static_cast<int64_t>(tile_m) * kBN;
+    const int64_t total = per_tile * tail_tiles;
+    const int S = p.tail_splits;
+    for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int r = static_cast<int>(e / per_tile);
+        const int64_t w = e - r * per_tile;
+        const int jl = static_cast<int>(w / tile_m);
+        const int il = static_cast<int>(w - static_cast<int64_t>(jl) * tile_m);
+        int b, mt, nt;
+        raster(p, p.full_units + r, b, mt, nt);
+        const int i = mt * tile_m + il, j = nt * kBN + jl;
+        if (i >= p.m || j >= p.n)
+            continue;
+        const float *src = W + static_cast<int64_t>(r) * S * per_tile + w;
+        float acc = src[0];
+        for (int s = 1; s < S; ++s)
+            acc = __fadd_rn(acc, src[s * per_tile]);
+        const int64_t idx = static_cast<int64_t>(b) * p.strideC + i + static_cast<int64_t>(j) * p.ldc;
+        float v = __fmul_rn(p.alpha, acc);
+        if (p.beta != 0.0f)
+            v = __fmaf_rn(p.beta, static_cast<const float *>(p.C)[idx], v);
+        static_cast<float *>(p.D)[idx] = v;
+    }
+}
+
 // FP32 -> TF32, round to nearest, ties to even, kept in FP32 bits (low 13 bits zero).
 // Inf passes through; NaN becomes a quiet NaN of the same sign (its payload could sit
 // entirely in the 13 dropped bits).  A carry out of the mantissa moves to the next
@@ -697,7 +759,7 @@ __global__ void __launch_bounds__(256) tcg_tf32_pack_kernel(const uint32_t *__re
 }
 
 typedef void (*GemmKernelFn)(const CUtensorMap, const CUtensorMap, const CUtensorMap,
-                             const GemmArgs);
+                             const CUtensorMap, const GemmArgs);
 
 template <int CG, int CBUF>
 static GemmKernelFn gemm_fn_cg(int out_kind, int kind)
@@ -903,7 +965,8 @@ cudaError_t launch_tf32_transpose_round(const void *in, int64_t ld, int64_t stri
 }
 
 cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmD,
-                        const GemmArgs &a, int out_kind, int cta_group, int grid, cudaStream_t s)
+                        const CUtensorMap &tmW, const GemmArgs &a, int out_kind, int cta_group,
+                        int grid, cudaStream_t s)
 {
     GemmKernelFn fn = gemm_fn(out_kind, cta_group, a.kind, a.c_bufs);
     cudaError_t e = prepare(fn);
@@ -921,7 +984,7 @@ cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, fn, tmA, tmB, tmD, a);
+    e = cudaLaunchKernelEx(&cfg, fn, tmA, tmB, tmD, tmW, a);
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
@@ -956,6 +1019,13 @@ cudaError_t launch_splitk_reduce(const float *W, int64_t ldw, int splits, int m,
                                                                 beta, D, ldc, strideC);
         break;
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tail_reduce(const float *W, int tail_tiles, int tile_m, const GemmArgs &a,
+                               int grid, cudaStream_t s)
+{
+    tcg_tail_reduce_kernel<<<grid, 256, 0, s>>>(W, tail_tiles, tile_m, a);
     return cudaGetLastError();
 }
 

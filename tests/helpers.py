@@ -67,10 +67,39 @@ def oracle_rowmajor(w, A, B, C, b=0, rows=None, cols=None, nthreads=None):
     return D.T, R.T, AB.T
 
 
-def model_rowmajor(w, A, B, C, b=0, rows=None, cols=None, nthreads=None, splits=1,
-                   k_per_split=0):
+def model_block(args, rows, cols, plan=None, batch_entry=0, tf32=False, nthreads=None,
+                **params):
+    """oracle.gemm_model over the block rows x cols of a column-major call (``args`` =
+    transa, transb, m, n, k, alpha, A, atype, lda, B, btype, ldb, beta, C, ctype, ldc),
+    each output tile with the K ranges the library gave it: ``plan`` = (tile_m, tile_n,
+    splits, k_per_split) from tcg_gemm_tile_plan (None: one accumulation over all of K)."""
+    i0, i1 = rows
+    j0, j1 = cols
+    if plan is None:
+        return oracle.gemm_model(*args, tf32=tf32, rows=rows, cols=cols, nthreads=nthreads,
+                                 **params)
+    tm, tn, splits, kps = plan
+    out = None
+    for ti in range(i0 // tm, (i1 - 1) // tm + 1):
+        for tj in range(j0 // tn, (j1 - 1) // tn + 1):
+            r0, r1 = max(i0, ti * tm), min(i1, (ti + 1) * tm)
+            c0, c1 = max(j0, tj * tn), min(j1, (tj + 1) * tn)
+            s = int(splits[batch_entry, ti, tj])
+            D = oracle.gemm_model(*args, tf32=tf32, rows=(r0, r1), cols=(c0, c1),
+                                  nthreads=nthreads, splits=s,
+                                  k_per_split=int(kps[batch_entry, ti, tj]) if s > 1 else 0,
+                                  **params)
+            if out is None:
+                out = np.zeros((i1 - i0, j1 - j0), dtype=D.dtype)
+            out[r0 - i0:r1 - i0, c0 - j0:c1 - j0] = D
+    return out
+
+
+def model_rowmajor(w, A, B, C, b=0, rows=None, cols=None, nthreads=None, plan=None):
     """The block-FMA model (oracle.PAGE_MODEL parameters) for the same row-major problem
-    and block as :func:`oracle_rowmajor`.  Returns D as a row-major block."""
+    and block as :func:`oracle_rowmajor`, with the library's per-tile K ranges ``plan``
+    (tcg_gemm_tile_plan of the column-major call, or None).  Returns D as a row-major
+    block."""
     m, n, k = w.m, w.n, w.k
     i0, i1 = rows if rows else (0, m)
     j0, j1 = cols if cols else (0, n)
@@ -78,10 +107,10 @@ def model_rowmajor(w, A, B, C, b=0, rows=None, cols=None, nthreads=None, splits=
     Bb = raw(B[b]).reshape(-1)
     Cb = raw(C[b]).reshape(-1) if C is not None else None
     t = TYPE_CODE[w.in_type]
-    D = oracle.gemm_model(oracle.OP_N, oracle.OP_N, n, m, k, w.alpha, Bb, t, n, Ab, t, k,
-                          w.beta, Cb, TYPE_CODE[w.out_type], n, tf32=(w.in_type == "f32"),
-                          rows=(j0, j1), cols=(i0, i1), nthreads=nthreads, splits=splits,
-                          k_per_split=k_per_split, **oracle.PAGE_MODEL[t])
+    args = (oracle.OP_N, oracle.OP_N, n, m, k, w.alpha, Bb, t, n, Ab, t, k, w.beta, Cb,
+            TYPE_CODE[w.out_type], n)
+    D = model_block(args, (j0, j1), (i0, i1), plan=plan, batch_entry=b,
+                    tf32=(w.in_type == "f32"), nthreads=nthreads, **oracle.PAGE_MODEL[t])
     return D.T
 
 

@@ -200,3 +200,25 @@ def test_host_buffer_calls_check_arguments_without_a_gpu():
     bargs = (N, N, 16, 16, 16, 1.0, None, tcg.TCG_R_16F, 16, 256, None, tcg.TCG_R_16F, 16, 256,
              0.0, None, tcg.TCG_R_32F, 16, 256, 2, tcg.TCG_COMPUTE_32F)
     assert lib.tcg_gemm_strided_batched_host(None, *bargs) == INV
+
+
+def test_tail_split_plan_rule():
+    # 256 tiles of 146 us (the TF32 4096 x 4096 x 16384 shape) on 76 tile slots: two full
+    # waves, the last 104 tiles in two K halves (3.5 tile times instead of 4)
+    st, full, s, kb = tcg.tcg_tail_split_plan(256, 256, 76, 256 * 1024 / 1.8e3, 262144.0)
+    assert (st, full, s, kb) == (0, 152, 2, 128)
+    # 1024 tiles of 36 us (8192^3 FP16): the half tile saved does not pay for the partial sums
+    assert tcg.tcg_tail_split_plan(1024, 64, 76, 64 * 1024 / 1.8e3, 262144.0)[1:] == (1024, 1, 64)
+    # whole waves, or fewer tiles than slots: nothing to split
+    assert tcg.tcg_tail_split_plan(152, 256, 76, 145.6, 262144.0)[2] == 1
+    assert tcg.tcg_tail_split_plan(50, 256, 76, 145.6, 262144.0)[2] == 1
+    # too few K blocks to cut
+    assert tcg.tcg_tail_split_plan(100, 3, 76, 1.0e4, 262144.0)[2] == 1
+    # every range non-empty
+    for tiles in (77, 100, 153, 400):
+        for nkb in (4, 9, 64, 300):
+            st, full, s, kb = tcg.tcg_tail_split_plan(tiles, nkb, 76, 1.0e5, 262144.0)
+            assert st == 0 and 0 <= full <= tiles and full % 76 == 0
+            assert (s - 1) * kb < nkb <= s * kb
+    assert tcg.tcg_tail_split_plan(-1, 4, 76, 1.0, 1.0)[0] == tcg.TCG_STATUS_INVALID_VALUE
+

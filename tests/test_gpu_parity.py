@@ -19,8 +19,8 @@ import torch
 
 import mixed_precision_tensor_gb300 as tcg
 import oracle
-from helpers import (TYPE_CODE, check_bound, decode_out, model_rowmajor, oracle_rowmajor, raw,
-                     values_equal)
+from helpers import (TYPE_CODE, check_bound, decode_out, model_block, model_rowmajor,
+                     oracle_rowmajor, raw, values_equal)
 from mixed_precision_tensor_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -145,9 +145,11 @@ def run_colmajor(h, transa, transb, m, n, k, alpha, beta, in_t, out_t, seed, dis
     pad = body[:, : ldc * n].reshape(batch, n, ldc)[:, :, m:]
     guards_ok = guards_ok and np.array_equal(pad.view(np.uint8),
                                              np.full_like(pad, canary).view(np.uint8))
-    # the K split this call used (the model accumulates the same ranges)
-    st, splits, kps = tcg.tcg_gemm_split_k(h.h, m, n, k, CODE[in_t], comp, batch)
-    tcg.check(st, "split plan")
+    # the K ranges this call gave every tile (the model accumulates the same ranges)
+    st, tm, tn, tsplits, tkps = tcg.tcg_gemm_tile_plan(h.h, m, n, k, CODE[in_t], comp,
+                                                       CODE[out_t], batch)
+    tcg.check(st, "tile plan")
+    plan = (tm, tn, tsplits, tkps)
     results = []
     for b in range(batch):
         args = (transa, transb, m, n, k, alpha, Araw[b * sA:(b + 1) * sA], TYPE_CODE[in_t], lda,
@@ -155,9 +157,9 @@ def run_colmajor(h, transa, transb, m, n, k, alpha, beta, in_t, out_t, seed, dis
                 Cin[b * sC:(b + 1) * sC], TYPE_CODE[out_t], ldc)
         D, R, AB = oracle.gemm(*args, tf32=(in_t == "f32" and not split3))
         # the three-product FP32 emulation is three GEMMs: not one block-FMA accumulation
-        Dm = None if split3 else oracle.gemm_model(*args, tf32=(in_t == "f32"), splits=splits,
-                                                   k_per_split=kps,
-                                                   **oracle.PAGE_MODEL[TYPE_CODE[in_t]])
+        Dm = None if split3 else model_block(args, (0, m), (0, n), plan=plan, batch_entry=b,
+                                             tf32=(in_t == "f32"),
+                                             **oracle.PAGE_MODEL[TYPE_CODE[in_t]])
         got = body[b, : ldc * n].reshape(n, ldc)[:, :m].T
         cdec = _decode(Cin[b * sC:(b + 1) * sC][: ldc * n].reshape(n, ldc)[:, :m].T, out_t)
         results.append((got, D, R, AB, cdec, Dm))
@@ -407,6 +409,33 @@ def test_split_k(cuda_device, m, n, k, in_t, out_t, alpha, beta, batch, forced):
     h.close()
 
 
+# ------------------------------------------------------------ tail split
+TAIL_CASES = [
+    # row-major m x n x k, in, out, alpha, beta: 77 output tiles of the column-major call
+    # (1792 x 2816) on 76 SM pairs, long K -> the tiles are all cut in two K ranges
+    (2816, 1792, 20480, "f16", "f32", 1.0, 0.0),
+    (2816, 1792, 20480, "bf16", "f32", 0.5, 1.0),
+]
+
+
+@pytest.mark.timeout(900)
+@pytest.mark.parametrize("m,n,k,in_t,out_t,alpha,beta", TAIL_CASES)
+def test_tail_split(handle, m, n, k, in_t, out_t, alpha, beta):
+    """Tail tiles cut along K, partial sums reduced by a second kernel: within the bound of
+    the exact oracle and bit-exact against the block-FMA model with the same per-tile K
+    ranges (sampled tiles, corners included)."""
+    w = wl.custom(m, n, k, in_t, out_t, alpha, beta, 1, seed=m + k)
+    plan = _plan(handle, w)
+    assert (plan["plan"][2] > 1).any(), "expected split tail tiles"
+    A, B, C = wl.draw(w)
+    out = _run_workload(handle, w, A, B, C)
+    _check_sampled(w, A, B, C, out, exact=False, count=12, model_tiles=6, **plan)
+    wi = wl.with_dist(w, "integer")
+    A, B, C = wl.draw(wi)
+    out = _run_workload(handle, wi, A, B, C)
+    _check_sampled(wi, A, B, C, out, exact=True, count=6)
+
+
 # ------------------------------------------------------------ the five workloads
 def _device_inputs(w, A, B, C):
     dev = torch.device("cuda:0")
@@ -438,11 +467,12 @@ def _run_workload(handle, w, A, B, C):
 
 
 def _plan(handle, w):
+    """Per-tile K ranges of the column-major call the workload makes."""
     comp = tcg.TCG_COMPUTE_32F_FAST_TF32 if w.in_type == "f32" else tcg.TCG_COMPUTE_32F
-    st, splits, kps = tcg.tcg_gemm_split_k(handle.h, w.n, w.m, w.k, CODE[w.in_type], comp,
-                                           w.batch)
-    tcg.check(st, "split plan")
-    return dict(splits=splits, k_per_split=kps)
+    st, tm, tn, splits, kps = tcg.tcg_gemm_tile_plan(handle.h, w.n, w.m, w.k, CODE[w.in_type],
+                                                     comp, CODE[w.out_type], w.batch)
+    tcg.check(st, "tile plan")
+    return dict(plan=(tm, tn, splits, kps))
 
 
 def _check_full(w, A, B, C, out, exact, plan=None):
@@ -456,7 +486,7 @@ def _check_full(w, A, B, C, out, exact, plan=None):
         else:
             ok, worst, idx = check_bound(g, ref, AB, cdec, w.k, w.alpha, w.beta, w.out_type)
             assert ok, f"batch {b}: worst normalised error {worst}"
-            Dm = model_rowmajor(w, A, B, C, b=b, **(plan or {}))
+            Dm = model_rowmajor(w, A, B, C, b=b, plan=plan)
             _assert_model_equal(g, decode_out(raw(Dm), w.out_type))
 
 
@@ -481,7 +511,7 @@ def _check_sampled(w, A, B, C, out, exact, count=64, model_tiles=8, plan=None):
         # corners come first)
         for (i0, i1, j0, j1) in tiles[:model_tiles]:
             g = decode_out(raw(np.ascontiguousarray(out[0][i0:i1, j0:j1])), w.out_type)
-            Dm = model_rowmajor(w, A, B, C, rows=(i0, i1), cols=(j0, j1), **(plan or {}))
+            Dm = model_rowmajor(w, A, B, C, rows=(i0, i1), cols=(j0, j1), plan=plan)
             _assert_model_equal(g, decode_out(raw(np.ascontiguousarray(Dm)), w.out_type))
     return worst_all
 
@@ -495,7 +525,7 @@ def test_small_workload_full_random(handle, name):
     w = wl.WORKLOADS[name]
     A, B, C = wl.draw(w)
     out = _run_workload(handle, w, A, B, C)
-    _check_full(w, A, B, C, out, exact=False, plan=_plan(handle, w))
+    _check_full(w, A, B, C, out, exact=False, **_plan(handle, w))
 
 
 @pytest.mark.parametrize("name", SMALL)
@@ -512,7 +542,7 @@ def test_large_workload_sampled_random(handle, name):
     w = wl.WORKLOADS[name]
     A, B, C = wl.draw(w)
     out = _run_workload(handle, w, A, B, C)
-    worst = _check_sampled(w, A, B, C, out, exact=False, plan=_plan(handle, w))
+    worst = _check_sampled(w, A, B, C, out, exact=False, **_plan(handle, w))
     print(f"{name}: worst normalised error over 64 tiles = {worst:.3e}")
 
 
