@@ -279,7 +279,7 @@ tcgStatus_t tcg_set_kernel_options(tcgHandle_t h, int cta_group, int group_m);
  * accumulation bit for bit.
  * tcg_set_split_k: 0 (default) splits automatically -- only when the tiles (times the
  * batch) fill less than half of the GPU's SM pairs, into at most 64 ranges of at least
- * four 2x128-byte K blocks each; 1 never splits; 2..64 forces that many ranges (fewer if
+ * eight 128-byte K blocks each; 1 never splits; 2..64 forces that many ranges (fewer if
  * K is short).  INVALID_VALUE: NULL h, splits outside 0..64. */
 tcgStatus_t tcg_set_split_k(tcgHandle_t h, int splits);
 
@@ -297,8 +297,8 @@ tcgStatus_t tcg_split_k_plan(int64_t tiles, int num_k_blocks, int clusters, int 
  * land in tile-sized workspace slices and are added in range order by a second kernel,
  * which then applies alpha and beta -- so the last wave takes a fraction of a tile's time.
  * Chosen when the tensor time it saves is over twice the partial sums' round trip.
- * tcg_tail_split_plan is the rule, pure host arithmetic: tiles, K blocks (2 x 128 bytes of
- * K each), tile slots (clusters), one tile's time in microseconds, one tile's FP32 bytes
+ * tcg_tail_split_plan is the rule, pure host arithmetic: tiles, K blocks (128 bytes of K
+ * each), tile slots (clusters), one tile's time in microseconds, one tile's FP32 bytes
  * -> the number of whole tiles, the ranges (1: no tail split) and K blocks per range.
  * INVALID_VALUE: NULL outputs or negative counts. */
 tcgStatus_t tcg_tail_split_plan(int64_t tiles, int num_k_blocks, int clusters, double tile_us,

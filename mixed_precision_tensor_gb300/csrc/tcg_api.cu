@@ -226,7 +226,7 @@ CUtensorMapDataType map_type(tcgDataType_t t)
     }
 }
 
-// Tiled map of rank 3 or 5 with 128-byte swizzle and zero fill out of range, cached
+// Tiled map of rank 3 or 4 with 128-byte swizzle and zero fill out of range, cached
 // per (pointer, type, dims, strides, box).
 tcgStatus_t get_map(tcgContext *h, const void *ptr, tcgDataType_t t, int rank,
                     const uint64_t *dims, const uint64_t *strides, const uint32_t *box,
@@ -294,7 +294,20 @@ tcgStatus_t operand_map(tcgContext *h, const void *ptr, tcgDataType_t t, bool km
                                  1};
         return get_map(h, ptr, t, 3, dims, str, box, out);
     }
-    // M/N-major: one box = one 128-byte chunk of rows over a stage's kDepth K rows.
+    // M/N-major with whole chunks: the 4-D view {c, K, rows / c, batch} brings all of a
+    // tile's chunks in one box (chunk after chunk, each over the stage's K rows).
+    const int c = 128 / es;
+    if (rows % c == 0) {
+        *mode = kMN4;
+        const uint64_t dims[4] = {static_cast<uint64_t>(c), static_cast<uint64_t>(k),
+                                  static_cast<uint64_t>(rows / c), nb};
+        const uint64_t str[3] = {ldb, 128, bstride};
+        const uint32_t box[4] = {static_cast<uint32_t>(c), static_cast<uint32_t>(kDepth * k_row),
+                                 static_cast<uint32_t>(box_rows / c), 1};
+        return get_map(h, ptr, t, 4, dims, str, box, out);
+    }
+    // M/N-major, ragged rows: one 3-D box per 128-byte chunk of rows (the 4-D view would
+    // read the next column's elements into the last chunk instead of zeros).
     *mode = kMN;
     const uint64_t dims[3] = {static_cast<uint64_t>(rows), static_cast<uint64_t>(k), nb};
     const uint64_t str[2] = {ldb, bstride};
@@ -353,8 +366,8 @@ SplitPlan plan_for(tcgContext *h, int64_t m, int64_t n, int64_t k, int64_t batch
 }
 
 // The tail split of an unsplit problem with FP32 output (see tail_plan); none otherwise.
-// A K block (2 x 128 bytes of K for every row) keeps the tensor pipe 1024 cycles busy on
-// either kernel variant; ~1.8 GHz is taken for the tile time.
+// A K block (kDepth x 128 bytes of K for every row) keeps the tensor pipe 512 cycles per
+// 128-byte row busy on either kernel variant; ~1.8 GHz is taken for the tile time.
 TailPlan tail_for(tcgContext *h, int64_t m, int64_t n, int64_t k, int64_t batch, int es, int cg,
                   bool fp32_out, const SplitPlan &split)
 {
@@ -363,7 +376,7 @@ TailPlan tail_for(tcgContext *h, int64_t m, int64_t n, int64_t k, int64_t batch,
     const int64_t tiles = ((m + kBM * cg - 1) / (kBM * cg)) * ((n + kBN - 1) / kBN) * batch;
     if (!fp32_out || split.splits > 1 || h->split_k != 0)
         return TailPlan{tiles, 1, nkb};
-    const double tile_us = nkb * 1024.0 / 1.8e3;
+    const double tile_us = nkb * 512.0 * kDepth / 1.8e3;
     return tail_plan(tiles, nkb, h->max_ctas[cg] / cg, tile_us, 4.0 * kBM * cg * kBN);
 }
 

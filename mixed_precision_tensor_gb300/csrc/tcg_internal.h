@@ -14,7 +14,7 @@ namespace tcg {
 constexpr int kBM = 128;               // rows of D per CTA (MMA M per CTA, TMEM lanes)
 constexpr int kBN = 256;               // columns of D per tile (MMA N, TMEM columns)
 constexpr int kRowBytes = 128;         // one 128-byte swizzle row of K
-constexpr int kDepth = 2;              // 128-byte K rows per operand row and stage
+constexpr int kDepth = 1;              // 128-byte K rows per operand row and stage
 constexpr int kABytes = kBM * kRowBytes;           // 16 KiB: A for one K row
 constexpr int kAccBufs = 2;            // TMEM accumulator double buffer
 constexpr int kTmemCols = kAccBufs * kBN;          // 512 columns = all of TMEM
@@ -34,22 +34,24 @@ constexpr int kSmemBytes = kDataBytes + kBarrierBytes + 1024;  // + alignment sl
 // Columns of D per epilogue chunk for an output of `bytes` per element.
 __host__ __device__ constexpr int epi_cols(int out_bytes) { return kEpiChunkBytes / (kBM * out_bytes); }
 
-// One ring stage holds kDepth 128-byte rows of K for every operand row: K = 128 FP16/BF16,
-// 64 TF32 or 256 FP8 elements.  The depth is what lets an M/N-major operand arrive as one
-// TMA box of 2 x 64 K rows per 128-byte chunk of M/N: boxes that cover only 64 K rows
-// (or interleave chunks within K groups) starve the tensor core on GB300 (measured: 76%
-// of the issue rate against 90% for K-major boxes), one box per chunk over the stage's
-// whole K range does not.
+// One ring stage holds kDepth 128-byte rows of K for every operand row: K = 64 FP16/BF16,
+// 32 TF32 or 128 FP8 elements (32 KiB a stage for a CTA of a pair, six stages).  What
+// the tensor core sees depends on how many bytes are on their way when a stage is
+// freed: with S stages of b bytes, (S - 2) * b of margin cover the load latency, so six
+// stages of 32 KiB beat three of 64 KiB (measured per SM cycle, 8192^3 FP16: 96% of the
+// MMA issue rate against 91-94%).  M/N-major tiles must still arrive in 16 KiB boxes:
+// one box per 64-row chunk (8 KiB) starved the tensor core (82-90%), so whole-chunk
+// operands use a 4-D view that brings a tile's chunks in one box (OperandMode kMN4).
 template <int CG, int CBUF>
 struct TileCfg {
     static constexpr int kEpiBufs = CBUF ? CBUF : 2;
     static constexpr int kEpiBytes = 2 * kEpiBufs * kEpiChunkBytes;   // 32 or 64 KiB
     static constexpr int kRingBytes = kDataBytes - kEpiBytes;         // 192 or 160 KiB
     static constexpr int kBRows = kBN / CG;                  // B rows loaded per CTA
-    static constexpr int kAStage = kABytes * kDepth;         // 32 KiB
-    static constexpr int kBStage = kBRows * kRowBytes * kDepth;   // 32 KiB (pair), 64 KiB
-    static constexpr int kStageBytes = kAStage + kBStage;    // 64 KiB (pair), 96 KiB (1 CTA)
-    static constexpr int kStages = kRingBytes / kStageBytes; // pair: 3 (2 with CBUF 4); 1 CTA: 2
+    static constexpr int kAStage = kABytes * kDepth;         // 16 KiB
+    static constexpr int kBStage = kBRows * kRowBytes * kDepth;   // 16 KiB (pair), 32 KiB
+    static constexpr int kStageBytes = kAStage + kBStage;    // 32 KiB (pair), 48 KiB (1 CTA)
+    static constexpr int kStages = kRingBytes / kStageBytes; // pair: 6 (5 with CBUF 4); 1 CTA: 4 (3)
     static constexpr int kTileM = kBM * CG;                  // rows of D per tile
 };
 
@@ -71,11 +73,14 @@ enum MmaKind { kKindF16 = 0, kKindTF32 = 1, kKindF8 = 2 };
 //   kK:   K contiguous.  3-D map {K, rows, batch}, box {one 128-byte row of K, rows};
 //         a stage holds kDepth such boxes one after the other (rows x 128 B each);
 //         inside a box, 8-row groups are 1 KiB apart.
-//   kMN:  M/N contiguous.  3-D map {rows, K, batch}, box {c, kDepth 128-byte rows of K}
-//         with c = 128 bytes / element size (64 for 16-bit operands, 128 for FP8; TF32
-//         operands are always made K-major); a stage holds one box per c-element chunk
-//         of rows, chunk after chunk, each covering the stage's whole K range.
-enum OperandMode { kK = 0, kMN = 1 };
+//   kMN:  M/N contiguous, rows not a multiple of c = 128 bytes / element size (64 for
+//         16-bit operands, 128 for FP8; TF32 operands are always made K-major).  3-D map
+//         {rows, K, batch}, box {c, kDepth 128-byte rows of K}; a stage holds one box per
+//         c-element chunk of rows, chunk after chunk, each covering the stage's K range.
+//   kMN4: M/N contiguous, rows a multiple of c.  4-D map {c, K, rows / c, batch}, box
+//         {c, kDepth 128-byte rows of K, chunks of the tile}: the same shared-memory
+//         layout as kMN from one box.
+enum OperandMode { kK = 0, kMN = 1, kMN4 = 2 };
 
 struct GemmArgs {
     int m, n, k;
@@ -168,7 +173,7 @@ inline TailPlan tail_plan(int64_t tiles, int num_k_blocks, int clusters, double 
 // output rounding.  Split only when the tiles fill less than half of the clusters, with
 // at least kMinSplitBlocks K blocks per range and at most kMaxSplits ranges; none of the
 // ranges is empty.
-constexpr int kMinSplitBlocks = 4;
+constexpr int kMinSplitBlocks = 8;
 constexpr int kMaxSplits = 64;
 struct SplitPlan {
     int splits;

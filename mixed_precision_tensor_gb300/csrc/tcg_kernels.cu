@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kEsize = KIND == kKindTF32 ? 4u : (KIND == kKindF8 ? 1u : 2u);
     constexpr uint32_t kKmma = 32u / kEsize;                  // K per MMA instruction
     constexpr int kMmasPerRow = kRowBytes / 32;               // 4 MMAs per 128-byte K row
-    constexpr int kMmasPerStage = kMmasPerRow * kDepth;       // 8
+    constexpr int kMmasPerStage = kMmasPerRow * kDepth;       // 4
     constexpr int kKRow = kRowBytes / kEsize;                 // K elements per 128-byte row
     constexpr int kMnBox = kRowBytes / kEsize;                // M/N elements per 128-byte chunk
     // Bytes of one kMnBox-element chunk of an M/N-major operand: kDepth K rows each.
@@ -317,8 +317,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t sb = b_smem + stage * kBStage;
                         const int k0 = kb * kDepth * kKRow;
                         // One operand tile: `rows` rows starting at row0, K from k0: kDepth
-                        // boxes of rows x 128 B (K-major) or one box per c-element chunk of
-                        // rows covering all kDepth K rows (M/N-major).
+                        // boxes of rows x 128 B (K-major), one 4-D box holding every
+                        // c-element chunk of rows (M/N-major, kMN4) or one box per chunk
+                        // (M/N-major with ragged rows, kMN); chunks cover all kDepth K rows.
                         auto box = [&](uint32_t d, const CUtensorMap *map, int x, int y, int z) {
                             if constexpr (CG == 2)
                                 tma_load_3d_pair(d, map, fb, x, y, z);
@@ -332,6 +333,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                                 for (int h = 0; h < kDepth; ++h)
                                     box(dst + h * kRows * kRowBytes, map, k0 + h * kKRow, row0, z);
+                            } else if (mode == kMN4) {
+                                if constexpr (CG == 2)
+                                    tma_load_4d_pair(dst, map, fb, 0, k0, row0 / kMnBox, z);
+                                else
+                                    tma_load_4d(dst, map, fb, 0, k0, row0 / kMnBox, z);
                             } else {
 #pragma unroll
                                 for (int h = 0; h < kRows / kMnBox; ++h)

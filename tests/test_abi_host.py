@@ -161,14 +161,15 @@ def test_product_path_has_no_oracle_dependency():
 
 
 def test_split_k_plan_rule():
-    # Split only when the tiles fill less than half of the clusters; at least 4 K blocks
+    # Split only when the tiles fill less than half of the clusters; at least 8 K blocks
     # per range; at most 64 ranges; no empty range.
     plan = lambda *a: tcg.tcg_split_k_plan(*a)
     assert plan(1, 512, 76) == (0, 64, 8)
     assert plan(40, 512, 76)[1:] == (1, 512)            # 80 > 76: the GPU is busy enough
     assert plan(10, 512, 76)[1] == 7                     # 76 // 10
-    assert plan(10, 12, 76)[1] == 3                      # at most 12 // 4 ranges
-    assert plan(1, 7, 76)[1:] == (1, 7)                  # too short to split
+    assert plan(10, 24, 76)[1] == 3                      # at most 24 // 8 ranges
+    assert plan(10, 12, 76)[1:] == (1, 12)               # 12 // 8: one range, no split
+    assert plan(1, 15, 76)[1:] == (1, 15)                # too short to split
     assert plan(500, 64, 76, 3)[1:] == (3, 22)           # forced
     assert plan(1, 2, 76, 8)[1:] == (2, 1)               # forced, capped by the K blocks
     for tiles in (1, 2, 5, 19, 37):
