@@ -452,30 +452,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t *stage0_ptr = epi_ptr + half * kEpiBufs * kEpiChunkBytes;
         const int rl = q * 32 + lane;                           // row within the CTA's 128
 
-        // Origin (first row, first column, slice) of chunk number gg of this half.  With
-        // K splits, D is the partial-sum workspace and unit (b, s) goes to slice
+        // Origin (first row, first column, slice) of chunk c of this half in work unit w.
+        // With K splits, D is the partial-sum workspace and unit (b, s) goes to slice
         // b * k_splits + s.  A split tail tile's unit goes to its own tile-sized slice of
-        // tmW instead (tail = true; rows and columns relative to the tile).
-        auto chunk_origin = [&](uint32_t gg, int &x, int &y, int &z, bool &tail) -> bool {
-            const int tile = cluster_id + static_cast<int>(gg / kChunks) * num_clusters;
-            if (tile >= p.total_tiles)
-                return false;
-            const int c = static_cast<int>(gg % kChunks);
-            const UnitInfo w = unit_info(p, tile);
+        // tmW instead (tail = true; rows and columns relative to the tile).  unit_info's
+        // divisions cost hundreds of cycles, so callers evaluate it once per unit.
+        auto chunk_origin = [&](const UnitInfo &w, int c, int &x, int &y, int &z, bool &tail) {
             tail = w.tail_slice >= 0;
             const int xr = static_cast<int>(rank) * kBM, yr = half * (kBN / 2) + c * kCols;
             x = tail ? xr : w.mt * kTileM + xr;
             y = tail ? yr : w.nt * kBN + yr;
             z = tail ? w.tail_slice : w.b * p.k_splits + w.ks;
-            return true;
         };
         // Leader: start the C load of chunk gg (if it exists) into buffer gg % kEpiBufs.
+        // The loads run ahead of the chunks being combined, into the next unit; that
+        // unit's description is kept between calls.
         uint32_t issued = 0;          // C loads issued: chunks [0, issued)
+        int ld_tile = -1;
+        UnitInfo ld_w{};
         auto load_c_chunk = [&](uint32_t gg) {
+            const int tile = cluster_id + static_cast<int>(gg / kChunks) * num_clusters;
+            if (tile >= p.total_tiles)
+                return;
+            if (tile != ld_tile) {
+                ld_w = unit_info(p, tile);
+                ld_tile = tile;
+            }
             int x, y, z;
             bool tail;
-            if (!chunk_origin(gg, x, y, z, tail))
-                return;
+            chunk_origin(ld_w, static_cast<int>(gg % kChunks), x, y, z, tail);
             const uint32_t buf = gg % kEpiBufs;
             const uint32_t bar = smem_u32(&ctl->c_full[half][buf]);
             if (!tail && x < p.m && y < p.n) {
@@ -499,6 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (named_barrier_or(bar_id, 128, !ok || ctl->abort_flag))
                 break;
             tc_fence_after();
+            const UnitInfo wt = unit_info(p, t);
             bool aborted = false;
 #pragma unroll 1
             for (int c = 0; c < kChunks; ++c, ++g) {
@@ -531,8 +537,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 int cx, cy, cz;
-                bool tail_unit = false;
-                chunk_origin(g, cx, cy, cz, tail_unit);
+                bool tail_unit;
+                chunk_origin(wt, c, cx, cy, cz, tail_unit);
                 // A TMA store writes the last row run of a column in whole 16-byte units,
                 // which would touch rows >= m inside the ldc padding: a chunk that crosses
                 // row m at a non-16-byte boundary is stored by the threads instead.  (Tail

