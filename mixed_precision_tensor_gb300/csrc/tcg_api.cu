@@ -592,8 +592,7 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
                                     splitk ? static_cast<int>(kOutF32) : ok, cg, grid, h->stream);
         h->launches += 1;
         if (e == cudaSuccess && tail_tiles) {
-            const int64_t total = tail_tiles * tile_m * kBN;
-            int64_t blocks = (total + 255) / 256;
+            int64_t blocks = tail_tiles * kBN;         // one column of a tail tile per block
             const int64_t cap = static_cast<int64_t>(h->num_sms) * 8;
             if (blocks > cap)
                 blocks = cap;
@@ -602,8 +601,7 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
             h->launches += 1;
         }
         if (e == cudaSuccess && splitk) {
-            const int64_t total = p.m * p.n * p.batch;
-            int64_t blocks = (total + 255) / 256;
+            int64_t blocks = p.n * p.batch;             // one column of D per block
             const int64_t cap = static_cast<int64_t>(h->num_sms) * 8;
             if (blocks > cap)
                 blocks = cap;

@@ -652,8 +652,9 @@ __global__ void tcg_scale_kernel(void *D, const void *C, int m, int n, int64_t l
 // Split-K reduction: D = alpha * sum_s W_s + beta * C, the partial sums W_s (FP32, one
 // slice per K range of every batch entry) added in range order in FP32, then the same
 // epilogue arithmetic as the GEMM kernel (alpha * acc, fma with beta * C, one rounding to
-// the output type).  Grid-stride over the m x n x batch elements, consecutive threads on
-// consecutive rows (coalesced in every slice and in C/D).
+// the output type).  A block takes one column of one batch entry at a time (grid-stride
+// over the batch x n columns), its threads the rows: every slice and C/D are read and
+// written along contiguous rows, and the index arithmetic is done once per column.
 template <int OUT>
 __global__ void __launch_bounds__(256) tcg_splitk_reduce_kernel(const float *__restrict__ W,
                                                                 int64_t ldw, int splits, int m,
@@ -661,59 +662,58 @@ __global__ void __launch_bounds__(256) tcg_splitk_reduce_kernel(const float *__r
                                                                 float beta, void *D, int64_t ldc,
                                                                 int64_t strideC)
 {
-    const int64_t per = static_cast<int64_t>(m) * n;
-    const int64_t total = per * batch;
     const int64_t slice = ldw * n;
-    for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
-         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t b = e / per;
-        const int64_t r = e - b * per;
-        const int64_t j = r / m;
-        const int64_t i = r - j * m;
-        const float *w = W + b * splits * slice + i + j * ldw;
-        float acc = w[0];
-        for (int s = 1; s < splits; ++s)
-            acc = __fadd_rn(acc, w[s * slice]);
-        const int64_t idx = b * strideC + i + j * ldc;
-        float v = __fmul_rn(alpha, acc);
-        if (beta != 0.0f)
-            v = __fmaf_rn(beta, load_c<OUT>(D, idx), v);
-        store_out<OUT>(D, idx, v);
+    const int64_t cols = static_cast<int64_t>(batch) * n;
+    for (int64_t bj = blockIdx.x; bj < cols; bj += gridDim.x) {
+        const int64_t b = bj / n;
+        const int64_t j = bj - b * n;
+        const float *wcol = W + b * splits * slice + j * ldw;
+        const int64_t dcol = b * strideC + j * ldc;
+        for (int i = threadIdx.x; i < m; i += blockDim.x) {
+            float acc = wcol[i];
+            for (int s = 1; s < splits; ++s)
+                acc = __fadd_rn(acc, wcol[s * slice + i]);
+            float v = __fmul_rn(alpha, acc);
+            if (beta != 0.0f)
+                v = __fmaf_rn(beta, load_c<OUT>(D, dcol + i), v);
+            store_out<OUT>(D, dcol + i, v);
+        }
     }
 }
 
 // Tail reduction (FP32 output only): for each split tail tile r (tiles full_units + r),
 // D = alpha * (W[r*S] + W[r*S + 1] + ... in that order, FP32) + beta * C over the tile's
 // elements inside the matrix.  W slices are tile-sized (tile_m x 256 FP32, leading
-// dimension tile_m).  Grid-stride over tail tiles x tile elements, consecutive threads on
-// consecutive rows.
+// dimension tile_m).  A block takes one column of one tail tile at a time (grid-stride over
+// tail tiles x 256 columns; the tile's position is worked out once per column), its
+// threads the rows.
 __global__ void __launch_bounds__(256) tcg_tail_reduce_kernel(const float *__restrict__ W,
                                                               int tail_tiles, int tile_m,
                                                               const GemmArgs p)
 {
     const int64_t per_tile = static_cast<int64_t>(tile_m) * kBN;
-    const int64_t total = per_tile * tail_tiles;
     const int S = p.tail_splits;
-    for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
-         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int r = static_cast<int>(e / per_tile);
-        const int64_t w = e - r * per_tile;
-        const int jl = static_cast<int>(w / tile_m);
-        const int il = static_cast<int>(w - static_cast<int64_t>(jl) * tile_m);
+    const int cols = tail_tiles * kBN;
+    for (int rc = blockIdx.x; rc < cols; rc += gridDim.x) {
+        const int r = rc / kBN;
+        const int jl = rc - r * kBN;
         int b, mt, nt;
         raster(p, p.full_units + r, b, mt, nt);
-        const int i = mt * tile_m + il, j = nt * kBN + jl;
-        if (i >= p.m || j >= p.n)
+        const int j = nt * kBN + jl;
+        if (j >= p.n)
             continue;
-        const float *src = W + static_cast<int64_t>(r) * S * per_tile + w;
-        float acc = src[0];
-        for (int s = 1; s < S; ++s)
-            acc = __fadd_rn(acc, src[s * per_tile]);
-        const int64_t idx = static_cast<int64_t>(b) * p.strideC + i + static_cast<int64_t>(j) * p.ldc;
-        float v = __fmul_rn(p.alpha, acc);
-        if (p.beta != 0.0f)
-            v = __fmaf_rn(p.beta, static_cast<const float *>(p.C)[idx], v);
-        static_cast<float *>(p.D)[idx] = v;
+        const float *wcol = W + static_cast<int64_t>(r) * S * per_tile + static_cast<int64_t>(jl) * tile_m;
+        const int64_t dcol = static_cast<int64_t>(b) * p.strideC + static_cast<int64_t>(j) * p.ldc;
+        const int i0 = mt * tile_m;
+        for (int il = threadIdx.x; il < tile_m && i0 + il < p.m; il += blockDim.x) {
+            float acc = wcol[il];
+            for (int s = 1; s < S; ++s)
+                acc = __fadd_rn(acc, wcol[s * per_tile + il]);
+            float v = __fmul_rn(p.alpha, acc);
+            if (p.beta != 0.0f)
+                v = __fmaf_rn(p.beta, static_cast<const float *>(p.C)[dcol + i0 + il], v);
+            static_cast<float *>(p.D)[dcol + i0 + il] = v;
+        }
     }
 }
 
