@@ -182,8 +182,10 @@ tcgStatus_t tcg_gemm_strided_batched(tcgHandle_t h, tcgOp_t transa, tcgOp_t tran
  * it keeps (grown with cudaMalloc on demand, freed by tcg_destroy; not capture-safe), runs
  * the GEMM on its stream, copies D back into C and returns when C holds D.  The copies in
  * and out are pipelined against the product: column panels of B/C (tcg_gemm_ex_host) or
- * groups of batch entries (batched), up to four, each at least one wave of output tiles,
- * copies in on one internal stream, copies out on another.  Arguments, layout rules
+ * groups of batch entries (batched), up to four, each at least one wave of output tiles;
+ * a single product of at least 8 waves goes as a grid of up to 4 x 4 blocks of D, each
+ * block row of op(A) and block column of op(B) copied in once, in the order of first use.
+ * Copies in run on one internal stream, copies out on another.  Arguments, layout rules
  * (leading dimensions and strides; no alignment needed for the host pointers), accuracy
  * and status codes as tcg_gemm_ex / tcg_gemm_strided_batched -- the result is theirs bit
  * for bit -- plus ALLOC_FAILED when the device buffers cannot be had.  Rows >= m inside

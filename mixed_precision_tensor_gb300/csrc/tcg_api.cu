@@ -42,7 +42,8 @@ struct MapKey {
     bool operator==(const MapKey &o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
 };
 
-constexpr int kHostChunks = 4;      // pipeline depth of the host-buffer calls
+constexpr int kHostChunks = 16;     // chunks of a host-buffer call (events per handle)
+constexpr int kHostPanels = 4;      // chunks of the panel / batch-group split
 
 struct MapEntry {
     MapKey key;
@@ -630,11 +631,11 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
 // The same GEMM with A, B and C in host memory: the operands are copied to device
 // buffers the handle keeps (same leading dimensions and strides as on the host), the
 // product runs on the handle's stream, and D is copied back into C.  The work is cut into
-// up to kHostChunks chunks -- column panels of B/C, or groups of batch entries -- so that
-// the copies of one chunk overlap the product of another (copies in on one stream, copies
-// out on another).  Every chunk still fills at least one wave of the GPU, so no chunk
-// makes a K-split decision the whole problem would not make: the result is the device
-// call's, bit for bit.
+// chunks -- up to kHostPanels column panels of B/C or groups of batch entries, or, for a
+// single product of at least 8 waves, a grid of up to 4 x 4 blocks of D -- so that the
+// copies of one chunk overlap the product of another (copies in on one stream, copies out
+// on another).  Chunk edges fall on tile edges and no chunk splits K (a problem that
+// would split its last tiles is run whole): the result is the device call's, bit for bit.
 
 // Elements spanned by a column-major rows x cols matrix with leading dimension ld, and
 // by `batch` of them stride elements apart (stride 0: one shared matrix).
@@ -731,7 +732,7 @@ tcgStatus_t run_host(tcgContext *h, const Problem &hp)
     const int64_t units = hp.batched ? hp.batch : n_tiles;        // what chunks split
     const int64_t per_unit = hp.batched ? m_tiles * n_tiles : m_tiles;
     int64_t chunks = clusters > 0 ? per_unit * units / clusters : 1;
-    chunks = chunks < 1 ? 1 : (chunks > kHostChunks ? kHostChunks : chunks);
+    chunks = chunks < 1 ? 1 : (chunks > kHostPanels ? kHostPanels : chunks);
     {   // a problem whose last tiles are K-split is run whole (chunks would tile differently)
         const bool tf32c = hp.compute != TCG_COMPUTE_32F;
         const int es_k = tf32c ? 4 : elem_size(hp.Atype);
@@ -776,6 +777,87 @@ tcgStatus_t run_host(tcgContext *h, const Problem &hp)
     if (cudaEventRecord(h->ev_out[0], h->stream) != cudaSuccess ||
         cudaStreamWaitEvent(h->h2d, h->ev_out[0], 0) != cudaSuccess)
         return fail();
+    // A large single product (at least 8 waves of tiles) goes as a grid of up to 4 x 4
+    // blocks of D.  Block (i, j) needs block row i of op(A) and block column j of op(B);
+    // each goes in once, in the order of first use, so that D's blocks start going out
+    // after the first row block of A and column block of B have arrived instead of after
+    // all of A, and the two directions of the host link stay busy together.  Block edges
+    // fall on tile edges, so every tile is accumulated exactly as in the whole call.
+    if (!hp.batched && product && chunks > 1 && m_tiles * n_tiles >= 8 * clusters) {
+        const int64_t mt_per = (m_tiles + 3) / 4, nt_per = (n_tiles + 3) / 4;
+        const int64_t mc = (m_tiles + mt_per - 1) / mt_per, nc = (n_tiles + nt_per - 1) / nt_per;
+        auto copy_a = [&](int64_t i0, int64_t i1) {
+            if (hp.transa == TCG_OP_N)                 // rows i0..i1 of an m x k matrix
+                return cudaMemcpy2DAsync(dAc + i0 * esa, (size_t)(hp.lda * esa), A + i0 * esa,
+                                         (size_t)(hp.lda * esa), (size_t)((i1 - i0) * esa),
+                                         (size_t)hp.k, cudaMemcpyHostToDevice, h->h2d) == cudaSuccess;
+            const int64_t off = i0 * hp.lda;           // columns i0..i1 of a k x m matrix
+            return h2d(dAc + off * esa, A + off * esa, span(hp.k, i1 - i0, hp.lda, 1, 0) * esa);
+        };
+        auto copy_b = [&](int64_t j0, int64_t j1) {
+            if (hp.transb == TCG_OP_N) {               // columns j0..j1 of a k x n matrix
+                const int64_t off = j0 * hp.ldb;
+                return h2d(dBc + off * esa, B + off * esa, span(hp.k, j1 - j0, hp.ldb, 1, 0) * esa);
+            }                                          // rows j0..j1 of an n x k matrix
+            return cudaMemcpy2DAsync(dBc + j0 * esa, (size_t)(hp.ldb * esa), B + j0 * esa,
+                                     (size_t)(hp.ldb * esa), (size_t)((j1 - j0) * esa),
+                                     (size_t)hp.k, cudaMemcpyHostToDevice, h->h2d) == cudaSuccess;
+        };
+        // rows i0..i1 of columns j0..j1 of C / D, in either direction
+        auto copy_block = [&](char *dst, const char *src, int64_t i0, int64_t i1, int64_t j0,
+                              int64_t j1, cudaMemcpyKind kind, cudaStream_t s) {
+            const int64_t off = (i0 + j0 * hp.ldc) * esc;
+            return cudaMemcpy2DAsync(dst + off, (size_t)(hp.ldc * esc), src + off,
+                                     (size_t)(hp.ldc * esc), (size_t)((i1 - i0) * esc),
+                                     (size_t)(j1 - j0), kind, s) == cudaSuccess;
+        };
+        // Blocks in growing squares (square q: the blocks with max(i, j) = q, first (q, 0..q-1)
+        // then (0..q, q)), so that each new block row of A and column of B is followed by
+        // the blocks it completes and the copies out keep pace with the copies in.
+        int64_t order_i[kHostChunks], order_j[kHostChunks], nblocks = 0;
+        for (int64_t q = 0; q < (mc > nc ? mc : nc); ++q)
+            for (int64_t r = 0; r < 2 * q + 1; ++r) {
+                const int64_t i = r < q ? q : r - q, j = r < q ? r : q;
+                if (i < mc && j < nc) {
+                    order_i[nblocks] = i;
+                    order_j[nblocks] = j;
+                    ++nblocks;
+                }
+            }
+        bool a_in[4] = {false, false, false, false}, b_in[4] = {false, false, false, false};
+        for (int64_t c = 0; c < nblocks; ++c) {
+            const int64_t i = order_i[c], j = order_j[c];
+            const int64_t i0 = i * mt_per * tile_m;
+            const int64_t i1 = (i + 1) * mt_per * tile_m < hp.m ? (i + 1) * mt_per * tile_m : hp.m;
+            const int64_t j0 = j * nt_per * kBN;
+            const int64_t j1 = (j + 1) * nt_per * kBN < hp.n ? (j + 1) * nt_per * kBN : hp.n;
+            if ((!a_in[i] && !copy_a(i0, i1)) || (!b_in[j] && !copy_b(j0, j1)) ||
+                (read_c && !copy_block(dCc, C, i0, i1, j0, j1, cudaMemcpyHostToDevice, h->h2d)))
+                return fail();
+            a_in[i] = b_in[j] = true;
+            if (cudaEventRecord(h->ev_in[c], h->h2d) != cudaSuccess ||
+                cudaStreamWaitEvent(h->stream, h->ev_in[c], 0) != cudaSuccess)
+                return fail();
+            Problem dp = hp;
+            dp.m = i1 - i0;
+            dp.n = j1 - j0;
+            dp.A = hp.transa == TCG_OP_N ? dAc + i0 * esa : dAc + i0 * hp.lda * esa;
+            dp.B = hp.transb == TCG_OP_N ? dBc + j0 * hp.ldb * esa : dBc + j0 * esa;
+            dp.C = dCc + (i0 + j0 * hp.ldc) * esc;
+            st = run(h, dp);
+            if (st != TCG_STATUS_SUCCESS) {
+                fail();
+                return st;
+            }
+            if (cudaEventRecord(h->ev_out[c], h->stream) != cudaSuccess ||
+                cudaStreamWaitEvent(h->d2h, h->ev_out[c], 0) != cudaSuccess ||
+                !copy_block(C, dCc, i0, i1, j0, j1, cudaMemcpyDeviceToHost, h->d2h))
+                return fail();
+        }
+        if (cudaStreamSynchronize(h->d2h) != cudaSuccess || cudaStreamSynchronize(h->h2d) != cudaSuccess)
+            return fail();
+        return TCG_STATUS_SUCCESS;
+    }
     // A whole (or, batched, per group below when it has a stride).
     const bool a_per_group = hp.batched && sA != 0;
     if (product && !a_per_group && !h2d(dAc, A, nA * esa))

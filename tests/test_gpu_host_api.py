@@ -35,6 +35,11 @@ CASES = [
     (2048, 4096, 1024, T, N, "f32", "f32", 1.0, -1.0, 0),      # TF32 pre-pass on the device
     (1024, 5120, 512, N, N, "e4m3", "f32", 2.0, 0.0, 16),      # FP8
     (256, 256, 32768, N, N, "f16", "f32", 1.0, 0.0, 0),        # split K, one chunk
+    # at least 8 waves of tiles: a grid of D blocks (ragged edges, all op combinations)
+    (8192, 5120, 512, N, N, "f16", "f32", 1.0, 0.0, 0),
+    (6400, 8192, 256, T, T, "bf16", "bf16", 0.5, 1.0, 8),
+    (8192, 6000, 384, N, T, "f16", "f16", 1.0, 0.5, 8),
+    (7936, 8192, 256, T, N, "e4m3", "f32", 2.0, 0.0, 16),
 ]
 
 
