@@ -48,7 +48,10 @@
  * B.  The first GEMM call on a handle binds it to the current device and
  * allocates a 4-byte device error word; make that call before any stream
  * capture.  The TF32 path and split-K calls need a workspace (see
- * tcg_set_workspace).
+ * tcg_set_workspace).  Once bound, and with its workspace large enough, a
+ * handle's device-buffer calls can be captured in a CUDA graph: they then make
+ * no allocation and no synchronisation, and replays give the eager results bit
+ * for bit.
  *
  * Pointers are device pointers (or memory the device can access, e.g. managed
  * memory) unless stated otherwise.
