@@ -417,7 +417,12 @@ def run_ours(args, w):
         "tensor_peak_at_clock": at_clock,
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{peak_src} ({'bf16_tflops' if bound == 'tensor' else 'hbm_gbs'})"},
+                     "peak_source": f"{peak_src} ({'bf16_tflops' if bound == 'tensor' else 'hbm_gbs'})",
+                     # context: the same ratio against cuBLAS's sustained (power-capped) rate,
+                     # the regime a long run of back-to-back calls ends in
+                     "frac_of_sustained": (achieved / (peak * float(
+                         peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+                         / float(peaks["bf16_tflops"])) if bound == "tensor" else None)},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
