@@ -593,7 +593,7 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
                                     splitk ? static_cast<int>(kOutF32) : ok, cg, grid, h->stream);
         h->launches += 1;
         if (e == cudaSuccess && tail_tiles) {
-            int64_t blocks = tail_tiles * kBN;         // one column of a tail tile per block
+            int64_t blocks = tail_tiles * (kBN / 16);  // 16 columns of a tail tile per block
             const int64_t cap = static_cast<int64_t>(h->num_sms) * 8;
             if (blocks > cap)
                 blocks = cap;

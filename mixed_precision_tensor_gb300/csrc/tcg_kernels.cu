@@ -684,35 +684,47 @@ __global__ void __launch_bounds__(256) tcg_splitk_reduce_kernel(const float *__r
 // Tail reduction (FP32 output only): for each split tail tile r (tiles full_units + r),
 // D = alpha * (W[r*S] + W[r*S + 1] + ... in that order, FP32) + beta * C over the tile's
 // elements inside the matrix.  W slices are tile-sized (tile_m x 256 FP32, leading
-// dimension tile_m).  A block takes one column of one tail tile at a time (grid-stride over
-// tail tiles x 256 columns; the tile's position is worked out once per column), its
-// threads the rows.
+// dimension tile_m).  A block takes 16 columns of one tail tile at a time (grid-stride
+// over tail tiles x 16 column groups; the tile's position is worked out once per group),
+// its threads the rows; every thread keeps 16 x S loads in flight.
+constexpr int kTailCols = 16;
 __global__ void __launch_bounds__(256) tcg_tail_reduce_kernel(const float *__restrict__ W,
                                                               int tail_tiles, int tile_m,
                                                               const GemmArgs p)
 {
+    constexpr int kGroups = kBN / kTailCols;
     const int64_t per_tile = static_cast<int64_t>(tile_m) * kBN;
     const int S = p.tail_splits;
-    const int cols = tail_tiles * kBN;
-    for (int rc = blockIdx.x; rc < cols; rc += gridDim.x) {
-        const int r = rc / kBN;
-        const int jl = rc - r * kBN;
+    const int groups = tail_tiles * kGroups;
+    for (int rg = blockIdx.x; rg < groups; rg += gridDim.x) {
+        const int r = rg / kGroups;
+        const int j0l = (rg - r * kGroups) * kTailCols;
         int b, mt, nt;
         raster(p, p.full_units + r, b, mt, nt);
-        const int j = nt * kBN + jl;
-        if (j >= p.n)
-            continue;
-        const float *wcol = W + static_cast<int64_t>(r) * S * per_tile + static_cast<int64_t>(jl) * tile_m;
-        const int64_t dcol = static_cast<int64_t>(b) * p.strideC + static_cast<int64_t>(j) * p.ldc;
-        const int i0 = mt * tile_m;
+        const int i0 = mt * tile_m, jb = nt * kBN + j0l;
+        const float *wt = W + static_cast<int64_t>(r) * S * per_tile + static_cast<int64_t>(j0l) * tile_m;
         for (int il = threadIdx.x; il < tile_m && i0 + il < p.m; il += blockDim.x) {
-            float acc = wcol[il];
-            for (int s = 1; s < S; ++s)
-                acc = __fadd_rn(acc, wcol[s * per_tile + il]);
-            float v = __fmul_rn(p.alpha, acc);
-            if (p.beta != 0.0f)
-                v = __fmaf_rn(p.beta, static_cast<const float *>(p.C)[dcol + i0 + il], v);
-            static_cast<float *>(p.D)[dcol + i0 + il] = v;
+            float acc[kTailCols];
+#pragma unroll
+            for (int jj = 0; jj < kTailCols; ++jj)
+                acc[jj] = wt[jj * tile_m + il];
+            for (int s = 1; s < S; ++s) {
+                const float *ws = wt + s * per_tile;
+#pragma unroll
+                for (int jj = 0; jj < kTailCols; ++jj)
+                    acc[jj] = __fadd_rn(acc[jj], ws[jj * tile_m + il]);
+            }
+            const int64_t row = static_cast<int64_t>(b) * p.strideC + i0 + il;
+#pragma unroll
+            for (int jj = 0; jj < kTailCols; ++jj) {
+                if (jb + jj >= p.n)
+                    break;
+                const int64_t idx = row + static_cast<int64_t>(jb + jj) * p.ldc;
+                float v = __fmul_rn(p.alpha, acc[jj]);
+                if (p.beta != 0.0f)
+                    v = __fmaf_rn(p.beta, static_cast<const float *>(p.C)[idx], v);
+                static_cast<float *>(p.D)[idx] = v;
+            }
         }
     }
 }
