@@ -7,10 +7,10 @@
 // accumulator elementwise; "CUDA Handbook, 17.5 Tensor Cores": one MMA instruction
 // is a rank-K slab of the outer-product sum over k).
 //
-//   warp 0 (one lane)   TMA producer: per stage, two 128-byte rows of K for every row of
+//   warp 0 (one lane)   TMA producer: per stage, one 128-byte row of K for every row of
 //                        the CTA's A (128 rows) and B (128 rows per CTA of a pair, 256
 //                        for a single CTA) into a ring of 128-byte-swizzled shared
-//                        memory (3 stages of 64 KiB for a pair); out-of-range
+//                        memory (6 stages of 32 KiB for a pair); out-of-range
 //                        rows/columns/K are zero-filled by TMA, which makes ragged m, n,
 //                        k exact.
 //   warp 1 (one lane)   MMA issuer: tcgen05.mma (M=128 or 256 for a pair, N=256; K=16
@@ -29,7 +29,10 @@
 // drained, TMEM is freed and the kernel returns.  No trap, no unbounded spin.
 //
 // tcg_scale_kernel: D = beta * C (k == 0 or alpha == 0, A and B not read).
-// tcg_tf32_pack_kernel: FP32 -> TF32 (round to nearest even) into a K-major copy.
+// tcg_splitk_reduce_kernel / tcg_tail_reduce_kernel: K-range partial sums added in
+// range order, then alpha, beta and the output rounding.
+// tcg_tf32_round_kernel / tcg_tf32_transpose_round_kernel / tcg_tf32_pack_kernel:
+// FP32 -> TF32 (round to nearest even) into K-major copies.
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
