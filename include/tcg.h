@@ -275,6 +275,16 @@ tcgStatus_t tcg_set_debug(tcgHandle_t h, uint64_t wait_limit_ns, int fault_injec
  * cta_group outside 0..2, group_m outside 0..1024. */
 tcgStatus_t tcg_set_kernel_options(tcgHandle_t h, int cta_group, int group_m);
 
+/* Output tile width (not a step the pages describe -- a scheduling choice): 256
+ * columns, or 128 for problems whose 256-wide tiles would fill at most half of the GPU's
+ * SM pairs and that split K at neither width, so that a small problem's epilogue is
+ * spread over twice the SMs (SM-pair kernel, FP16/BF16 inputs; other calls always use
+ * 256).  tile_n: 0 (default) chooses so; 128 or 256 forces that width wherever a variant
+ * exists.  Results are the same either way: every output element is accumulated in the
+ * same K order (tcg_gemm_tile_plan reports the width a call uses).  INVALID_VALUE: NULL h,
+ * other values. */
+tcgStatus_t tcg_set_tile_n(tcgHandle_t h, int tile_n);
+
 /* K splitting ("split-K"; not a step the pages describe -- a scheduling choice of this
  * library for problems with few output tiles): the K range of every output tile is cut
  * into `splits` consecutive ranges, each range's products are accumulated on their own

@@ -41,7 +41,7 @@ EXPORTS = ("tcg_create", "tcg_destroy", "tcg_set_stream", "tcg_set_workspace",
            "tcg_set_debug", "tcg_launch_count", "tcg_set_kernel_options",
            "tcg_gemm_tf32_noalloc", "tcg_set_split_k", "tcg_split_k_plan",
            "tcg_gemm_split_k", "tcg_gemm_ex_host", "tcg_gemm_strided_batched_host",
-           "tcg_tail_split_plan", "tcg_gemm_tile_plan")
+           "tcg_tail_split_plan", "tcg_gemm_tile_plan", "tcg_set_tile_n")
 
 _lock = threading.Lock()
 _lib = None
@@ -110,6 +110,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.tcg_set_kernel_options.argtypes = [vp, ci, ci]
         lib.tcg_set_split_k.restype = st
         lib.tcg_set_split_k.argtypes = [vp, ci]
+        lib.tcg_set_tile_n.restype = st
+        lib.tcg_set_tile_n.argtypes = [vp, ci]
         lib.tcg_split_k_plan.restype = st
         lib.tcg_split_k_plan.argtypes = [i64, ci, ci, ci, ctypes.POINTER(ci), ctypes.POINTER(ci)]
         lib.tcg_gemm_split_k.restype = st
@@ -220,6 +222,10 @@ def tcg_set_kernel_options(h: int, cta_group: int = 0, group_m: int = 0) -> int:
 
 def tcg_set_split_k(h: int, splits: int = 0) -> int:
     return load_library().tcg_set_split_k(h, splits)
+
+
+def tcg_set_tile_n(h: int, tile_n: int = 0) -> int:
+    return load_library().tcg_set_tile_n(h, tile_n)
 
 
 def tcg_split_k_plan(tiles: int, num_k_blocks: int, clusters: int, forced: int = 0):

@@ -69,6 +69,7 @@ struct tcgContext {
     int cta_group = 2;
     int group_m = 0;           // 0: choose per problem
     int split_k = 0;           // 0: choose per problem, 1: never split, >= 2: that many ranges
+    int tile_n = 0;            // 0: choose per problem, or kBN / kBNNarrow
     // Host-buffer calls: device copies of A, B, C (grown on demand) and two copy streams.
     void *stage_buf[3] = {nullptr, nullptr, nullptr};
     size_t stage_bytes[3] = {0, 0, 0};
@@ -355,27 +356,51 @@ size_t splitk_ws_bytes(int64_t m, int64_t n, int64_t batch, int splits)
     return ((size_t)(batch * splits) * (size_t)(ldw * n) * 4 + 255) / 256 * 256;
 }
 
+// Output tiles of a problem with tiles of (128 cg) x bn.
+int64_t tiles_of(int64_t m, int64_t n, int64_t batch, int cg, int bn)
+{
+    return ((m + kBM * cg - 1) / (kBM * cg)) * ((n + bn - 1) / bn) * batch;
+}
+
 // The K split the GEMM of this problem gets on handle h (see split_plan).
-SplitPlan plan_for(tcgContext *h, int64_t m, int64_t n, int64_t k, int64_t batch, int es, int cg)
+SplitPlan plan_for(tcgContext *h, int64_t m, int64_t n, int64_t k, int64_t batch, int es, int cg,
+                   int bn = kBN)
 {
     if (h->max_ctas[cg] == 0)
         h->max_ctas[cg] = gemm_max_resident_ctas(cg, h->num_sms);
     const int64_t k_block = static_cast<int64_t>(kDepth) * (128 / es);
     const int nkb = static_cast<int>((k + k_block - 1) / k_block);
-    const int64_t tiles = ((m + kBM * cg - 1) / (kBM * cg)) * ((n + kBN - 1) / kBN) * batch;
-    return split_plan(tiles, nkb, h->max_ctas[cg] / cg, h->split_k);
+    return split_plan(tiles_of(m, n, batch, cg, bn), nkb, h->max_ctas[cg] / cg, h->split_k);
+}
+
+// The tile width of a call (see kBNNarrow).  Automatic choice: the narrow tile when the
+// 256-wide tiles would fill at most half of the SM pairs and K is split at neither width
+// (a split already spreads such a problem over the GPU).
+int tile_n_for(tcgContext *h, int64_t m, int64_t n, int64_t k, int64_t batch, int es, int cg,
+               int kind)
+{
+    if (!gemm_has_narrow(cg, kind) || h->tile_n == kBN ||
+        tiles_of(m, n, batch, cg, kBNNarrow) * kMaxSplits > INT32_MAX)
+        return kBN;
+    if (h->tile_n == kBNNarrow)
+        return kBNNarrow;
+    const SplitPlan wide = plan_for(h, m, n, k, batch, es, cg, kBN);
+    const int64_t clusters = h->max_ctas[cg] / cg;
+    if (wide.splits > 1 || clusters <= 0 || tiles_of(m, n, batch, cg, kBN) * 2 > clusters)
+        return kBN;
+    return plan_for(h, m, n, k, batch, es, cg, kBNNarrow).splits > 1 ? kBN : kBNNarrow;
 }
 
 // The tail split of an unsplit problem with FP32 output (see tail_plan); none otherwise.
 // A K block (kDepth x 128 bytes of K for every row) keeps the tensor pipe 512 cycles per
 // 128-byte row busy on either kernel variant; ~1.8 GHz is taken for the tile time.
 TailPlan tail_for(tcgContext *h, int64_t m, int64_t n, int64_t k, int64_t batch, int es, int cg,
-                  bool fp32_out, const SplitPlan &split)
+                  bool fp32_out, const SplitPlan &split, int bn = kBN)
 {
     const int64_t k_block = static_cast<int64_t>(kDepth) * (128 / es);
     const int nkb = static_cast<int>((k + k_block - 1) / k_block);
-    const int64_t tiles = ((m + kBM * cg - 1) / (kBM * cg)) * ((n + kBN - 1) / kBN) * batch;
-    if (!fp32_out || split.splits > 1 || h->split_k != 0)
+    const int64_t tiles = tiles_of(m, n, batch, cg, bn);
+    if (!fp32_out || split.splits > 1 || h->split_k != 0 || bn != kBN)
         return TailPlan{tiles, 1, nkb};
     const double tile_us = nkb * 512.0 * kDepth / 1.8e3;
     return tail_plan(tiles, nkb, h->max_ctas[cg] / cg, tile_us, 4.0 * kBM * cg * kBN);
@@ -441,11 +466,12 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
     const bool tf32 = p.compute == TCG_COMPUTE_32F_FAST_TF32 || split3;
     const int cg = h->cta_group;
     const int es_k = tf32 ? 4 : elem_size(p.Atype);
-    const SplitPlan plan = plan_for(h, p.m, p.n, p.k, p.batch, es_k, cg);
+    const int kind = tf32 ? kKindTF32 : (is_fp8(p.Atype) ? kKindF8 : kKindF16);
+    const int bn = tile_n_for(h, p.m, p.n, p.k, p.batch, es_k, cg, kind);
+    const SplitPlan plan = plan_for(h, p.m, p.n, p.k, p.batch, es_k, cg, bn);
     const TailPlan tail = tail_for(h, p.m, p.n, p.k, p.batch, es_k, cg, p.Ctype == TCG_R_32F,
-                                   plan);
-    const int64_t n_tiles_total = ((p.m + kBM * cg - 1) / (kBM * cg)) * ((p.n + kBN - 1) / kBN) *
-                                  p.batch;
+                                   plan, bn);
+    const int64_t n_tiles_total = tiles_of(p.m, p.n, p.batch, cg, bn);
     const int64_t tail_tiles = tail.splits > 1 ? n_tiles_total - tail.full_tiles : 0;
     const size_t tf32_bytes = tf32 ? (split3 ? 2 : 1) * tf32_ws_bytes(p.m, p.n, p.k, p.batch) : 0;
     const size_t splitk_bytes = plan.splits > 1 ? splitk_ws_bytes(p.m, p.n, p.batch, plan.splits)
@@ -530,7 +556,7 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
         std::memset(&a, 0, sizeof a);
         a.m = m; a.n = n; a.k = k; a.batch = batch;
         a.num_m_tiles = (m + kBM * cg - 1) / (kBM * cg);
-        a.num_n_tiles = (n + kBN - 1) / kBN;
+        a.num_n_tiles = (n + bn - 1) / bn;
         const int es = elem_size(at);
         a.k_row = 128 / es;                           // one 128-byte swizzle row of K
         a.num_k_blocks = (k + kDepth * a.k_row - 1) / (kDepth * a.k_row);
@@ -548,7 +574,7 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
             a.tail_kb_per_split = a.num_k_blocks;
         }
         a.group_m = h->group_m > 0 ? h->group_m : 8;
-        a.kind = tf32 ? kKindTF32 : (fp8 ? kKindF8 : kKindF16);
+        a.kind = kind;
         // operand format codes: kind::f16 F16 = 0, BF16 = 1; kind::tf32 TF32 = 2;
         // kind::f8f6f4 E4M3 = 0, E5M2 = 1
         const uint32_t fmt = tf32 ? 2u
@@ -558,7 +584,7 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
                   | (fmt << 7) | (fmt << 10)              // A, B formats
                   | ((a_kmajor ? 0u : 1u) << 15)          // A: 0 = K-major, 1 = M-major
                   | ((b_kmajor ? 0u : 1u) << 16)          // B: 0 = K-major, 1 = N-major
-                  | (static_cast<uint32_t>(kBN >> 3) << 17)
+                  | (static_cast<uint32_t>(bn >> 3) << 17)           // N = 256 or 128
                   | (static_cast<uint32_t>((kBM * cg) >> 4) << 24);   // M = 128 or 256
         // Split, the kernel writes the raw FP32 accumulators (alpha 1, beta 0) into the
         // partial-sum slices and the reduction applies alpha and beta.
@@ -581,7 +607,7 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
                                      a.k_row, &abc, &a.a_mode, &tmA);
         if (s2 != TCG_STATUS_SUCCESS)
             return s2;
-        s2 = operand_map(h, opB, at, b_kmajor, p.n, p.k, ldb, sB, p.batch, kBN / cg, a.k_row,
+        s2 = operand_map(h, opB, at, b_kmajor, p.n, p.k, ldb, sB, p.batch, bn / cg, a.k_row,
                          &bbc, &a.b_mode, &tmB);
         if (s2 != TCG_STATUS_SUCCESS)
             return s2;
@@ -590,7 +616,8 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
         const int64_t want = static_cast<int64_t>(a.total_tiles) * cg;
         const int grid = static_cast<int>(want < h->max_ctas[cg] ? want : h->max_ctas[cg]);
         cudaError_t e = launch_gemm(tmA, tmB, tmD, tmW, a,
-                                    splitk ? static_cast<int>(kOutF32) : ok, cg, grid, h->stream);
+                                    splitk ? static_cast<int>(kOutF32) : ok, cg, bn, grid,
+                                    h->stream);
         h->launches += 1;
         if (e == cudaSuccess && tail_tiles) {
             int64_t blocks = tail_tiles * (kBN / 16);  // 16 columns of a tail tile per block
@@ -1047,7 +1074,7 @@ tcgStatus_t tcg_gemm_workspace_size(tcgOp_t transa, tcgOp_t transb, int64_t m, i
         if (pl.splits > 1) {
             *bytes += splitk_ws_bytes(m, n, batch_count, pl.splits);
         } else {        // tail split of an FP32-output call
-            const TailPlan tp = tail_plan(tiles, nkb, sms / 2, nkb * 1024.0 / 1.8e3,
+            const TailPlan tp = tail_plan(tiles, nkb, sms / 2, nkb * 512.0 * kDepth / 1.8e3,
                                           4.0 * 2 * kBM * kBN);
             if (tp.splits > 1)
                 *bytes += (size_t)((tiles - tp.full_tiles) * tp.splits) * (size_t)(2 * kBM * kBN) * 4;
@@ -1174,6 +1201,14 @@ tcgStatus_t tcg_set_split_k(tcgHandle_t h, int splits)
     return TCG_STATUS_SUCCESS;
 }
 
+tcgStatus_t tcg_set_tile_n(tcgHandle_t h, int tile_n)
+{
+    if (!h || (tile_n != 0 && tile_n != kBN && tile_n != kBNNarrow))
+        return TCG_STATUS_INVALID_VALUE;
+    h->tile_n = tile_n;
+    return TCG_STATUS_SUCCESS;
+}
+
 tcgStatus_t tcg_split_k_plan(int64_t tiles, int num_k_blocks, int clusters, int forced,
                              int *splits, int *kb_per_split)
 {
@@ -1211,23 +1246,25 @@ tcgStatus_t tcg_gemm_tile_plan(tcgHandle_t h, int64_t m, int64_t n, int64_t k,
     if (st != TCG_STATUS_SUCCESS)
         return st;
     const int cg = h->cta_group;
-    *tile_m = kBM * cg;
-    *tile_n = kBN;
     const bool tf32 = compute == TCG_COMPUTE_32F_FAST_TF32 || compute == TCG_COMPUTE_32F_3XTF32;
     const int es = tf32 ? 4 : elem_size(Atype);
+    const int kind = tf32 ? kKindTF32 : (is_fp8(Atype) ? kKindF8 : kKindF16);
+    const int bn = k > 0 ? tile_n_for(h, m, n, k, batch_count, es, cg, kind) : kBN;
+    *tile_m = kBM * cg;
+    *tile_n = bn;
     const int64_t k_row = 128 / es, k_block = kDepth * k_row;
     GemmArgs a;
     std::memset(&a, 0, sizeof a);
     a.num_m_tiles = static_cast<int>((m + kBM * cg - 1) / (kBM * cg));
-    a.num_n_tiles = static_cast<int>((n + kBN - 1) / kBN);
+    a.num_n_tiles = static_cast<int>((n + bn - 1) / bn);
     a.group_m = h->group_m > 0 ? h->group_m : 8;
     const int64_t tiles = static_cast<int64_t>(a.num_m_tiles) * a.num_n_tiles * batch_count;
     if (max_tiles < tiles || (tiles > 0 && (!splits || !k_per_split)))
         return TCG_STATUS_INVALID_VALUE;
     if (tiles == 0 || k == 0)
         return TCG_STATUS_SUCCESS;
-    const SplitPlan sp = plan_for(h, m, n, k, batch_count, es, cg);
-    const TailPlan tp = tail_for(h, m, n, k, batch_count, es, cg, Ctype == TCG_R_32F, sp);
+    const SplitPlan sp = plan_for(h, m, n, k, batch_count, es, cg, bn);
+    const TailPlan tp = tail_for(h, m, n, k, batch_count, es, cg, Ctype == TCG_R_32F, sp, bn);
     // tiles in raster order -> (b, mt, nt); entry b * mt_count * nt_count + mt * nt_count + nt
     for (int64_t t = 0; t < tiles; ++t) {
         int b, mt, nt;
@@ -1442,7 +1479,7 @@ extern "C" tcgStatus_t tcg_gemm_tf32_noalloc(void *stream, tcgOp_t transa, tcgOp
         return st;
     const int64_t want = static_cast<int64_t>(a.total_tiles) * cg;
     const int grid = static_cast<int>(want < d->max_ctas ? want : d->max_ctas);
-    if (launch_gemm(tmA, tmB, tmD, tmD, a, kOutF32, cg, grid, s) != cudaSuccess) {
+    if (launch_gemm(tmA, tmB, tmD, tmD, a, kOutF32, cg, kBN, grid, s) != cudaSuccess) {
         cudaGetLastError();
         return TCG_STATUS_EXECUTION_FAILED;
     }

@@ -8,16 +8,19 @@
 namespace tcg {
 
 // Tile shape of the persistent GEMM kernel (one CTA per SM).  With a CTA pair
-// (cta_group::2) a tile is 256 x 256: each CTA of the pair holds 128 rows of A and 128
+// (cta_group::2) a tile is 256 x BN: each CTA of the pair holds 128 rows of A and BN / 2
 // rows of B per stage and 128 rows of the accumulator; with a single CTA a tile is
-// 128 x 256 and the CTA holds all 256 rows of B.
+// 128 x BN and the CTA holds all BN rows of B.  BN is 256, or 128 for problems too small
+// to fill the GPU (twice the tiles: the epilogue of a lone tile is spread over twice the
+// SMs; SM-pair kernel with FP16/BF16 inputs only).
 constexpr int kBM = 128;               // rows of D per CTA (MMA M per CTA, TMEM lanes)
 constexpr int kBN = 256;               // columns of D per tile (MMA N, TMEM columns)
+constexpr int kBNNarrow = 128;         // the narrow tile width
 constexpr int kRowBytes = 128;         // one 128-byte swizzle row of K
 constexpr int kDepth = 1;              // 128-byte K rows per operand row and stage
 constexpr int kABytes = kBM * kRowBytes;           // 16 KiB: A for one K row
-constexpr int kAccBufs = 2;            // TMEM accumulator double buffer
-constexpr int kTmemCols = kAccBufs * kBN;          // 512 columns = all of TMEM
+constexpr int kTmemCols = 512;         // all of TMEM: 512 / BN accumulators (2 or 4)
+constexpr int kMaxAccBufs = kTmemCols / kBNNarrow;
 constexpr int kEpiWarps = 8;           // two warps per TMEM lane quarter
 constexpr int kThreads = 32 * (2 + kEpiWarps);     // producer, MMA, 8 epilogue warps
 // Shared memory: operand ring + epilogue staging = kDataBytes.  Epilogue staging: each
@@ -29,7 +32,7 @@ constexpr int kThreads = 32 * (2 + kEpiWarps);     // producer, MMA, 8 epilogue 
 // 256 x 256 problems).
 constexpr int kDataBytes = 224 * 1024;
 constexpr int kEpiChunkBytes = 8 * 1024;
-constexpr int kBarrierBytes = 256;
+constexpr int kBarrierBytes = 512;
 constexpr int kSmemBytes = kDataBytes + kBarrierBytes + 1024;  // + alignment slack
 // Columns of D per epilogue chunk for an output of `bytes` per element.
 __host__ __device__ constexpr int epi_cols(int out_bytes) { return kEpiChunkBytes / (kBM * out_bytes); }
@@ -42,17 +45,18 @@ __host__ __device__ constexpr int epi_cols(int out_bytes) { return kEpiChunkByte
 // MMA issue rate against 91-94%).  M/N-major tiles must still arrive in 16 KiB boxes:
 // one box per 64-row chunk (8 KiB) starved the tensor core (82-90%), so whole-chunk
 // operands use a 4-D view that brings a tile's chunks in one box (OperandMode kMN4).
-template <int CG, int CBUF>
+template <int CG, int CBUF, int BN = kBN>
 struct TileCfg {
     static constexpr int kEpiBufs = CBUF ? CBUF : 2;
     static constexpr int kEpiBytes = 2 * kEpiBufs * kEpiChunkBytes;   // 32 or 64 KiB
     static constexpr int kRingBytes = kDataBytes - kEpiBytes;         // 192 or 160 KiB
-    static constexpr int kBRows = kBN / CG;                  // B rows loaded per CTA
+    static constexpr int kBRows = BN / CG;                   // B rows loaded per CTA
     static constexpr int kAStage = kABytes * kDepth;         // 16 KiB
     static constexpr int kBStage = kBRows * kRowBytes * kDepth;   // 16 KiB (pair), 32 KiB
     static constexpr int kStageBytes = kAStage + kBStage;    // 32 KiB (pair), 48 KiB (1 CTA)
     static constexpr int kStages = kRingBytes / kStageBytes; // pair: 6 (5 with CBUF 4); 1 CTA: 4 (3)
     static constexpr int kTileM = kBM * CG;                  // rows of D per tile
+    static constexpr int kAccBufs = kTmemCols / BN;          // TMEM accumulators (2 or 4)
 };
 
 // Bits of the device error word (which bounded wait gave up).
@@ -208,9 +212,12 @@ inline SplitPlan split_plan(int64_t tiles, int num_k_blocks, int clusters, int f
 // tmD maps D (= C) as {m, n, batch} with box {128, epi_cols(out bytes), 1}, no swizzle.
 // tmW maps the tail partial sums (tile_m x 256 x slices FP32), used only when
 // a.tail_splits > 1 (any valid map otherwise).
+// bn: the tile width (kBN, or kBNNarrow where gemm_has_narrow says a variant exists).
 cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmD,
                         const CUtensorMap &tmW, const GemmArgs &a, int out_kind, int cta_group,
-                        int grid, cudaStream_t s);
+                        int bn, int grid, cudaStream_t s);
+// Whether a narrow-tile (kBNNarrow) variant of the GEMM kernel exists for this launch.
+bool gemm_has_narrow(int cta_group, int kind);
 // D (FP32) of the split tail tiles from their partial sums W (see tcg_tail_reduce_kernel).
 cudaError_t launch_tail_reduce(const float *W, int tail_tiles, int tile_m, const GemmArgs &a,
                                int grid, cudaStream_t s);

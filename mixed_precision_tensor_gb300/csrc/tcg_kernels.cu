@@ -44,14 +44,14 @@
 
 namespace tcg {
 
-constexpr int kMaxStages = TileCfg<2, 0>::kStages;
+constexpr int kMaxStages = TileCfg<2, 0, kBNNarrow>::kStages;
 constexpr int kMaxEpiBufs = 4;
 
 struct SmemCtl {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
-    uint64_t acc_full[kAccBufs];
-    uint64_t acc_empty[kAccBufs];
+    uint64_t acc_full[kMaxAccBufs];
+    uint64_t acc_empty[kMaxAccBufs];
     uint64_t c_full[2][kMaxEpiBufs];   // epilogue half x staging buffer: C chunk landed
     uint64_t drain;
     uint32_t tmem_base;
@@ -174,14 +174,15 @@ __device__ __forceinline__ float load_c(const void *C, int64_t idx)
 // and signal the even CTA's "full" barrier, the MMA completion is multicast to both
 // CTAs' "empty" and "accumulator full" barriers, and both CTAs' epilogues report to the
 // even CTA's "accumulator empty" barrier.
-template <int OUT, int CG, int KIND, int CBUF>
+template <int OUT, int CG, int KIND, int CBUF, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     tcg_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmD,
                     const __grid_constant__ CUtensorMap tmW, const GemmArgs p)
 {
-    using Cfg = TileCfg<CG, CBUF>;
+    using Cfg = TileCfg<CG, CBUF, BN>;
+    constexpr int kAccBufs = Cfg::kAccBufs;
     constexpr bool BETA = CBUF != 0;                          // C is read
     constexpr int kStages = Cfg::kStages;
     constexpr int kRingBytes = Cfg::kRingBytes;
@@ -298,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const UnitInfo w = unit_info(p, t);
                 const int kb_begin = w.kb0, kb_end = w.kb1;
                 const int m0 = w.mt * kTileM + static_cast<int>(rank) * kBM;
-                const int n0 = w.nt * kBN + static_cast<int>(rank) * kBRows;
+                const int n0 = w.nt * BN + static_cast<int>(rank) * kBRows;
                 const int za = p.a_bcast ? 0 : w.b, zb = p.b_bcast ? 0 : w.b;
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
                     const uint32_t fb_local = smem_u32(&ctl->full[stage]);
@@ -367,15 +368,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = cluster_id; ok && t < p.total_tiles; t += num_clusters, ++it) {
                 const UnitInfo w = unit_info(p, t);
                 const int kb_begin = w.kb0, kb_end = w.kb1;
-                const int acc = it & 1;
-                const uint32_t acc_phase = (it >> 1) & 1;
+                const int acc = it % kAccBufs;
+                const uint32_t acc_phase = (it / kAccBufs) & 1;
                 if (!wait_bounded<CG>(smem_u32(&ctl->acc_empty[acc]), acc_phase ^ 1u, ctl, p,
                                       kErrMmaAcc)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
                     if (!wait_bounded<CG>(smem_u32(&ctl->full[stage]), phase, ctl, p,
                                           kErrMmaFull)) {
@@ -433,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // -------------------------------------------------------------- epilogue
-        // Two halves of 4 warps; half h owns TMEM columns [128h, 128h + 128) of each tile
+        // Two halves of 4 warps; half h owns TMEM columns [h BN/2, (h + 1) BN/2) of each tile
         // for all 128 rows (warp w reads TMEM lane quarter w % 4), in chunks of kCols
         // columns.  Per chunk: C (with beta != 0) lands by TMA in a staging buffer, every
         // thread combines its row with the accumulator in place (the buffer is a
@@ -443,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // kEpiBufs - 1 chunks ahead of it (across tile boundaries).
         constexpr int kOutBytes = OUT == kOutF32 ? 4 : 2;
         constexpr int kCols = epi_cols(kOutBytes);             // 16 (FP32) or 32 (16-bit)
-        constexpr int kChunks = (kBN / 2) / kCols;             // per half per tile
+        constexpr int kChunks = (BN / 2) / kCols;              // per half per tile
         constexpr int kAhead = BETA ? kEpiBufs - 1 : 0;        // C loads in flight
         const int q = warp & 3;
         const int half = (warp - 2) >> 2;
@@ -462,9 +463,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // divisions cost hundreds of cycles, so callers evaluate it once per unit.
         auto chunk_origin = [&](const UnitInfo &w, int c, int &x, int &y, int &z, bool &tail) {
             tail = w.tail_slice >= 0;
-            const int xr = static_cast<int>(rank) * kBM, yr = half * (kBN / 2) + c * kCols;
+            const int xr = static_cast<int>(rank) * kBM, yr = half * (BN / 2) + c * kCols;
             x = tail ? xr : w.mt * kTileM + xr;
-            y = tail ? yr : w.nt * kBN + yr;
+            y = tail ? yr : w.nt * BN + yr;
             z = tail ? w.tail_slice : w.b * p.k_splits + w.ks;
         };
         // Leader: start the C load of chunk gg (if it exists) into buffer gg % kEpiBufs.
@@ -500,8 +501,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t g = 0;                                         // chunks done by this half
         int it = 0;
         for (int t = cluster_id; t < p.total_tiles; t += num_clusters, ++it) {
-            const int acc = it & 1;
-            const uint32_t acc_phase = (it >> 1) & 1;
+            const int acc = it % kAccBufs;
+            const uint32_t acc_phase = (it / kAccBufs) & 1;
             bool ok = wait_bounded<CG>(smem_u32(&ctl->acc_full[acc]), acc_phase, ctl, p,
                                        kErrEpilogue);
             if (named_barrier_or(bar_id, 128, !ok || ctl->abort_flag))
@@ -523,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();                                   // tcgen05.ld is warp-collective
                 const uint32_t taddr = tmem_base + lane_off +
-                                       static_cast<uint32_t>(acc * kBN + half * (kBN / 2) + c * kCols);
+                                       static_cast<uint32_t>(acc * BN + half * (BN / 2) + c * kCols);
                 uint32_t v[kCols];
                 if constexpr (kCols == 16)
                     tmem_ld_32x32b_x16(taddr, v);
@@ -792,24 +793,43 @@ template <int CG, int CBUF>
 static GemmKernelFn gemm_fn_cg(int out_kind, int kind)
 {
     if (kind == kKindTF32)   // TF32 inputs always produce FP32 output
-        return tcg_gemm_kernel<kOutF32, CG, kKindTF32, CBUF>;
+        return tcg_gemm_kernel<kOutF32, CG, kKindTF32, CBUF, kBN>;
     if (kind == kKindF8) {
         switch (out_kind) {
-        case kOutF32: return tcg_gemm_kernel<kOutF32, CG, kKindF8, CBUF>;
-        case kOutF16: return tcg_gemm_kernel<kOutF16, CG, kKindF8, CBUF>;
-        default: return tcg_gemm_kernel<kOutBF16, CG, kKindF8, CBUF>;
+        case kOutF32: return tcg_gemm_kernel<kOutF32, CG, kKindF8, CBUF, kBN>;
+        case kOutF16: return tcg_gemm_kernel<kOutF16, CG, kKindF8, CBUF, kBN>;
+        default: return tcg_gemm_kernel<kOutBF16, CG, kKindF8, CBUF, kBN>;
         }
     }
     switch (out_kind) {
-    case kOutF32: return tcg_gemm_kernel<kOutF32, CG, kKindF16, CBUF>;
-    case kOutF16: return tcg_gemm_kernel<kOutF16, CG, kKindF16, CBUF>;
-    default: return tcg_gemm_kernel<kOutBF16, CG, kKindF16, CBUF>;
+    case kOutF32: return tcg_gemm_kernel<kOutF32, CG, kKindF16, CBUF, kBN>;
+    case kOutF16: return tcg_gemm_kernel<kOutF16, CG, kKindF16, CBUF, kBN>;
+    default: return tcg_gemm_kernel<kOutBF16, CG, kKindF16, CBUF, kBN>;
     }
 }
 
-// c_bufs: 0 (beta == 0), 2 or 4 (C staging buffers per epilogue half; 4 only for pairs).
-static GemmKernelFn gemm_fn(int out_kind, int cta_group, int kind, int c_bufs)
+// Narrow tiles (kBNNarrow): SM pairs with FP16/BF16 inputs only.
+template <int CBUF>
+static GemmKernelFn gemm_fn_narrow(int out_kind)
 {
+    switch (out_kind) {
+    case kOutF32: return tcg_gemm_kernel<kOutF32, 2, kKindF16, CBUF, kBNNarrow>;
+    case kOutF16: return tcg_gemm_kernel<kOutF16, 2, kKindF16, CBUF, kBNNarrow>;
+    default: return tcg_gemm_kernel<kOutBF16, 2, kKindF16, CBUF, kBNNarrow>;
+    }
+}
+
+bool gemm_has_narrow(int cta_group, int kind)
+{
+    return cta_group == 2 && kind == kKindF16;
+}
+
+// c_bufs: 0 (beta == 0), 2 or 4 (C staging buffers per epilogue half; 4 only for pairs).
+static GemmKernelFn gemm_fn(int out_kind, int cta_group, int kind, int c_bufs, int bn = kBN)
+{
+    if (bn == kBNNarrow && gemm_has_narrow(cta_group, kind))
+        return c_bufs == 4 ? gemm_fn_narrow<4>(out_kind)
+                           : (c_bufs ? gemm_fn_narrow<2>(out_kind) : gemm_fn_narrow<0>(out_kind));
     if (cta_group == 2) {
         if (c_bufs == 4)
             return gemm_fn_cg<2, 4>(out_kind, kind);
@@ -993,9 +1013,11 @@ cudaError_t launch_tf32_transpose_round(const void *in, int64_t ld, int64_t stri
 
 cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmD,
                         const CUtensorMap &tmW, const GemmArgs &a, int out_kind, int cta_group,
-                        int grid, cudaStream_t s)
+                        int bn, int grid, cudaStream_t s)
 {
-    GemmKernelFn fn = gemm_fn(out_kind, cta_group, a.kind, a.c_bufs);
+    if (bn != kBN && !(bn == kBNNarrow && gemm_has_narrow(cta_group, a.kind)))
+        return cudaErrorInvalidValue;
+    GemmKernelFn fn = gemm_fn(out_kind, cta_group, a.kind, a.c_bufs, bn);
     cudaError_t e = prepare(fn);
     if (e != cudaSuccess)
         return e;

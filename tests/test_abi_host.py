@@ -188,6 +188,11 @@ def test_split_k_argument_checks():
     assert tcg.tcg_split_k_plan(1, 4, 76, 65)[0] == INV
     assert tcg.load_library().tcg_split_k_plan(1, 4, 76, 0, None, None) == INV
     assert tcg.tcg_set_split_k(None, 2) == INV
+    assert tcg.tcg_set_tile_n(None, 128) == INV
+    h = tcg.tcg_create()
+    assert tcg.tcg_set_tile_n(h, 64) == INV and tcg.tcg_set_tile_n(h, 129) == INV
+    assert tcg.tcg_set_tile_n(h, 128) == 0 and tcg.tcg_set_tile_n(h, 0) == 0
+    tcg.tcg_destroy(h)
     assert tcg.tcg_gemm_split_k(None, 1, 1, 1, tcg.TCG_R_16F, tcg.TCG_COMPUTE_32F)[0] == INV
 
 

@@ -38,11 +38,15 @@ def handle(cuda_device):
     h.close()
 
 
-@pytest.fixture(scope="module", params=[1, 2], ids=["1sm", "2sm"])
+@pytest.fixture(scope="module", params=[(1, 0), (2, 256), (2, 128)],
+                ids=["1sm", "2sm", "2sm-n128"])
 def any_handle(cuda_device, request):
-    """A handle on each kernel variant: single-SM 128x256 tiles, SM-pair 256x256 tiles."""
+    """A handle on each kernel variant: single-SM 128x256 tiles, SM-pair 256x256 tiles and
+    SM-pair 256x128 tiles (FP16/BF16 inputs; the others fall back to 256 columns)."""
     h = tcg.Handle()
-    tcg.check(tcg.tcg_set_kernel_options(h.h, request.param, 0))
+    cta_group, tile_n = request.param
+    tcg.check(tcg.tcg_set_kernel_options(h.h, cta_group, 0))
+    tcg.check(tcg.tcg_set_tile_n(h.h, tile_n))
     yield h
     h.close()
 
