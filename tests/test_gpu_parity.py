@@ -612,3 +612,27 @@ def test_seeded_random_configurations(any_handle, case):
                                   batch=batch)
     assert guards_ok, "guard band or ldc padding written"
     _assert_results(res, k, alpha, beta, out_t, exact=False)
+
+
+def test_tile_width_rule(cuda_device):
+    """Narrow (256 x 128) tiles exactly where the rule says: FP16/BF16 inputs on SM pairs,
+    256-wide tiles filling at most half of the pairs, no K split at either width."""
+    h = tcg.Handle()
+    F16, F32, E4M3 = tcg.TCG_R_16F, tcg.TCG_R_32F, tcg.TCG_R_8F_E4M3
+    C32, TF = tcg.TCG_COMPUTE_32F, tcg.TCG_COMPUTE_32F_FAST_TF32
+    width = lambda m, n, k, at=F16, comp=C32, batch=1: tcg.tcg_gemm_tile_plan(
+        h.h, m, n, k, at, comp, F32, batch)[2]
+    assert width(256, 256, 256) == 128                 # one tile: narrow
+    assert width(512, 512, 512) == 128
+    assert width(8192, 8192, 64) == 256                # 1024 tiles: wide
+    assert width(256, 256, 256, batch=512) == 256      # the batched shape: wide
+    assert width(256, 256, 65536) == 256               # K is split: wide
+    assert width(256, 256, 256, at=E4M3) == 256        # no narrow FP8 variant
+    assert width(256, 256, 256, at=F32, comp=TF) == 256
+    tcg.check(tcg.tcg_set_tile_n(h.h, 256))
+    assert width(256, 256, 256) == 256                 # forced
+    tcg.check(tcg.tcg_set_tile_n(h.h, 128))
+    assert width(8192, 8192, 64) == 128
+    tcg.check(tcg.tcg_set_kernel_options(h.h, 1, 0))
+    assert width(256, 256, 256) == 256                 # single-CTA kernel: wide only
+    h.close()
