@@ -117,7 +117,7 @@ tcgStatus_t tcg_set_stream(tcgHandle_t h, void *stream);
 
 /* Give the handle caller-owned device scratch memory for the TF32 path (which
  * writes TF32-rounded, K-major copies of op(A) and op(B) before the product) and for
- * the FP32 partial sums of split-K calls (tcg_set_split_k).
+ * the FP32 partial sums of split-K and tail-split calls (tcg_set_split_k).
  * ptr must be 256-byte aligned; bytes may be 0 to detach.  Without a caller
  * workspace the handle grows one of its own with cudaMalloc on the first TF32
  * call that needs more (not capture-safe).  Errors: INVALID_VALUE. */
@@ -125,8 +125,9 @@ tcgStatus_t tcg_set_workspace(tcgHandle_t h, void *ptr, size_t bytes);
 
 /* Bytes of workspace a tcg_gemm_strided_batched call with these arguments
  * needs on the current device with the default kernel options: TF32 rounded copies,
- * plus the FP32 partial sums when the call splits K (see tcg_set_split_k); 0 for an
- * unsplit 16-bit or FP8 call.  Errors: INVALID_VALUE (NULL bytes). */
+ * plus the FP32 partial sums when the call splits K (see tcg_set_split_k) or cuts the
+ * tiles of a partial last wave (tcg_tail_split_plan); 0 for an unsplit 16-bit or FP8
+ * call.  Errors: INVALID_VALUE (NULL bytes). */
 tcgStatus_t tcg_gemm_workspace_size(tcgOp_t transa, tcgOp_t transb, int64_t m, int64_t n,
                                     int64_t k, tcgDataType_t Atype,
                                     tcgComputeType_t compute, int64_t batch_count,
