@@ -42,7 +42,12 @@
  *   leading dimensions must be multiples of 16 elements (16 bytes).
  *
  * Ownership and threading.  The caller owns every device buffer; libtcg never
- * frees or keeps them.  All calls are asynchronous on the handle's stream and
+ * frees or keeps them.  The device-buffer calls accept only device memory of the
+ * handle's device (cudaMalloc, stream-ordered pool or VMM allocations) for A, B, C
+ * and the workspace: each pointer is checked with cudaPointerGetAttributes (once per
+ * pointer value and handle; the last 16 that passed are remembered), and pageable,
+ * pinned (cudaHostAlloc), managed or another device's memory is INVALID_VALUE with
+ * nothing launched.  Host memory goes through the _host entry points.  All calls are asynchronous on the handle's stream and
  * return without a device synchronisation (except tcg_get_device_error).  A
  * handle is not thread-safe: use one per host thread.  C must not overlap A or
  * B.  The first GEMM call on a handle binds it to the current device and
@@ -154,7 +159,9 @@ tcgStatus_t tcg_gemm_workspace_size(tcgOp_t transa, tcgOp_t transb, int64_t m, i
  * exact in FP32 give bit-exact results.
  *
  * Returns SUCCESS once the work is queued.  INVALID_VALUE: NULL handle or
- * needed pointer, negative sizes, ld too small, misaligned pointer or ld.
+ * needed pointer, negative sizes, ld too small, misaligned pointer or ld, a
+ * pointer (or the caller's workspace) that is not device memory of the handle's
+ * device.
  * NOT_SUPPORTED: type/compute combination.  ARCH_MISMATCH: not sm_103.
  * EXECUTION_FAILED: launch error.  ALLOC_FAILED: first-use allocations.
  */
@@ -239,7 +246,8 @@ tcgStatus_t tcg_gemm_strided_batched_host(tcgHandle_t h, tcgOp_t transa, tcgOp_t
  * handle to report it through.
  *
  * Returns SUCCESS once queued; INVALID_VALUE for the argument errors of
- * tcg_gemm_ex; NOT_SUPPORTED for problems beyond the scratch size;
+ * tcg_gemm_ex (pointers are checked to be device memory of the current device on
+ * every call: there is no handle to remember them in); NOT_SUPPORTED for problems beyond the scratch size;
  * ARCH_MISMATCH off sm_103; NOT_INITIALIZED / EXECUTION_FAILED for CUDA errors.
  */
 tcgStatus_t tcg_gemm_tf32_noalloc(void *stream, tcgOp_t transa, tcgOp_t transb, int64_t m,

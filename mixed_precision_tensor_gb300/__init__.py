@@ -329,6 +329,31 @@ def check(status: int, what: str = "") -> None:
         raise TcgError(status, what)
 
 
+def _check_rowmajor(A, B, C, host: bool) -> None:
+    """Shapes, types, layout and placement that gemm_rowmajor's pointer-level call relies
+    on; the library sees only pointers and leading dimensions, so a mismatch here would
+    otherwise read the wrong elements rather than fail."""
+    if A.dim() not in (2, 3) or B.dim() != A.dim() or C.dim() != A.dim():
+        raise ValueError("gemm_rowmajor: A, B, C must all be 2-D or all 3-D (batched)")
+    if A.shape[:-2] != B.shape[:-2] or A.shape[:-2] != C.shape[:-2]:
+        raise ValueError("gemm_rowmajor: batch sizes of A, B, C differ")
+    m, k = A.shape[-2:]
+    if B.shape[-2] != k or C.shape[-2:] != (m, B.shape[-1]):
+        raise ValueError(f"gemm_rowmajor: shapes {tuple(A.shape)} @ {tuple(B.shape)} -> "
+                         f"{tuple(C.shape)} do not agree")
+    if A.dtype != B.dtype:
+        raise ValueError("gemm_rowmajor: A and B must have the same dtype")
+    if not (A.is_contiguous() and B.is_contiguous() and C.is_contiguous()):
+        raise ValueError("gemm_rowmajor: A, B, C must be contiguous row-major tensors")
+    on_gpu = [t.is_cuda for t in (A, B, C)]
+    if host and any(on_gpu):
+        raise ValueError("gemm_rowmajor(host=True) takes CPU tensors")
+    if not host and not all(on_gpu):
+        raise ValueError("gemm_rowmajor takes CUDA tensors (host=True for CPU tensors)")
+    if not host and len({t.device for t in (A, B, C)}) != 1:
+        raise ValueError("gemm_rowmajor: A, B, C must be on one device")
+
+
 def gemm_rowmajor(handle: Handle, A, B, C, alpha=1.0, beta=0.0, tf32=False,
                   split3=False, host=False) -> None:
     """Row-major D = alpha*A@B + beta*C in place in C (torch CUDA tensors; CPU tensors,
@@ -338,6 +363,7 @@ def gemm_rowmajor(handle: Handle, A, B, C, alpha=1.0, beta=0.0, tf32=False,
     (batch, m, n), all contiguous row-major.  Issued as the column-major call
     gemm(N, N, n, m, k, alpha, B, n, A, k, beta, C, n) (C^T = B^T A^T).
     """
+    _check_rowmajor(A, B, C, host)
     batched = A.dim() == 3
     m, k = A.shape[-2:]
     n = B.shape[-1]

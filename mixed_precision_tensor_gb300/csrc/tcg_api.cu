@@ -30,6 +30,7 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
 
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
 constexpr int kMapCacheSize = 32;
+constexpr int kPtrCacheSize = 16;
 
 struct MapKey {
     const void *ptr;
@@ -80,6 +81,8 @@ struct tcgContext {
     EncodeTiledFn encode = nullptr;
     MapEntry cache[kMapCacheSize];
     int cache_next = 0;
+    const void *ptr_ok[kPtrCacheSize] = {};   // pointers already found to be device memory
+    int ptr_next = 0;
 };
 
 namespace {
@@ -110,6 +113,7 @@ struct Problem {
     int64_t batch;
     tcgComputeType_t compute;
     bool batched;
+    bool staged = false;       // A, B, C are the handle's own staging buffers (host-buffer calls)
 };
 
 // Pure host argument checks: no CUDA call is made before they pass.
@@ -215,6 +219,55 @@ tcgStatus_t bind_device(tcgContext *h)
     h->num_sms = sms;
     h->device = dev;
     return TCG_STATUS_SUCCESS;
+}
+
+// The device-buffer calls hand their pointers to TMA and to plain kernel loads and
+// stores, where a host address would fault the GPU rather than fail the call.  So each
+// pointer must be device memory of the bound device (cudaMalloc, stream-ordered pool or
+// VMM allocation); pageable, pinned (cudaHostAlloc) and managed memory are rejected.
+// The query is a pure lookup, made in relaxed capture mode so that a call being
+// captured into a CUDA graph cannot have it counted as an unsafe call.
+tcgStatus_t device_ptr_ok(int dev, const void *p)
+{
+    cudaPointerAttributes at;
+    cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+    const bool swapped = cudaThreadExchangeStreamCaptureMode(&mode) == cudaSuccess;
+    const cudaError_t e = cudaPointerGetAttributes(&at, p);
+    if (swapped)
+        cudaThreadExchangeStreamCaptureMode(&mode);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return TCG_STATUS_INVALID_VALUE;
+    }
+    return at.type == cudaMemoryTypeDevice && at.device == dev ? TCG_STATUS_SUCCESS
+                                                                : TCG_STATUS_INVALID_VALUE;
+}
+
+// device_ptr_ok with a small per-handle cache of the pointer values that passed, so a
+// repeated call costs no driver query.
+tcgStatus_t device_ptr_cached(tcgContext *h, const void *p)
+{
+    for (int i = 0; i < kPtrCacheSize; ++i)
+        if (h->ptr_ok[i] == p)
+            return TCG_STATUS_SUCCESS;
+    const tcgStatus_t st = device_ptr_ok(h->device, p);
+    if (st == TCG_STATUS_SUCCESS) {
+        h->ptr_ok[h->ptr_next] = p;
+        h->ptr_next = (h->ptr_next + 1) % kPtrCacheSize;
+    }
+    return st;
+}
+
+// The operands a device-buffer call touches: C always, A and B when the product is formed.
+tcgStatus_t check_ptrs(tcgContext *h, const Problem &p)
+{
+    tcgStatus_t st = device_ptr_cached(h, p.C);
+    if (st == TCG_STATUS_SUCCESS && p.k > 0 && p.alpha != 0.0f) {
+        st = device_ptr_cached(h, p.A);
+        if (st == TCG_STATUS_SUCCESS)
+            st = device_ptr_cached(h, p.B);
+    }
+    return st;
 }
 
 CUtensorMapDataType map_type(tcgDataType_t t)
@@ -411,7 +464,7 @@ TailPlan tail_for(tcgContext *h, int64_t m, int64_t n, int64_t k, int64_t batch,
 tcgStatus_t acquire_ws(tcgContext *h, size_t need, void **ws)
 {
     if (h->ws_user) {
-        if (h->ws_user_bytes < need)
+        if (h->ws_user_bytes < need || device_ptr_cached(h, h->ws_user) != TCG_STATUS_SUCCESS)
             return TCG_STATUS_INVALID_VALUE;
         *ws = h->ws_user;
         return TCG_STATUS_SUCCESS;
@@ -444,6 +497,11 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
     st = bind_device(h);
     if (st != TCG_STATUS_SUCCESS)
         return st;
+    if (!p.staged) {
+        st = check_ptrs(h, p);
+        if (st != TCG_STATUS_SUCCESS)
+            return st;
+    }
     h->used = true;
     const int ok = out_kind(p.Ctype);
     const int m = static_cast<int>(p.m), n = static_cast<int>(p.n), k = static_cast<int>(p.k);
@@ -866,6 +924,7 @@ tcgStatus_t run_host(tcgContext *h, const Problem &hp)
                 cudaStreamWaitEvent(h->stream, h->ev_in[c], 0) != cudaSuccess)
                 return fail();
             Problem dp = hp;
+            dp.staged = true;
             dp.m = i1 - i0;
             dp.n = j1 - j0;
             dp.A = hp.transa == TCG_OP_N ? dAc + i0 * esa : dAc + i0 * hp.lda * esa;
@@ -892,6 +951,7 @@ tcgStatus_t run_host(tcgContext *h, const Problem &hp)
     for (int64_t c = 0; c < chunks; ++c) {
         const int64_t u0 = c * per_chunk, u1 = u0 + per_chunk < units ? u0 + per_chunk : units;
         Problem dp = hp;
+        dp.staged = true;
         dp.A = dA;
         dp.B = dB;
         dp.C = dC;
@@ -998,8 +1058,13 @@ tcgStatus_t tcg_destroy(tcgHandle_t h)
 {
     if (!h)
         return TCG_STATUS_INVALID_VALUE;
+    // Drain every stream that may still use the handle's memory before freeing it.
     if (h->used)
         cudaStreamSynchronize(h->stream);
+    if (h->h2d)
+        cudaStreamSynchronize(h->h2d);
+    if (h->d2h)
+        cudaStreamSynchronize(h->d2h);
     if (h->d_err)
         cudaFree(h->d_err);
     if (h->ws_own)
@@ -1007,14 +1072,10 @@ tcgStatus_t tcg_destroy(tcgHandle_t h)
     for (int i = 0; i < 3; ++i)
         if (h->stage_buf[i])
             cudaFree(h->stage_buf[i]);
-    if (h->h2d) {
-        cudaStreamSynchronize(h->h2d);
+    if (h->h2d)
         cudaStreamDestroy(h->h2d);
-    }
-    if (h->d2h) {
-        cudaStreamSynchronize(h->d2h);
+    if (h->d2h)
         cudaStreamDestroy(h->d2h);
-    }
     for (int i = 0; i < kHostChunks; ++i) {
         if (h->ev_in[i])
             cudaEventDestroy(h->ev_in[i]);
@@ -1401,6 +1462,13 @@ extern "C" tcgStatus_t tcg_gemm_tf32_noalloc(void *stream, tcgOp_t transa, tcgOp
     }
     NoAllocDevice *d = nullptr;
     st = noalloc_setup(dev, &d);
+    if (st == TCG_STATUS_SUCCESS)
+        st = device_ptr_ok(dev, C);
+    if (st == TCG_STATUS_SUCCESS && product) {
+        st = device_ptr_ok(dev, A);
+        if (st == TCG_STATUS_SUCCESS)
+            st = device_ptr_ok(dev, B);
+    }
     if (st != TCG_STATUS_SUCCESS)
         return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

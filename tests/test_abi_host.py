@@ -228,3 +228,26 @@ def test_tail_split_plan_rule():
             assert (s - 1) * kb < nkb <= s * kb
     assert tcg.tcg_tail_split_plan(-1, 4, 76, 1.0, 1.0)[0] == tcg.TCG_STATUS_INVALID_VALUE
 
+
+
+def test_gemm_rowmajor_argument_checks(lib):
+    """The row-major convenience refuses operands that the pointer-level call would
+    misread (shapes, dtypes, layout, placement) before calling the library."""
+    import torch
+    h = tcg.Handle()
+    f16 = torch.float16
+    A, B, C = torch.zeros(8, 16, dtype=f16), torch.zeros(16, 24, dtype=f16), torch.zeros(8, 24)
+    bad = [
+        (A, torch.zeros(12, 24, dtype=f16), C, {}),                       # inner sizes differ
+        (A, B, torch.zeros(8, 16), {}),                                   # wrong output shape
+        (A, B.to(torch.bfloat16), C, {}),                                 # A, B dtypes differ
+        (A, torch.zeros(24, 16, dtype=f16).t(), C, {}),                   # not contiguous
+        (A[None], B, C[None], {}),                                        # 3-D with 2-D
+        (A[None].expand(2, 8, 16), B[None].expand(2, 16, 24), C[None].expand(2, 8, 24), {}),
+        (A[None], B[None].repeat(2, 1, 1), C[None], {}),                  # batch sizes differ
+        (A, B, C, {}),                                                    # CPU tensors, device call
+    ]
+    for a, b, c, kw in bad:
+        with pytest.raises(ValueError):
+            tcg.gemm_rowmajor(h, a, b, c, **kw)
+    h.close()

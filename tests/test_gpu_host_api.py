@@ -142,3 +142,53 @@ def test_host_call_degenerate_cases(cuda_device):
                                 tcg.TCG_R_16F, 8, 0.0, C, tcg.TCG_R_32F, 72,
                                 tcg.TCG_COMPUTE_32F) == 0
     h.close()
+
+
+def test_device_call_refuses_host_memory(cuda_device):
+    """Device-buffer calls take device memory only: pageable or pinned host memory for an
+    operand, the output or the workspace is INVALID_VALUE with nothing launched."""
+    h = tcg.Handle()
+    F16, F32 = tcg.TCG_R_16F, tcg.TCG_R_32F
+    C32, TF32 = tcg.TCG_COMPUTE_32F, tcg.TCG_COMPUTE_32F_FAST_TF32
+    INV = tcg.TCG_STATUS_INVALID_VALUE
+    dA = torch.ones(64, 64, dtype=torch.float16, device="cuda")
+    dB = torch.ones(64, 64, dtype=torch.float16, device="cuda")
+    dC = torch.zeros(64, 64, device="cuda")
+    for pin in (False, True):
+        hX = torch.ones(64, 64, dtype=torch.float16)
+        hC = torch.zeros(64, 64)
+        if pin:
+            hX, hC = hX.pin_memory(), hC.pin_memory()
+        before = tcg.tcg_launch_count(h.h)
+        for A, B, C in ((hX, dB, dC), (dA, hX, dC), (dA, dB, hC)):
+            assert tcg.tcg_gemm_ex(h.h, N, N, 64, 64, 64, 1.0, A, F16, 64, B, F16, 64, 0.0, C,
+                                   F32, 64, C32) == INV
+        assert tcg.tcg_gemm_ex(h.h, N, N, 64, 64, 0, 1.0, None, F16, 64, None, F16, 64, 2.0, hC,
+                               F32, 64, C32) == INV            # D = beta*C alone checks C too
+        assert tcg.tcg_gemm_strided_batched(h.h, N, N, 64, 64, 64, 1.0, dA, F16, 64, 0, hX, F16,
+                                            64, 0, 0.0, dC, F32, 64, 4096, 1, C32) == INV
+        assert tcg.tcg_launch_count(h.h) == before
+    # the allocation-free TF32 entry point checks on every call
+    fA = torch.ones(64, 64, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    assert tcg.tcg_gemm_tf32_noalloc(s, N, N, 64, 64, 64, 1.0, fA, 64, fA, 64, 0.0,
+                                     torch.zeros(64, 64).pin_memory(), 64) == INV
+    # a workspace in pinned host memory is refused when a call would use it
+    hw = torch.empty(1 << 20, dtype=torch.uint8).pin_memory()
+    base = (hw.data_ptr() + 255) // 256 * 256
+    tcg.check(tcg.tcg_set_workspace(h.h, base, (1 << 20) - 256))
+    before = tcg.tcg_launch_count(h.h)
+    fC = torch.zeros(64, 64, device="cuda")
+    assert tcg.tcg_gemm_ex(h.h, N, N, 64, 64, 64, 1.0, fA, F32, 64, fA, F32, 64, 0.0, fC, F32,
+                           64, TF32) == INV
+    assert tcg.tcg_launch_count(h.h) == before
+    tcg.check(tcg.tcg_set_workspace(h.h, None, 0))
+    # device memory still works on the same handle
+    tcg.check(tcg.tcg_gemm_ex(h.h, N, N, 64, 64, 64, 1.0, dA, F16, 64, dB, F16, 64, 0.0, dC,
+                              F32, 64, C32))
+    tcg.check(tcg.tcg_gemm_ex(h.h, N, N, 64, 64, 64, 1.0, fA, F32, 64, fA, F32, 64, 0.0, fC,
+                              F32, 64, TF32))
+    tcg.check(tcg.tcg_get_device_error(h.h))
+    torch.cuda.synchronize()
+    assert torch.all(dC == 64.0) and torch.all(fC == 64.0)
+    h.close()
