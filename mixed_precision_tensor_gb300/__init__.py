@@ -368,10 +368,13 @@ def gemm_rowmajor(handle: Handle, A, B, C, alpha=1.0, beta=0.0, tf32=False,
     m, k = A.shape[-2:]
     n = B.shape[-1]
     at, ct = dtype_code(A.dtype), dtype_code(C.dtype)
-    comp = TCG_COMPUTE_32F_FAST_TF32 if (tf32 or A.dtype.is_floating_point and
-                                         at == TCG_R_32F) else TCG_COMPUTE_32F
+    # FP32 inputs always go through TF32 (one product) or its three-product split
     if split3:
         comp = TCG_COMPUTE_32F_3XTF32
+    elif tf32 or at == TCG_R_32F:
+        comp = TCG_COMPUTE_32F_FAST_TF32
+    else:
+        comp = TCG_COMPUTE_32F
     one = tcg_gemm_ex_host if host else tcg_gemm_ex
     many = tcg_gemm_strided_batched_host if host else tcg_gemm_strided_batched
     if not batched:
