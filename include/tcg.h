@@ -47,19 +47,20 @@
  * and the workspace: each pointer is checked with cudaPointerGetAttributes (once per
  * pointer value and handle; the last 16 that passed are remembered), and pageable,
  * pinned (cudaHostAlloc), managed or another device's memory is INVALID_VALUE with
- * nothing launched.  Host memory goes through the _host entry points.  All calls are asynchronous on the handle's stream and
- * return without a device synchronisation (except tcg_get_device_error).  A
- * handle is not thread-safe: use one per host thread.  C must not overlap A or
+ * nothing launched.  Host memory goes through the _host entry points.  All calls
+ * are asynchronous on the handle's stream and return without a device
+ * synchronisation (except tcg_get_device_error).  A handle is not thread-safe: use
+ * one per host thread.  C must not overlap A or
  * B.  The first GEMM call on a handle binds it to the current device and
  * allocates a 4-byte device error word; make that call before any stream
  * capture.  The TF32 path and split-K calls need a workspace (see
  * tcg_set_workspace).  Once bound, and with its workspace large enough, a
  * handle's device-buffer calls can be captured in a CUDA graph: they then make
- * no allocation and no synchronisation, and replays give the eager results bit
- * for bit.
+ * no allocation and no synchronisation (a pointer not seen before is checked in
+ * relaxed capture mode), and replays give the eager results bit for bit.
  *
- * Pointers are device pointers (or memory the device can access, e.g. managed
- * memory) unless stated otherwise.
+ * Pointers are device pointers (device memory of the handle's device, as above)
+ * unless stated otherwise.
  */
 #ifndef TCG_H_
 #define TCG_H_
