@@ -164,7 +164,9 @@ tcgStatus_t tcg_gemm_workspace_size(tcgOp_t transa, tcgOp_t transb, int64_t m, i
  * pointer (or the caller's workspace) that is not device memory of the handle's
  * device.
  * NOT_SUPPORTED: type/compute combination.  ARCH_MISMATCH: not sm_103.
- * EXECUTION_FAILED: launch error.  ALLOC_FAILED: first-use allocations.
+ * EXECUTION_FAILED: launch error, or the driver refused a tensor map (a leading
+ * dimension or stride of 2^40 bytes or more; nothing launched).  ALLOC_FAILED:
+ * first-use allocations.
  */
 tcgStatus_t tcg_gemm_ex(tcgHandle_t h, tcgOp_t transa, tcgOp_t transb, int64_t m, int64_t n,
                         int64_t k, float alpha, const void *A, tcgDataType_t Atype,

@@ -604,6 +604,32 @@ def _fuzz_cases(count=160, seed=20261202):
     return cases
 
 
+def test_encoder_refusal_is_reported(cuda_device):
+    """A tensor map the driver refuses is a host-side failure: EXECUTION_FAILED, nothing
+    launched, the handle still usable.  The refusal is real, not injected: lda = 2^40
+    elements is a 2^41-byte stride, beyond the encoder's 2^40-byte limit.  With k = 1 the
+    kernel would read column 0 of A only (K past 1 is zero-filled, never fetched), so the
+    call stays in bounds even if a map were built."""
+    h = tcg.Handle()
+    F16, F32, C32 = tcg.TCG_R_16F, tcg.TCG_R_32F, tcg.TCG_COMPUTE_32F
+    m, n = 64, 64
+    A = torch.ones(m, dtype=torch.float16, device="cuda")            # column 0 only
+    B = torch.ones(n, 8, dtype=torch.float16, device="cuda")         # k x n, ldb = 8
+    C = torch.zeros(n, m, device="cuda")
+    before = tcg.tcg_launch_count(h.h)
+    st = tcg.tcg_gemm_ex(h.h, N, N, m, n, 1, 1.0, A, F16, 1 << 40, B, F16, 8, 0.0, C, F32, m,
+                         C32)
+    assert st == tcg.TCG_STATUS_EXECUTION_FAILED, tcg.tcg_status_string(st)
+    assert tcg.tcg_launch_count(h.h) == before
+    assert tcg.tcg_get_device_error(h.h) == tcg.TCG_STATUS_SUCCESS
+    tcg.check(tcg.tcg_gemm_ex(h.h, N, N, m, n, 1, 1.0, A, F16, m, B, F16, 8, 0.0, C, F32, m,
+                              C32))
+    tcg.check(tcg.tcg_get_device_error(h.h))
+    torch.cuda.synchronize()
+    assert torch.all(C == 1.0)
+    h.close()
+
+
 @pytest.mark.parametrize("case", _fuzz_cases(), ids=lambda c: f"fuzz{c[0]}")
 def test_seeded_random_configurations(any_handle, case):
     i, m, n, k, transa, transb, in_t, out_t, alpha, beta, batch, extra_ld = case
