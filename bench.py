@@ -40,8 +40,8 @@ def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
 
-def load_peaks():
-    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+def load_peaks(root: str = ROOT):
+    p = os.path.join(root, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
@@ -49,15 +49,15 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def traffic_record(kernel: str, workload: str):
+def traffic_record(kernel: str, workload: str, root: str = ROOT):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the
     current kernel source (its source digest must match), else None."""
     import hashlib
-    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    p = os.path.join(root, "profiles", "dram_traffic.txt")
     if not os.path.exists(p):
         return None
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "mixed_precision_tensor_gb300", "csrc")
+    csrc = os.path.join(root, "mixed_precision_tensor_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
@@ -109,31 +109,38 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        rows = []
-        for line in out.splitlines():
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 10:
-                continue
-            try:
-                ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
-                sm, smax = float(parts[2]), float(parts[3])
-            except ValueError:
-                continue
-            rows.append((ts, sm, smax, parts))
-        during = [r for r in rows if self.t0 and self.t1 and self.t0 <= r[0] <= self.t1]
-        use = during if during else rows[-3:]
-        if not use:
-            return None
-        reasons = set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in use:
-            for nm, v in zip(names, r[3][6:10]):
-                if v.strip().lower() == "active":
-                    reasons.add(nm)
-        return {"sm_mhz": statistics.median(r[1] for r in use),
-                "sm_max_mhz": max(r[2] for r in use),
-                "samples": len(use), "samples_in_timed_region": len(during),
-                "reasons": sorted(reasons)}
+        return summarise_clocks(out, self.t0, self.t1)
+
+
+def summarise_clocks(out: str, t0, t1):
+    """Median SM clock, the maximum clock and the throttle reasons seen in the samples of
+    the timed region [t0, t1] (the last three samples if none fall inside it), from
+    nvidia-smi CSV lines in ClockSampler.FIELDS order; None without samples."""
+    rows = []
+    for line in out.splitlines():
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) < 10:
+            continue
+        try:
+            ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+            sm, smax = float(parts[2]), float(parts[3])
+        except ValueError:
+            continue
+        rows.append((ts, sm, smax, parts))
+    during = [r for r in rows if t0 and t1 and t0 <= r[0] <= t1]
+    use = during if during else rows[-3:]
+    if not use:
+        return None
+    reasons = set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for r in use:
+        for nm, v in zip(names, r[3][6:10]):
+            if v.strip().lower() == "active":
+                reasons.add(nm)
+    return {"sm_mhz": statistics.median(r[1] for r in use),
+            "sm_max_mhz": max(r[2] for r in use),
+            "samples": len(use), "samples_in_timed_region": len(during),
+            "reasons": sorted(reasons)}
 
 
 def dist_setup(n_gpus):
