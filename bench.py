@@ -265,6 +265,39 @@ def run_reference(args, w):
     return 0
 
 
+def roofline_entry(w, kernel_ms, peaks, peak_src, traffic):
+    """The JSON line's roofline object for workload ``w`` whose step took ``kernel_ms``.
+
+    Bound: tensor when the arithmetic intensity (FLOP per algorithmic byte) is at or above
+    the ridge of the measured peaks (~284 FLOP/B), else HBM.  A contraction's peak is the
+    measured dense BF16 rate scaled by the nominal ratio of its own kind: TF32 half, FP8
+    twice, and the three-product TF32 split a third of TF32 (three products per useful
+    one)."""
+    bound = "hbm" if w.flops / max(1, w.algorithmic_bytes()) < 284 else "tensor"
+    if bound == "tensor":
+        peak = float(peaks["bf16_tflops"])        # FP16 and BF16 share the dense rate
+        if w.in_type == "f32":
+            peak = peak / 2.0                     # TF32 dense rate: half of FP16/BF16
+        if w.in_type in ("e4m3", "e5m2"):
+            peak = peak * 2.0                     # FP8 dense rate: twice FP16/BF16
+        if w.compute == "3xtf32":
+            peak = peak / 3.0                     # three TF32 products per useful product
+        achieved = w.flops / (kernel_ms * 1e-3) / 1e12
+        unit = "TFLOP/s"
+    else:
+        peak = float(peaks["hbm_gbs"])
+        achieved = w.algorithmic_bytes() / (kernel_ms * 1e-3) / 1e9
+        unit = "GB/s"
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": traffic,
+            "peak_source": f"{peak_src} ({'bf16_tflops' if bound == 'tensor' else 'hbm_gbs'})",
+            # context: the same ratio against cuBLAS's sustained (power-capped) rate, the
+            # regime a long run of back-to-back calls ends in
+            "frac_of_sustained": (achieved / (peak * float(
+                peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+                / float(peaks["bf16_tflops"])) if bound == "tensor" else None)}
+
+
 def run_ours(args, w):
     import numpy as np
     import torch
@@ -377,22 +410,9 @@ def run_ours(args, w):
     e2e_value = w.flops * world / (e2e_ms * 1e-3) / 1e12
     tcg.check(tcg.tcg_get_device_error(h.h), "e2e")
 
-    bound = "hbm" if w.flops / max(1, w.algorithmic_bytes()) < 284 else "tensor"
-    if bound == "tensor":
-        peak = float(peaks["bf16_tflops"])        # FP16 and BF16 share the dense rate
-        if w.in_type == "f32":
-            peak = peak / 2.0                     # TF32 dense rate: half of FP16/BF16
-        if w.in_type in ("e4m3", "e5m2"):
-            peak = peak * 2.0                     # FP8 dense rate: twice FP16/BF16
-        if w.compute == "3xtf32":
-            peak = peak / 3.0                     # three TF32 products per useful product
-        achieved = w.flops / (kernel_ms * 1e-3) / 1e12
-        unit = "TFLOP/s"
-    else:
-        peak = float(peaks["hbm_gbs"])
-        achieved = w.algorithmic_bytes() / (kernel_ms * 1e-3) / 1e9
-        unit = "GB/s"
-    traffic = traffic_record("tcg_gemm_kernel", w.name)
+    roof = roofline_entry(w, kernel_ms, peaks, peak_src,
+                          traffic_record("tcg_gemm_kernel", w.name))
+    bound, peak = roof["bound"], roof["peak"]
     # Dense tensor peak at the SM clock sampled during the timed region: SMs x nominal
     # dense FLOP per clock per SM (8192 for FP16/BF16 kind::f16, half for kind::tf32; the
     # rate that ncu's tensor-pipe utilisation counter treats as 100%).
@@ -422,14 +442,7 @@ def run_ours(args, w):
         "pct_of_peak": 100.0 * value / world / (peak if bound == "tensor" else float(
             peaks["bf16_tflops"])),
         "tensor_peak_at_clock": at_clock,
-        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                     "frac": achieved / peak, "traffic": traffic,
-                     "peak_source": f"{peak_src} ({'bf16_tflops' if bound == 'tensor' else 'hbm_gbs'})",
-                     # context: the same ratio against cuBLAS's sustained (power-capped) rate,
-                     # the regime a long run of back-to-back calls ends in
-                     "frac_of_sustained": (achieved / (peak * float(
-                         peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-                         / float(peaks["bf16_tflops"])) if bound == "tensor" else None)},
+        "roofline": roof,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,

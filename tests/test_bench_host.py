@@ -94,3 +94,36 @@ def test_peaks_measured_or_fallback(tmp_path):
     (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6500.0}))
     peaks, src = bench.load_peaks(str(tmp_path))
     assert src == "measured" and peaks["hbm_gbs"] == 6500.0
+
+
+def test_roofline_bound_peak_and_fractions():
+    """Bound by arithmetic intensity; each contraction against its own dense peak (BF16
+    measured rate x the nominal ratio of its kind); HBM-bound work against the copy rate."""
+    import pytest
+    from mixed_precision_tensor_gb300 import workloads as wl
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1500.0}
+    W = wl.WORKLOADS
+
+    def at(w, tflops):                      # step time at which w runs at `tflops`
+        return w.flops / (tflops * 1e12) * 1e3
+
+    c2 = W["fp16_gemm_8192"]
+    r = bench.roofline_entry(c2, at(c2, 1000.0), peaks, "measured", 123.0)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["traffic"] == 123.0
+    assert r["peak"] == 2000.0 and r["achieved"] == pytest.approx(1000.0)
+    assert r["frac"] == pytest.approx(0.5)
+    assert r["frac_of_sustained"] == pytest.approx(1000.0 / 1500.0)
+    assert r["peak_source"] == "measured (bf16_tflops)"
+    for name, peak in (("tf32_gemm_4096x4096x16384", 1000.0), ("fp8e4m3_gemm_8192", 4000.0),
+                       ("fp32_3xtf32_4096x4096x16384", 2000.0 / 2.0 / 3.0),  # TF32 / 3
+                       ("bf16_proj_16384x4096x4096", 2000.0)):
+        r = bench.roofline_entry(W[name], 1.0, peaks, "measured", None)
+        assert r["bound"] == "tensor" and r["peak"] == pytest.approx(peak), name
+    # 512 x 256^3 FP16 -> FP16, beta != 0: A, B, C read and D written once, 2 bytes each
+    c5 = W["fp16_batched_512x256"]
+    assert c5.algorithmic_bytes() == 4 * 512 * 256 * 256 * 2
+    ms = c5.algorithmic_bytes() / 3000e9 * 1e3                    # 3000 GB/s
+    r = bench.roofline_entry(c5, ms, peaks, "fallback", None)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == 6000.0
+    assert r["achieved"] == pytest.approx(3000.0) and r["frac"] == pytest.approx(0.5)
+    assert r["frac_of_sustained"] is None and r["peak_source"] == "fallback (hbm_gbs)"
