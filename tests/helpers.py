@@ -96,7 +96,7 @@ def model_block(args, rows, cols, plan=None, batch_entry=0, tf32=False, nthreads
 
 
 def model_rowmajor(w, A, B, C, b=0, rows=None, cols=None, nthreads=None, plan=None):
-    """The block-FMA model (oracle.PAGE_MODEL parameters) for the same row-major problem
+    """The block-FMA model (oracle.MODEL parameters) for the same row-major problem
     and block as :func:`oracle_rowmajor`, with the library's per-tile K ranges ``plan``
     (tcg_gemm_tile_plan of the column-major call, or None).  Returns D as a row-major
     block."""
@@ -110,7 +110,7 @@ def model_rowmajor(w, A, B, C, b=0, rows=None, cols=None, nthreads=None, plan=No
     args = (oracle.OP_N, oracle.OP_N, n, m, k, w.alpha, Bb, t, n, Ab, t, k, w.beta, Cb,
             TYPE_CODE[w.out_type], n)
     D = model_block(args, (j0, j1), (i0, i1), plan=plan, batch_entry=b,
-                    tf32=(w.in_type == "f32"), nthreads=nthreads, **oracle.PAGE_MODEL[t])
+                    tf32=(w.in_type == "f32"), nthreads=nthreads, **oracle.MODEL[t])
     return D.T
 
 
