@@ -243,10 +243,12 @@ tcgStatus_t tcg_gemm_strided_batched_host(tcgHandle_t h, tcgOp_t transa, tcgOp_t
  *
  * The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) and the tensor-map encoder with that device current; make
- * that first call before any stream capture.  The call makes no cudaMalloc,
- * cudaFree or other allocating call.  A bounded device wait that runs out stops
- * the kernel early (output undefined) without a status: this entry point has no
- * handle to report it through.
+ * that first call before any stream capture.  The addresses belong to the device's
+ * context: after a cudaDeviceReset the next call finds a new context (by its id)
+ * and looks them up again, so that first-call rule applies again too.  The call
+ * makes no cudaMalloc, cudaFree or other allocating call.  A bounded device wait
+ * that runs out stops the kernel early (output undefined) and sets a bit in a
+ * device error word of these calls; tcg_noalloc_device_error reports it.
  *
  * Returns SUCCESS once queued; INVALID_VALUE for the argument errors of
  * tcg_gemm_ex (pointers are checked to be device memory of the current device on
@@ -257,6 +259,15 @@ tcgStatus_t tcg_gemm_tf32_noalloc(void *stream, tcgOp_t transa, tcgOp_t transb, 
                                   int64_t n, int64_t k, float alpha, const float *A,
                                   int64_t lda, const float *B, int64_t ldb, float beta,
                                   float *C, int64_t ldc);
+
+/* Status of the tcg_gemm_tf32_noalloc calls on the current device: synchronises
+ * `stream` (a cudaStream_t; NULL = legacy default stream), then reads the calls'
+ * device error word -- a sticky word in the library's own device memory that every
+ * bounded wait that gave up since the last query has marked -- and clears it.
+ * Returns SUCCESS, TIMEOUT (some call's kernel stopped early; its output is
+ * undefined), or EXECUTION_FAILED if the synchronisation or the read failed;
+ * NOT_INITIALIZED without a device.  Allocates nothing (plain symbol copies). */
+tcgStatus_t tcg_noalloc_device_error(void *stream);
 
 /* Synchronise the handle's stream, then return and clear the sticky device
  * error word: SUCCESS, or TIMEOUT if a bounded wait inside a kernel gave up

@@ -39,7 +39,7 @@ EXPORTS = ("tcg_create", "tcg_destroy", "tcg_set_stream", "tcg_set_workspace",
            "tcg_gemm_workspace_size", "tcg_gemm_ex", "tcg_gemm_strided_batched",
            "tcg_get_device_error", "tcg_last_device_error_bits", "tcg_status_string",
            "tcg_set_debug", "tcg_launch_count", "tcg_set_kernel_options",
-           "tcg_gemm_tf32_noalloc", "tcg_set_split_k", "tcg_split_k_plan",
+           "tcg_gemm_tf32_noalloc", "tcg_noalloc_device_error", "tcg_set_split_k", "tcg_split_k_plan",
            "tcg_gemm_split_k", "tcg_gemm_ex_host", "tcg_gemm_strided_batched_host",
            "tcg_tail_split_plan", "tcg_gemm_tile_plan", "tcg_set_tile_n")
 
@@ -117,6 +117,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.tcg_gemm_split_k.restype = st
         lib.tcg_gemm_split_k.argtypes = [vp, i64, i64, i64, ci, ci, i64, ctypes.POINTER(ci),
                                          ctypes.POINTER(i64)]
+        lib.tcg_noalloc_device_error.restype = st
+        lib.tcg_noalloc_device_error.argtypes = [vp]
         lib.tcg_gemm_tf32_noalloc.restype = st
         lib.tcg_gemm_tf32_noalloc.argtypes = [vp, ci, ci, i64, i64, i64, f32, vp, i64, vp, i64,
                                               f32, vp, i64]
@@ -282,6 +284,12 @@ def tcg_gemm_tf32_noalloc(stream, transa, transb, m, n, k, alpha, A, lda, B, ldb
     return load_library().tcg_gemm_tf32_noalloc(stream, transa, transb, m, n, k, float(alpha),
                                                 _ptr(A), lda, _ptr(B), ldb, float(beta),
                                                 _ptr(C), ldc)
+
+
+def tcg_noalloc_device_error(stream) -> int:
+    """Synchronise ``stream`` (raw cudaStream_t or None), then return and clear the
+    status word of the allocation-free calls.  See include/tcg.h."""
+    return load_library().tcg_noalloc_device_error(stream)
 
 
 # ------------------------------------------------------------ conveniences

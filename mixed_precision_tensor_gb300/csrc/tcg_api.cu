@@ -1376,7 +1376,9 @@ tcgStatus_t tcg_gemm_split_k(tcgHandle_t h, int64_t m, int64_t n, int64_t k,
 // The array is a file-scope __device__ object: every GPU that loads the library
 // holds it (kNoAllocScratchBytes) until the process exits.  Host code must not
 // use its name as a pointer (on the host it only stands in for the symbol); the
-// device address is looked up once per device with cudaGetSymbolAddress.
+// device address is looked up once per device and context with
+// cudaGetSymbolAddress: a cudaDeviceReset ends the context, and with it the
+// addresses, so a call made in a new context looks them up again.
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;   // 32 MiB
@@ -1384,8 +1386,12 @@ constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;   // 32 MiB
 __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 __device__ __align__(256) uint32_t g_noalloc_err;
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
 struct NoAllocDevice {
     bool ready = false;
+    unsigned long long ctx_id = 0;   // the context the addresses below belong to
     void *scratch = nullptr;     // device address of g_noalloc_scratch
     uint32_t *err = nullptr;     // device address of g_noalloc_err
     EncodeTiledFn encode = nullptr;
@@ -1396,16 +1402,57 @@ struct NoAllocDevice {
 constexpr int kNoAllocMaxDevices = 64;
 NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
 std::mutex g_noalloc_mutex;
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
 
-// Once per device, with that device current: resolve the scratch and error-word
-// addresses and the tensor-map encoder, and size the persistent grid.
+// Unique id of the calling thread's current context (the runtime's primary context of
+// the current device once a runtime call has made it current).
+tcgStatus_t current_context_id(unsigned long long *id)
+{
+    if (!g_ctx_get_current || !g_ctx_get_id) {
+        void *f1 = nullptr, *f2 = nullptr;
+        cudaDriverEntryPointQueryResult q1, q2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault,
+                                             &q1) != cudaSuccess ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault,
+                                             &q2) != cudaSuccess ||
+            q1 != cudaDriverEntryPointSuccess || q2 != cudaDriverEntryPointSuccess || !f1 ||
+            !f2) {
+            cudaGetLastError();
+            return TCG_STATUS_NOT_INITIALIZED;
+        }
+        g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+        g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f2);
+    }
+    CUcontext ctx = nullptr;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || !ctx || g_ctx_get_id(ctx, id) != CUDA_SUCCESS)
+        return TCG_STATUS_NOT_INITIALIZED;
+    return TCG_STATUS_SUCCESS;
+}
+
+// Once per device and context, with that device current: resolve the scratch and
+// error-word addresses and the tensor-map encoder, and size the persistent grid.
 tcgStatus_t noalloc_setup(int dev, NoAllocDevice **out)
 {
     if (dev < 0 || dev >= kNoAllocMaxDevices)
         return TCG_STATUS_NOT_SUPPORTED;
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    unsigned long long ctx_id = 0;
+    tcgStatus_t cst = current_context_id(&ctx_id);
+    if (cst != TCG_STATUS_SUCCESS) {
+        // No context current on this thread yet: cudaSetDevice makes the device's
+        // primary context current (it allocates nothing).
+        if (cudaSetDevice(dev) != cudaSuccess) {
+            cudaGetLastError();
+            return TCG_STATUS_NOT_INITIALIZED;
+        }
+        cst = current_context_id(&ctx_id);
+        if (cst != TCG_STATUS_SUCCESS)
+            return cst;
+    }
     NoAllocDevice &d = g_noalloc_dev[dev];
-    if (!d.ready) {
+    if (!d.ready || d.ctx_id != ctx_id) {
+        d.ready = false;
         int major = 0, minor = 0, sms = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
@@ -1434,6 +1481,7 @@ tcgStatus_t noalloc_setup(int dev, NoAllocDevice **out)
         d.encode = reinterpret_cast<EncodeTiledFn>(fn);
         d.num_sms = sms;
         d.max_ctas = gemm_max_resident_ctas(2, sms);
+        d.ctx_id = ctx_id;
         d.ready = true;
     }
     *out = &d;
@@ -1496,8 +1544,7 @@ extern "C" tcgStatus_t tcg_gemm_tf32_noalloc(void *stream, tcgOp_t transa, tcgOp
     uint8_t *Bk = Ak + ((size_t)(m * kp) * 4 + 255) / 256 * 256;
     const bool a_kmajor = transa == TCG_OP_T, b_kmajor = transb == TCG_OP_N;
     const int grid_pack = d->num_sms * 8;
-    if (cudaMemsetAsync(d->err, 0, sizeof(uint32_t), s) != cudaSuccess ||
-        launch_tf32_pack(A, lda, 0, a_kmajor ? 1 : 0, static_cast<int>(m), static_cast<int>(k), 1,
+    if (launch_tf32_pack(A, lda, 0, a_kmajor ? 1 : 0, static_cast<int>(m), static_cast<int>(k), 1,
                          Ak, kp, m * kp, grid_pack, s) != cudaSuccess ||
         launch_tf32_pack(B, ldb, 0, b_kmajor ? 1 : 0, static_cast<int>(n), static_cast<int>(k), 1,
                          Bk, kp, n * kp, grid_pack, s) != cudaSuccess) {
@@ -1552,4 +1599,35 @@ extern "C" tcgStatus_t tcg_gemm_tf32_noalloc(void *stream, tcgOp_t transa, tcgOp
         return TCG_STATUS_EXECUTION_FAILED;
     }
     return TCG_STATUS_SUCCESS;
+}
+
+// The error word of the allocation-free calls: every bounded device wait that gave up
+// since the last query has set a bit in it (it starts at zero when the library's module
+// is loaded into a context).  Synchronises `stream` first so that the calls queued on it
+// have finished, then reads and clears the word with plain symbol copies (nothing is
+// allocated).
+extern "C" tcgStatus_t tcg_noalloc_device_error(void *stream)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return TCG_STATUS_NOT_INITIALIZED;
+    }
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return TCG_STATUS_EXECUTION_FAILED;
+    }
+    uint32_t bits = 0;
+    if (cudaMemcpyFromSymbol(&bits, g_noalloc_err, sizeof bits) != cudaSuccess) {
+        cudaGetLastError();
+        return TCG_STATUS_EXECUTION_FAILED;
+    }
+    if (bits == 0)
+        return TCG_STATUS_SUCCESS;
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbol(g_noalloc_err, &zero, sizeof zero) != cudaSuccess) {
+        cudaGetLastError();
+        return TCG_STATUS_EXECUTION_FAILED;
+    }
+    return TCG_STATUS_TIMEOUT;
 }

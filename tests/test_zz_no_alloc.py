@@ -1,13 +1,17 @@
 """The allocation-free TF32 entry point (tcg_gemm_tf32_noalloc) against the
-regular one (tcg_gemm_ex with a workspace).
+regular one (tcg_gemm_ex with a workspace) and against the oracle.
 
 Some callers cannot allocate device memory when they multiply (latency-critical
 loops, processes whose device memory belongs to another allocator); for them the
 library keeps the TF32 path's scratch in a fixed array compiled into it.  This
-file checks, through the C ABI, that two calls in a row give the regular entry
-point's results within the tests' usual bound, and that problems too large for
-the fixed array are refused before any device work.  It sits in its own file,
-collected last, so that a failure here cannot hide the other tests' results.
+file checks, through the C ABI, on calls made one after another: the regular
+entry point's results within the tests' usual bound; the exact oracle's D within
+the same bound; and the block-FMA model bit for bit (the allocation-free call
+never splits K, so every tile is one accumulation over all of K).  All four op
+combinations run.  It also checks that the calls' error word reads clear and that
+problems too large for the fixed array are refused before any device work.  It
+sits in its own file, collected last, so that a failure here cannot hide the
+other tests' results.
 """
 import numpy as np
 import pytest
@@ -65,26 +69,38 @@ def _block(x, c):
     return x[: c["ldc"] * c["n"]].reshape(c["n"], c["ldc"])[:, : c["m"]].T.astype(np.float64)
 
 
-def test_noalloc_matches_regular_entry_point_twice(cuda_device):
+def test_noalloc_matches_regular_entry_point_and_oracle(cuda_device):
     h = tcg.Handle()
     stream = torch.cuda.Stream()
     cases = [_case(101, N, N, 300, 520, 333, 0.75, -0.5),
-             _case(202, T, N, 1024, 768, 2048, 1.0, 1.0)]
-    for c in cases:                                   # two calls in a row
+             _case(202, T, N, 1024, 768, 2048, 1.0, 1.0),
+             _case(303, N, T, 257, 129, 100, 1.0, 0.0),
+             _case(404, T, T, 640, 384, 520, -2.0, 0.25)]
+    for c in cases:                                   # calls one after another
         want = _run_regular(h, c)
         got = _run_noalloc(c, stream)
-        # bound of the parity tests, from the oracle's sum of |a||b|
-        _, _, absab = oracle.gemm(c["transa"], c["transb"], c["m"], c["n"], c["k"], c["alpha"],
-                                  c["A"], oracle.F32, c["lda"], c["B"], oracle.F32, c["ldb"],
-                                  c["beta"], c["C"], oracle.F32, c["ldc"], tf32=True,
-                                  want_r=False)
-        ok, worst, _ = check_bound(_block(got, c), _block(want, c), absab, _block(c["C"], c),
+        args = (c["transa"], c["transb"], c["m"], c["n"], c["k"], c["alpha"], c["A"], oracle.F32,
+                c["lda"], c["B"], oracle.F32, c["ldb"], c["beta"], c["C"], oracle.F32, c["ldc"])
+        D, _, absab = oracle.gemm(*args, tf32=True, want_r=False)
+        cval = _block(c["C"], c)
+        # the regular entry point's result, within the parity tests' bound
+        ok, worst, _ = check_bound(_block(got, c), _block(want, c), absab, cval,
                                    c["k"], c["alpha"], c["beta"], "f32")
-        assert ok, f"worst normalised difference {worst}"
+        assert ok, f"against tcg_gemm_ex: worst normalised difference {worst}"
+        # the exact oracle's D, within the same bound
+        ok, worst, _ = check_bound(_block(got, c), D.astype(np.float64), absab, cval,
+                                   c["k"], c["alpha"], c["beta"], "f32")
+        assert ok, f"against the oracle: worst normalised error {worst}"
+        # the block-FMA model, bit for bit: one accumulation over all of K per tile
+        Dm = oracle.gemm_model(*args, tf32=True, **oracle.MODEL[oracle.F32])
+        g = _block(got, c)
+        same = (g == Dm) | (np.isnan(g) & np.isnan(Dm))
+        assert same.all(), f"{int((~same).sum())} elements differ from the block-FMA model"
         # the ldc padding rows are never written
         pad_in = c["C"][: c["ldc"] * c["n"]].reshape(c["n"], c["ldc"])[:, c["m"]:]
         pad_out = got[: c["ldc"] * c["n"]].reshape(c["n"], c["ldc"])[:, c["m"]:]
         assert np.array_equal(pad_in, pad_out)
+    assert tcg.tcg_noalloc_device_error(stream.cuda_stream) == tcg.TCG_STATUS_SUCCESS
     h.close()
 
 
