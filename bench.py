@@ -19,11 +19,9 @@ workload, and prints the same line with "impl": "reference".
 from __future__ import annotations
 
 import argparse
-import datetime as _dt
 import json
 import os
 import statistics
-import subprocess
 import sys
 import time
 
@@ -73,74 +71,108 @@ def traffic_record(kernel: str, workload: str, root: str = ROOT):
     return None
 
 
-class ClockSampler:
-    """nvidia-smi clock/throttle sampling during the timed region."""
-    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+# NVML (read-only queries) through ctypes: the GPU machine has the driver's libnvidia-ml but
+# no Python NVML package.  Nothing here sets a clock, a limit or any other GPU setting.
+NVML_CLOCK_SM = 1
+# nvmlClocksEventReasons bits (throttle reasons) that the JSON line reports by name
+REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+               "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
 
-    def __init__(self, index: int):
-        self.index = index
-        self.proc = None
-        self.t0 = self.t1 = None
+
+class Nvml:
+    """One GPU's SM clock, maximum SM clock, power draw and clock-event reasons.
+
+    ``lib`` is the loaded NVML library (a ctypes CDLL) or anything with the same
+    functions (the CPU tests pass a fake).  ``uuid`` picks the GPU the CUDA device is
+    (NVML numbers every GPU of the machine, CUDA only the visible ones); ``index`` is
+    the fallback."""
+
+    def __init__(self, lib, uuid=None, index=0):
+        import ctypes
+        self.lib = lib
+        self.c = ctypes
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.dev = ctypes.c_void_p()
+        rc = 1
+        if uuid:
+            rc = lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.dev))
+        if rc != 0:
+            rc = lib.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(self.dev))
+        if rc != 0:
+            raise RuntimeError("no NVML handle for the device")
+        fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self.reasons_fn = fn if fn is not None else lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    @classmethod
+    def open(cls, uuid=None, index=0):
+        import ctypes
+        return cls(ctypes.CDLL("libnvidia-ml.so.1"), uuid, index)
+
+    def sample(self):
+        """(sm_mhz, sm_max_mhz, power_w, reason_bits); None for a field that failed."""
+        c = self.c
+        sm, smax, mw, rs = c.c_uint(), c.c_uint(), c.c_uint(), c.c_ulonglong()
+        ok_sm = self.lib.nvmlDeviceGetClockInfo(self.dev, NVML_CLOCK_SM, c.byref(sm)) == 0
+        ok_max = self.lib.nvmlDeviceGetMaxClockInfo(self.dev, NVML_CLOCK_SM, c.byref(smax)) == 0
+        ok_pw = self.lib.nvmlDeviceGetPowerUsage(self.dev, c.byref(mw)) == 0
+        ok_rs = self.reasons_fn(self.dev, c.byref(rs)) == 0
+        return (float(sm.value) if ok_sm else None, float(smax.value) if ok_max else None,
+                mw.value / 1000.0 if ok_pw else None, int(rs.value) if ok_rs else None)
+
+
+class ClockSampler:
+    """Samples an Nvml source on a background thread every ``period_s`` (1 ms) and
+    summarises the samples that fall inside a timed region (perf_counter times)."""
+
+    def __init__(self, nvml, period_s=0.001):
+        import threading
+        self.nvml = nvml
+        self.period = period_s
+        self.samples = []                     # (t, sm, smax, power_w, reasons)
+        self._stop = threading.Event()
+        self._thread = threading.Thread(target=self._run, daemon=True)
+
+    def _run(self):
+        while not self._stop.is_set():
+            t = time.perf_counter()
+            try:
+                self.samples.append((t,) + tuple(self.nvml.sample()))
+            except Exception:
+                pass
+            self._stop.wait(self.period)
 
     def start(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
-
-    def mark_begin(self):
-        self.t0 = _dt.datetime.now()
-
-    def mark_end(self):
-        self.t1 = _dt.datetime.now()
+        self._thread.start()
+        return self
 
     def stop(self):
-        if self.proc is None:
-            return None
-        time.sleep(0.12)
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
-        return summarise_clocks(out, self.t0, self.t1)
+        self._stop.set()
+        self._thread.join(timeout=2)
+
+    def region(self, t0, t1):
+        return summarise_samples(list(self.samples), t0, t1)
 
 
-def summarise_clocks(out: str, t0, t1):
-    """Median SM clock, the maximum clock and the throttle reasons seen in the samples of
-    the timed region [t0, t1] (the last three samples if none fall inside it), from
-    nvidia-smi CSV lines in ClockSampler.FIELDS order; None without samples."""
-    rows = []
-    for line in out.splitlines():
-        parts = [x.strip() for x in line.split(",")]
-        if len(parts) < 10:
-            continue
-        try:
-            ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
-            sm, smax = float(parts[2]), float(parts[3])
-        except ValueError:
-            continue
-        rows.append((ts, sm, smax, parts))
-    during = [r for r in rows if t0 and t1 and t0 <= r[0] <= t1]
-    use = during if during else rows[-3:]
-    if not use:
-        return None
+def summarise_samples(samples, t0, t1):
+    """Clock record of the timed region [t0, t1]: median SM clock, maximum SM clock,
+    largest power draw and the clock-event reasons seen in the samples taken inside it.
+    With no sample inside, the clock is unknown (None), never borrowed from outside."""
+    during = [r for r in samples if t0 <= r[0] <= t1 and r[1] is not None]
+    if not during:
+        return {"sm_mhz": None, "sm_max_mhz": None, "samples_in_timed_region": 0,
+                "reasons": [], "source": "nvml"}
     reasons = set()
-    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-    for r in use:
-        for nm, v in zip(names, r[3][6:10]):
-            if v.strip().lower() == "active":
-                reasons.add(nm)
-    return {"sm_mhz": statistics.median(r[1] for r in use),
-            "sm_max_mhz": max(r[2] for r in use),
-            "samples": len(use), "samples_in_timed_region": len(during),
-            "reasons": sorted(reasons)}
+    for r in during:
+        if r[4] is not None:
+            reasons.update(nm for nm, bit in REASON_BITS.items() if r[4] & bit)
+    maxes = [r[2] for r in during if r[2] is not None]
+    powers = [r[3] for r in during if r[3] is not None]
+    return {"sm_mhz": statistics.median(r[1] for r in during),
+            "sm_max_mhz": max(maxes) if maxes else None,
+            "power_w_max": max(powers) if powers else None,
+            "samples_in_timed_region": len(during),
+            "reasons": sorted(reasons), "source": "nvml"}
 
 
 def dist_setup(n_gpus):
@@ -298,8 +330,97 @@ def roofline_entry(w, kernel_ms, peaks, peak_src, traffic):
                 / float(peaks["bf16_tflops"])) if bound == "tensor" else None)}
 
 
-def run_ours(args, w):
+def _device_tensors(w, dev):
+    """Workload ``w``'s seeded inputs on the device: (A, B, C0 or None, out, host draws)."""
     import numpy as np
+    import torch
+
+    from mixed_precision_tensor_gb300 import workloads as wl
+    A, B, C = wl.draw(w)
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+    squeeze = w.batch == 1
+    views = {"bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
+
+    def host(x):
+        a = np.ascontiguousarray(x[0] if squeeze else x)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+
+    def to_dev(x, t):
+        tt = host(x).to(dev)
+        return tt.view(views[t]) if t in views else tt
+    dA, dB = to_dev(A, w.in_type), to_dev(B, w.in_type)
+    oshape = (w.m, w.n) if squeeze else (w.batch, w.m, w.n)
+    dC0 = to_dev(C, w.out_type) if C is not None else None
+    dC = dC0.clone() if dC0 is not None else torch.empty(oshape, dtype=tdt[w.out_type],
+                                                         device=dev)
+    return dA, dB, dC, (A, B, C, host, views, oshape, tdt)
+
+
+def time_steps(step, stream, steps, warmup, flush, world, sampler, counter=None):
+    """W untimed warm-up steps, then exactly K timed steps on ``stream`` bracketed by a
+    barrier and a device synchronisation.  Per-step CUDA events on the launching stream
+    (with an L2 flush before each step when ``flush`` is given); the clock record covers
+    the timed region; ``counter`` (the library's launch counter) is read around it.
+    Returns (per-step kernel ms, region ms, clocks, launches in the timed region)."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, warmup)):
+            step()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    n0 = counter() if counter else 0
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        g0.record(stream)
+        for i in range(steps):
+            if flush is not None:
+                flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        g1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    launches = (counter() - n0) if counter else 0
+    barrier(world)
+    kernel_ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / steps
+    region_ms = g0.elapsed_time(g1)
+    clocks = sampler.region(t0, t1) if sampler is not None else None
+    return kernel_ms, region_ms, clocks, launches
+
+
+def per_clk_flops(w):
+    """Dense FLOP per clock per SM of the workload's MMA kind (the rate ncu's tensor-pipe
+    utilisation treats as 100%): 8192 for kind::f16, half for kind::tf32, twice for FP8;
+    the three-product TF32 split delivers a third of the TF32 rate as useful FLOPs."""
+    if w.in_type == "f32":
+        return 4096 // 3 if w.compute == "3xtf32" else 4096
+    return 16384 if w.in_type in ("e4m3", "e5m2") else 8192
+
+
+def at_clock_entry(w, tflops, clocks, sms):
+    """The workload's dense tensor peak at the median SM clock sampled in its timed
+    region, and the fraction reached; None without an in-region clock sample."""
+    if not clocks or not clocks.get("sm_mhz"):
+        return None
+    pk = sms * per_clk_flops(w) * clocks["sm_mhz"] * 1e6 / 1e12
+    return {"sm_mhz": clocks["sm_mhz"], "sms": sms, "flop_per_clk_per_sm": per_clk_flops(w),
+            "peak_tflops": pk, "frac": tflops / pk,
+            "samples_in_timed_region": clocks.get("samples_in_timed_region", 0)}
+
+
+# The other workloads of the run, each timed in the same process with the same steps and
+# warm-up as the headline: the four other synthetic workloads, then the FP8 and
+# three-product TF32 variants of the survey's next rows.
+SIDE_WORKLOADS = ["fp16_gemm_256", "bf16_proj_16384x4096x4096", "tf32_gemm_4096x4096x16384",
+                  "fp16_batched_512x256", "fp8e4m3_gemm_8192", "fp32_3xtf32_4096x4096x16384"]
+
+
+def run_ours(args, w):
     import torch
 
     import mixed_precision_tensor_gb300 as tcg
@@ -310,79 +431,56 @@ def run_ours(args, w):
     dev = torch.device("cuda", local)
     tcg.load_library()
     peaks, peak_src = load_peaks()
-
-    A, B, C = wl.draw(w)
-    tdt = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
-    squeeze = w.batch == 1
-
-    def host(x):
-        a = np.ascontiguousarray(x[0] if squeeze else x)
-        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
-
-    def to_dev(x, t):
-        tt = host(x).to(dev)
-        views = {"bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
-        return tt.view(views[t]) if t in views else tt
-    dA, dB = to_dev(A, w.in_type), to_dev(B, w.in_type)
-    oshape = (w.m, w.n) if squeeze else (w.batch, w.m, w.n)
-    dC0 = to_dev(C, w.out_type) if C is not None else None
-    dC = dC0.clone() if dC0 is not None else torch.empty(oshape, dtype=tdt[w.out_type],
-                                                         device=dev)
+    props = torch.cuda.get_device_properties(dev)
+    sms = props.multi_processor_count
+    sampler = None
+    try:
+        uuid = getattr(props, "uuid", None)
+        sampler = ClockSampler(Nvml.open(f"GPU-{uuid}" if uuid else None, local)).start()
+    except Exception as e:            # no NVML: the clock record says so
+        log(f"clock sampling unavailable: {e}")
     stream = torch.cuda.Stream(device=dev)
     h = tcg.Handle(stream)
+
+    def measure(wk):
+        """Time workload ``wk`` (device-resident inputs); returns its record and tensors."""
+        dA, dB, dC, extra = _device_tensors(wk, dev)
+        A, B, C = extra[0], extra[1], extra[2]
+        in_bytes = A.nbytes + B.nbytes + (C.nbytes if C is not None else 0)
+        flush = (torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+                 if in_bytes <= L2_BYTES else None)
+        tf32 = wk.in_type == "f32"
+
+        def step():
+            tcg.gemm_rowmajor(h, dA, dB, dC, alpha=wk.alpha, beta=wk.beta, tf32=tf32,
+                              split3=wk.compute == "3xtf32")
+        kernel_ms, region_ms, clocks, launches = time_steps(
+            step, stream, args.steps, args.warmup, flush, world, sampler,
+            counter=lambda: tcg.tcg_launch_count(h.h))
+        tcg.check(tcg.tcg_get_device_error(h.h), f"{wk.name}: timed region")
+        step_ms = kernel_ms if flush is not None else region_ms / args.steps
+        step_ms = max_over_ranks(step_ms, world)
+        rec = {"ms_per_step": step_ms, "us_per_call": step_ms * 1e3,
+               "tflops": wk.flops * world / (step_ms * 1e-3) / 1e12,
+               "gpu_launches": launches, "clocks": clocks,
+               "l2": ("inputs larger than L2" if flush is None else
+                      "L2 flushed between steps (write of a 258 MiB buffer)")}
+        rec["roofline"] = roofline_entry(wk, kernel_ms, peaks, peak_src,
+                                         traffic_record("tcg_gemm_kernel", wk.name))
+        rec["tensor_peak_at_clock"] = at_clock_entry(wk, rec["tflops"] / world, clocks, sms)
+        if rec["roofline"]["bound"] == "hbm":
+            rec["hbm_gbs"] = rec["roofline"]["achieved"]
+        return rec, (dA, dB, dC, extra)
+
+    head, (dA, dB, dC, extra) = measure(w)
+    A, B, C, host, views, oshape, tdt = extra
     tf32 = w.in_type == "f32"
-    in_bytes = A.nbytes + B.nbytes + (C.nbytes if C is not None else 0)
-    flush = None
-    if in_bytes <= L2_BYTES:
-        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
-
-    def step():
-        tcg.gemm_rowmajor(h, dA, dB, dC, alpha=w.alpha, beta=w.beta, tf32=tf32,
-                          split3=w.compute == "3xtf32")
-
-    with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup)):
-            step()
-    tcg.check(tcg.tcg_get_device_error(h.h), "warm-up")
-
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    g0 = torch.cuda.Event(enable_timing=True)
-    g1 = torch.cuda.Event(enable_timing=True)
-    launches0 = tcg.tcg_launch_count(h.h)
-    barrier(world)
-    torch.cuda.synchronize()
-    sampler.mark_begin()
-    with torch.cuda.stream(stream):
-        g0.record(stream)
-        for i in range(args.steps):
-            if flush is not None:
-                flush.zero_()
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
-        g1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    sampler.mark_end()
-    launches = tcg.tcg_launch_count(h.h) - launches0
-    tcg.check(tcg.tcg_get_device_error(h.h), "timed region")
-    clocks = sampler.stop()
-    kernel_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps
-    region_ms = g0.elapsed_time(g1)
-    step_ms = kernel_ms if flush is not None else region_ms / args.steps
-    step_ms_max = max_over_ranks(step_ms, world)
-    value = w.flops * world / (step_ms_max * 1e-3) / 1e12
+    value = head["tflops"]
 
     # End to end through the C ABI's host-buffer call (tcg_gemm_ex_host /
     # tcg_gemm_strided_batched_host): pinned host inputs, the copies in, the GEMM and the
     # copy of D back into host memory all inside the timed region; the library pipelines
     # the copies against the product.  Each call returns when D is in host memory.
-    views = {"bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
-
     def pinned(x, t):
         tt = host(x).pin_memory()
         return tt.view(views[t]) if t in views else tt
@@ -409,47 +507,54 @@ def run_ours(args, w):
     e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / e2e_steps, world)
     e2e_value = w.flops * world / (e2e_ms * 1e-3) / 1e12
     tcg.check(tcg.tcg_get_device_error(h.h), "e2e")
+    del hA, hB, hD, dA, dB, dC, extra
 
-    roof = roofline_entry(w, kernel_ms, peaks, peak_src,
-                          traffic_record("tcg_gemm_kernel", w.name))
+    roof = head["roofline"]
     bound, peak = roof["bound"], roof["peak"]
-    # Dense tensor peak at the SM clock sampled during the timed region: SMs x nominal
-    # dense FLOP per clock per SM (8192 for FP16/BF16 kind::f16, half for kind::tf32; the
-    # rate that ncu's tensor-pipe utilisation counter treats as 100%).
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    per_clk = {"f32": 4096 // 3 if w.compute == "3xtf32" else 4096, "e4m3": 16384,
-               "e5m2": 16384}.get(w.in_type, 8192)
-    at_clock = None
-    if clocks and clocks.get("sm_mhz"):
-        pk = sms * per_clk * clocks["sm_mhz"] * 1e6 / 1e12
-        at_clock = {"sm_mhz": clocks["sm_mhz"], "sms": sms, "flop_per_clk_per_sm": per_clk,
-                    "peak_tflops": pk, "frac": value / world / pk}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": max(3, args.warmup), "ms_per_step": step_ms_max, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None,
+        "warmup": max(3, args.warmup), "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": {"f16": "f16", "bf16": "bf16", "f32": "tf32", "e4m3": "e4m3",
                   "e5m2": "e5m2"}[w.in_type] +
                  ("x3" if w.compute == "3xtf32" else ""),
         "data": "synthetic",
         "config": {"workload": w.name, "m": w.m, "n": w.n, "k": w.k, "batch": w.batch,
                    "in": w.in_type, "accumulate": "f32", "out": w.out_type,
-                   "alpha": w.alpha, "beta": w.beta, "seed": w.seed,
-                   "l2": ("inputs larger than L2" if flush is None else
-                          "L2 flushed between steps (write of a 258 MiB buffer)"),
-                   "input_bytes": in_bytes,
+                   "alpha": w.alpha, "beta": w.beta, "seed": w.seed, "l2": head["l2"],
+                   "input_bytes": A.nbytes + B.nbytes + (C.nbytes if C is not None else 0),
                    "parallelism": f"replicas x{world}"},
+        # the headline's fraction of the dense tensor peak: against the measured cuBLAS
+        # burst rate (pct_of_peak, roofline.frac) and against SMs x FLOP/clk x the SM clock
+        # sampled in the timed region (tensor_peak_at_clock)
         "pct_of_peak": 100.0 * value / world / (peak if bound == "tensor" else float(
             peaks["bf16_tflops"])),
-        "tensor_peak_at_clock": at_clock,
+        "tensor_peak_at_clock": head["tensor_peak_at_clock"],
         "roofline": roof,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches,
-        "clocks": clocks,
+        "gpu_launches": head["gpu_launches"],
+        "clocks": head["clocks"],
     }
+    if not args.only_headline:
+        side = {}
+        for name in SIDE_WORKLOADS:
+            if name == w.name:
+                continue
+            wk = wl.WORKLOADS[name]
+            rec, tensors = measure(wk)
+            del tensors
+            rec["config"] = {"m": wk.m, "n": wk.n, "k": wk.k, "batch": wk.batch,
+                             "in": wk.in_type, "out": wk.out_type, "alpha": wk.alpha,
+                             "beta": wk.beta, "seed": wk.seed,
+                             "compute": wk.compute or "default"}
+            side[name] = rec
+            torch.cuda.empty_cache()
+        line["workloads"] = side
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, A, B, C)
+    if sampler is not None:
+        sampler.stop()
     h.close()
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -467,6 +572,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only-headline", action="store_true",
+                    help="time the chosen workload only (no 'workloads' object)")
     args = ap.parse_args()
     from mixed_precision_tensor_gb300 import workloads as wl
     w = wl.WORKLOADS[args.workload or wl.HEADLINE]

@@ -1,47 +1,100 @@
 """Host logic of bench.py that decides what the JSON line may claim, without a GPU:
-the clock summary from nvidia-smi samples (the timed region only; throttle reasons),
+the clock summary from NVML samples (the timed region only; throttle reasons; a fake
+NVML library stands in for the driver's),
 the DRAM-traffic record (reported only while the kernel sources match the digest it
 was measured on) and the choice between measured and fallback peaks."""
-import datetime as dt
 import hashlib
 import json
 import os
 
 import bench
 
-FMT = "%Y/%m/%d %H:%M:%S.%f"
-
-
-def _line(t, sm, smax=2070, hw="Not Active", hwt="Not Active", swt="Not Active",
-          cap="Not Active"):
-    return ", ".join([t.strftime(FMT)[:-3], "0", str(sm), str(smax), "900.0",
-                      "0x0000000000000000", hw, hwt, swt, cap])
-
-
 def test_clock_summary_uses_the_timed_region_only():
-    t0 = dt.datetime(2026, 1, 1, 12, 0, 0)
-    lines = [_line(t0 - dt.timedelta(seconds=1), 2070, hwt="Active"),   # before: ignored
-             "garbage line", "",
-             _line(t0 + dt.timedelta(milliseconds=100), 1400, cap="Active"),
-             _line(t0 + dt.timedelta(milliseconds=200), 1500),
-             _line(t0 + dt.timedelta(milliseconds=300), 1450, cap="Active"),
-             _line(t0 + dt.timedelta(seconds=5), 900, hw="Active")]          # after: ignored
-    s = bench.summarise_clocks("\n".join(lines), t0, t0 + dt.timedelta(seconds=1))
+    cap, hwt = bench.REASON_BITS["sw_power_cap"], bench.REASON_BITS["hw_thermal_slowdown"]
+    samples = [(9.0, 2070.0, 2070.0, 300.0, hwt),          # before the region: ignored
+               (10.1, 1400.0, 2070.0, 1300.0, cap),
+               (10.2, 1500.0, 2070.0, 1350.0, 0),
+               (10.3, 1450.0, 2070.0, 1390.0, cap | 0x1),   # idle bit: not reported
+               (10.4, None, None, None, None),             # a failed query: skipped
+               (15.0, 900.0, 2070.0, 100.0, bench.REASON_BITS["hw_slowdown"])]   # after
+    s = bench.summarise_samples(samples, 10.0, 11.0)
     assert s["sm_mhz"] == 1450 and s["sm_max_mhz"] == 2070
-    assert s["samples"] == 3 and s["samples_in_timed_region"] == 3
+    assert s["samples_in_timed_region"] == 3 and s["power_w_max"] == 1390.0
     assert s["reasons"] == ["sw_power_cap"]
 
 
-def test_clock_summary_falls_back_to_the_last_samples():
-    t0 = dt.datetime(2026, 1, 1, 12, 0, 0)
-    lines = [_line(t0 + dt.timedelta(seconds=i), 1000 + 100 * i,
-                   swt="Active" if i == 4 else "Not Active") for i in range(5)]
-    # a region that no sample falls in: the last three samples stand in, flagged as such
-    s = bench.summarise_clocks("\n".join(lines), t0 - dt.timedelta(hours=1),
-                               t0 - dt.timedelta(minutes=59))
-    assert s["samples_in_timed_region"] == 0 and s["samples"] == 3
-    assert s["sm_mhz"] == 1300 and s["reasons"] == ["sw_thermal_slowdown"]
-    assert bench.summarise_clocks("", t0, t0) is None
+def test_clock_summary_never_borrows_samples_from_outside_the_region():
+    samples = [(float(i), 1000.0 + 100 * i, 2070.0, 500.0, 0) for i in range(5)]
+    s = bench.summarise_samples(samples, 100.0, 101.0)
+    assert s["samples_in_timed_region"] == 0 and s["sm_mhz"] is None
+    assert bench.at_clock_entry(bench_workload(), 1000.0, s, 152) is None
+    assert bench.summarise_samples([], 0.0, 1.0)["sm_mhz"] is None
+
+
+def bench_workload(name="fp16_gemm_8192"):
+    from mixed_precision_tensor_gb300 import workloads as wl
+    return wl.WORKLOADS[name]
+
+
+class _FakeNvml:
+    """The NVML functions bench.Nvml calls, answering like a GPU at 1500 of 2070 MHz under
+    the power cap; records every call, and has no function that sets anything."""
+
+    def __init__(self):
+        self.calls = []
+
+    def _set(self, ref, v):
+        ref._obj.value = v
+
+    def nvmlInit_v2(self):
+        self.calls.append("init")
+        return 0
+
+    def nvmlDeviceGetHandleByUUID(self, uuid, ref):
+        self.calls.append(("uuid", uuid))
+        return 0 if uuid == b"GPU-abc" else 13
+
+    def nvmlDeviceGetHandleByIndex_v2(self, i, ref):
+        self.calls.append(("index", i))
+        return 0
+
+    def nvmlDeviceGetClockInfo(self, dev, kind, ref):
+        assert kind == bench.NVML_CLOCK_SM
+        self._set(ref, 1500)
+        return 0
+
+    def nvmlDeviceGetMaxClockInfo(self, dev, kind, ref):
+        self._set(ref, 2070)
+        return 0
+
+    def nvmlDeviceGetPowerUsage(self, dev, ref):
+        self._set(ref, 1391000)
+        return 0
+
+    def nvmlDeviceGetCurrentClocksEventReasons(self, dev, ref):
+        self._set(ref, bench.REASON_BITS["sw_power_cap"])
+        return 0
+
+
+def test_nvml_sampling_against_a_fake_library():
+    lib = _FakeNvml()
+    n = bench.Nvml(lib, uuid="GPU-abc", index=3)
+    assert ("uuid", b"GPU-abc") in lib.calls and ("index", 3) not in lib.calls
+    assert n.sample() == (1500.0, 2070.0, 1391.0, bench.REASON_BITS["sw_power_cap"])
+    n2 = bench.Nvml(lib, uuid="GPU-other", index=3)            # unknown UUID: the index
+    assert ("index", 3) in lib.calls and n2.sample()[0] == 1500.0
+    sampler = bench.ClockSampler(n, period_s=0.0005).start()
+    import time
+    t0 = time.perf_counter()
+    time.sleep(0.03)
+    t1 = time.perf_counter()
+    sampler.stop()
+    s = sampler.region(t0, t1)
+    assert s["samples_in_timed_region"] >= 5
+    assert s["sm_mhz"] == 1500.0 and s["reasons"] == ["sw_power_cap"]
+    e = bench.at_clock_entry(bench_workload(), 1500.0, s, 152)
+    assert e["peak_tflops"] == 152 * 8192 * 1500e6 / 1e12
+    assert abs(e["frac"] - 1500.0 / e["peak_tflops"]) < 1e-12
 
 
 def _tree(tmp_path, sources, records):
