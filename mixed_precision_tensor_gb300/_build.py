@@ -1,12 +1,16 @@
 """Build libtcg.so in-tree with nvcc for sm_103a (no CMake, no torch extension).
 
 Each .cu file compiles to an object in parallel; the objects link into
-``mixed_precision_tensor_gb300/_lib/libtcg.so`` with a static CUDA runtime.
+``mixed_precision_tensor_gb300/_lib/libtcg.so`` with a static CUDA runtime.  A stamp
+beside the library (``libtcg.so.key``) records a hash of the sources, the flags and the
+host architecture; the library is rebuilt whenever that key differs.
 """
 from __future__ import annotations
 
 import concurrent.futures as cf
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
 
@@ -27,24 +31,47 @@ def nvcc() -> str:
     return path if os.path.exists(path) else (shutil.which("nvcc") or "nvcc")
 
 
+FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC"]
+
+
 def _deps():
-    return [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "tcg.h")]
+    return sorted([os.path.join(CSRC, f) for f in os.listdir(CSRC)] +
+                  [os.path.join(INCLUDE, "tcg.h")])
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def source_key(deps=None) -> str:
+    """What a build depends on: the sources' contents, the compiler flags and the host
+    architecture (a library built on another machine, or from other sources, is stale
+    whatever its modification time)."""
+    h = hashlib.sha256()
+    for d in (deps if deps is not None else _deps()):
+        h.update(os.path.basename(d).encode() + b"\0")
+        with open(d, "rb") as f:
+            h.update(f.read())
+    h.update(" ".join(FLAGS).encode())
+    h.update(platform.machine().encode())
+    return h.hexdigest()
+
+
+def stamp_path(lib_path: str) -> str:
+    return lib_path + ".key"
+
+
+def up_to_date(lib_path: str = LIB_PATH, key: str | None = None) -> bool:
+    """True when ``lib_path`` exists and its stamp records the current source key."""
+    if not os.path.exists(lib_path) or not os.path.exists(stamp_path(lib_path)):
         return False
-    t = os.path.getmtime(LIB_PATH)
-    return all(os.path.getmtime(d) <= t for d in _deps())
+    with open(stamp_path(lib_path)) as f:
+        return f.read().strip() == (key if key is not None else source_key())
 
 
 def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     if not force and up_to_date():
         return LIB_PATH
+    key = source_key()
     os.makedirs(OUT_DIR, exist_ok=True)
     os.makedirs(OBJ_DIR, exist_ok=True)
-    flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-                    "-I", INCLUDE, "-I", CSRC]
+    flags = FLAGS + ["-I", INCLUDE, "-I", CSRC]
     if verbose_ptxas:
         flags += ["-Xptxas", "-v"]
 
@@ -64,6 +91,9 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB_PATH)
+    with open(stamp_path(LIB_PATH) + f".{os.getpid()}.tmp", "w") as f:
+        f.write(key + "\n")
+    os.replace(stamp_path(LIB_PATH) + f".{os.getpid()}.tmp", stamp_path(LIB_PATH))
     if verbose_ptxas:
         for _, log in results:
             print(log)
