@@ -206,7 +206,7 @@ def _issm_batched(kind, A64, B64, batch, m, n):
     tcg.check(tcg.tcg_get_device_error(h.h))
     got = D.cpu().numpy()
     h.close()
-    Araw, Braw = _raw(At, kind), _raw(Bt, kind)
+    Araw, Braw = _raw(At, kind).reshape(-1), _raw(Bt, kind).reshape(-1)
     per_a, per_b = m * k, k * n
     bad = 0
     first = []
