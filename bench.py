@@ -356,7 +356,8 @@ def _device_tensors(w, dev):
     return dA, dB, dC, (A, B, C, host, views, oshape, tdt)
 
 
-def time_steps(step, stream, steps, warmup, flush, world, sampler, counter=None):
+def time_steps(step, stream, steps, warmup, flush, world, sampler, counter=None,
+               before=None):
     """W untimed warm-up steps, then exactly K timed steps on ``stream`` bracketed by a
     barrier and a device synchronisation.  Per-step CUDA events on the launching stream
     (with an L2 flush before each step when ``flush`` is given); the clock record covers
@@ -370,6 +371,8 @@ def time_steps(step, stream, steps, warmup, flush, world, sampler, counter=None)
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     g0 = torch.cuda.Event(enable_timing=True)
     g1 = torch.cuda.Event(enable_timing=True)
+    if before is not None:
+        before()
     barrier(world)
     torch.cuda.synchronize()
     n0 = counter() if counter else 0
@@ -402,15 +405,21 @@ def per_clk_flops(w):
     return 16384 if w.in_type in ("e4m3", "e5m2") else 8192
 
 
-def at_clock_entry(w, tflops, clocks, sms):
-    """The workload's dense tensor peak at the median SM clock sampled in its timed
-    region, and the fraction reached; None without an in-region clock sample."""
-    if not clocks or not clocks.get("sm_mhz"):
+def at_clock_entry(w, tflops, clocks, sms, kernel_mhz=None):
+    """The workload's dense tensor peak at the SM clock of its timed region, and the
+    fraction reached.  The clock is the one the GEMM kernel itself measured (its SM
+    cycles over its nanoseconds, ``kernel_mhz``) when given, else the median of the NVML
+    samples inside the region; None with neither."""
+    mhz, src = None, None
+    if kernel_mhz:
+        mhz, src = kernel_mhz, "kernel clock64 / globaltimer"
+    elif clocks and clocks.get("sm_mhz"):
+        mhz, src = clocks["sm_mhz"], "nvml samples in the timed region"
+    if mhz is None:
         return None
-    pk = sms * per_clk_flops(w) * clocks["sm_mhz"] * 1e6 / 1e12
-    return {"sm_mhz": clocks["sm_mhz"], "sms": sms, "flop_per_clk_per_sm": per_clk_flops(w),
-            "peak_tflops": pk, "frac": tflops / pk,
-            "samples_in_timed_region": clocks.get("samples_in_timed_region", 0)}
+    pk = sms * per_clk_flops(w) * mhz * 1e6 / 1e12
+    return {"sm_mhz": mhz, "clock_source": src, "sms": sms,
+            "flop_per_clk_per_sm": per_clk_flops(w), "peak_tflops": pk, "frac": tflops / pk}
 
 
 # The other workloads of the run, each timed in the same process with the same steps and
@@ -456,7 +465,14 @@ def run_ours(args, w):
                               split3=wk.compute == "3xtf32")
         kernel_ms, region_ms, clocks, launches = time_steps(
             step, stream, args.steps, args.warmup, flush, world, sampler,
-            counter=lambda: tcg.tcg_launch_count(h.h))
+            counter=lambda: tcg.tcg_launch_count(h.h),
+            before=lambda: tcg.check(tcg.tcg_set_clock_probe(h.h, 1), "clock probe"))
+        st, cyc, ns = tcg.tcg_read_clock_probe(h.h)
+        tcg.check(st, "clock probe")
+        tcg.check(tcg.tcg_set_clock_probe(h.h, 0), "clock probe")
+        kernel_mhz = cyc / ns * 1e3 if ns else None
+        if clocks is not None:
+            clocks["sm_mhz_kernel"] = kernel_mhz
         tcg.check(tcg.tcg_get_device_error(h.h), f"{wk.name}: timed region")
         step_ms = kernel_ms if flush is not None else region_ms / args.steps
         step_ms = max_over_ranks(step_ms, world)
@@ -467,7 +483,8 @@ def run_ours(args, w):
                       "L2 flushed between steps (write of a 258 MiB buffer)")}
         rec["roofline"] = roofline_entry(wk, kernel_ms, peaks, peak_src,
                                          traffic_record("tcg_gemm_kernel", wk.name))
-        rec["tensor_peak_at_clock"] = at_clock_entry(wk, rec["tflops"] / world, clocks, sms)
+        rec["tensor_peak_at_clock"] = at_clock_entry(wk, rec["tflops"] / world, clocks, sms,
+                                                     kernel_mhz)
         if rec["roofline"]["bound"] == "hbm":
             rec["hbm_gbs"] = rec["roofline"]["achieved"]
         return rec, (dA, dB, dC, extra)

@@ -290,6 +290,17 @@ const char *tcg_status_string(tcgStatus_t s);
  * trap); 0 turns it off.  INVALID_VALUE: NULL h. */
 tcgStatus_t tcg_set_debug(tcgHandle_t h, uint64_t wait_limit_ns, int fault_inject);
 
+/* Clock probe, for measurement: the SM clock a GEMM kernel actually ran at.  on = 1
+ * zeroes two device counters of the handle (allocated on first use) and makes every
+ * later GEMM-kernel launch on h add, per CTA, the SM cycles (clock64) and the
+ * nanoseconds (globaltimer) it ran for; on = 0 stops adding.  tcg_read_clock_probe
+ * synchronises h's stream and returns the two sums: cycles / ns is the mean SM clock
+ * in GHz over those launches (0 / 0 before any).  The kernels' other work is
+ * unchanged.  INVALID_VALUE: NULL h or output pointer; ALLOC_FAILED,
+ * EXECUTION_FAILED for CUDA errors. */
+tcgStatus_t tcg_set_clock_probe(tcgHandle_t h, int on);
+tcgStatus_t tcg_read_clock_probe(tcgHandle_t h, uint64_t *sm_cycles, uint64_t *ns);
+
 /* Kernel options (0 = default for each).  cta_group: 2 (default) runs each 256x256
  * output tile on a pair of SMs (tcgen05 cta_group::2, B split between the pair's
  * shared memories); 1 runs 128x256 tiles on single SMs.  group_m: how many tile rows

@@ -39,7 +39,8 @@ EXPORTS = ("tcg_create", "tcg_destroy", "tcg_set_stream", "tcg_set_workspace",
            "tcg_gemm_workspace_size", "tcg_gemm_ex", "tcg_gemm_strided_batched",
            "tcg_get_device_error", "tcg_last_device_error_bits", "tcg_status_string",
            "tcg_set_debug", "tcg_launch_count", "tcg_set_kernel_options",
-           "tcg_gemm_tf32_noalloc", "tcg_noalloc_device_error", "tcg_set_split_k", "tcg_split_k_plan",
+           "tcg_gemm_tf32_noalloc", "tcg_noalloc_device_error", "tcg_set_clock_probe",
+           "tcg_read_clock_probe", "tcg_set_split_k", "tcg_split_k_plan",
            "tcg_gemm_split_k", "tcg_gemm_ex_host", "tcg_gemm_strided_batched_host",
            "tcg_tail_split_plan", "tcg_gemm_tile_plan", "tcg_set_tile_n")
 
@@ -117,6 +118,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.tcg_gemm_split_k.restype = st
         lib.tcg_gemm_split_k.argtypes = [vp, i64, i64, i64, ci, ci, i64, ctypes.POINTER(ci),
                                          ctypes.POINTER(i64)]
+        lib.tcg_set_clock_probe.restype = st
+        lib.tcg_set_clock_probe.argtypes = [vp, ci]
+        lib.tcg_read_clock_probe.restype = st
+        lib.tcg_read_clock_probe.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64),
+                                             ctypes.POINTER(ctypes.c_uint64)]
         lib.tcg_noalloc_device_error.restype = st
         lib.tcg_noalloc_device_error.argtypes = [vp]
         lib.tcg_gemm_tf32_noalloc.restype = st
@@ -284,6 +290,19 @@ def tcg_gemm_tf32_noalloc(stream, transa, transb, m, n, k, alpha, A, lda, B, ldb
     return load_library().tcg_gemm_tf32_noalloc(stream, transa, transb, m, n, k, float(alpha),
                                                 _ptr(A), lda, _ptr(B), ldb, float(beta),
                                                 _ptr(C), ldc)
+
+
+def tcg_set_clock_probe(h, on) -> int:
+    """Start (on=1, counters zeroed) or stop adding GEMM kernels' SM cycles and
+    nanoseconds to the handle's clock probe.  See include/tcg.h."""
+    return load_library().tcg_set_clock_probe(h, int(on))
+
+
+def tcg_read_clock_probe(h):
+    """(status, sm_cycles, ns) summed over the probed GEMM launches (syncs h's stream)."""
+    c, n = ctypes.c_uint64(0), ctypes.c_uint64(0)
+    st = load_library().tcg_read_clock_probe(h, ctypes.byref(c), ctypes.byref(n))
+    return st, c.value, n.value
 
 
 def tcg_noalloc_device_error(stream) -> int:

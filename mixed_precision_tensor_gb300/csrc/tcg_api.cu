@@ -59,6 +59,8 @@ struct tcgContext {
     int num_sms = 0;
     cudaStream_t stream = nullptr;
     uint32_t *d_err = nullptr;
+    unsigned long long *d_clk = nullptr;   // clock probe counters (tcg_set_clock_probe)
+    bool clk_on = false;
     void *ws_user = nullptr;
     size_t ws_user_bytes = 0;
     void *ws_own = nullptr;
@@ -659,6 +661,7 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
         a.err = h->d_err;
         a.wait_limit_ns = h->wait_limit_ns;
         a.fault_inject = h->fault_inject;
+        a.clk = h->clk_on ? h->d_clk : nullptr;
         CUtensorMap tmA, tmB;
         bool abc = false, bbc = false;
         tcgStatus_t s2 = operand_map(h, opA, at, a_kmajor, p.m, p.k, lda, sA, p.batch, kBM,
@@ -1067,6 +1070,8 @@ tcgStatus_t tcg_destroy(tcgHandle_t h)
         cudaStreamSynchronize(h->d2h);
     if (h->d_err)
         cudaFree(h->d_err);
+    if (h->d_clk)
+        cudaFree(h->d_clk);
     if (h->ws_own)
         cudaFree(h->ws_own);
     for (int i = 0; i < 3; ++i)
@@ -1244,6 +1249,50 @@ tcgStatus_t tcg_set_debug(tcgHandle_t h, uint64_t wait_limit_ns, int fault_injec
 }
 
 uint64_t tcg_launch_count(tcgHandle_t h) { return h ? h->launches : 0; }
+
+tcgStatus_t tcg_set_clock_probe(tcgHandle_t h, int on)
+{
+    if (!h)
+        return TCG_STATUS_INVALID_VALUE;
+    if (!on) {
+        h->clk_on = false;
+        return TCG_STATUS_SUCCESS;
+    }
+    tcgStatus_t st = bind_device(h);
+    if (st != TCG_STATUS_SUCCESS)
+        return st;
+    if (!h->d_clk) {
+        if (cudaMalloc(&h->d_clk, 2 * sizeof(unsigned long long)) != cudaSuccess) {
+            cudaGetLastError();
+            h->d_clk = nullptr;
+            return TCG_STATUS_ALLOC_FAILED;
+        }
+    }
+    if (cudaMemsetAsync(h->d_clk, 0, 2 * sizeof(unsigned long long), h->stream) != cudaSuccess) {
+        cudaGetLastError();
+        return TCG_STATUS_EXECUTION_FAILED;
+    }
+    h->clk_on = true;
+    return TCG_STATUS_SUCCESS;
+}
+
+tcgStatus_t tcg_read_clock_probe(tcgHandle_t h, uint64_t *sm_cycles, uint64_t *ns)
+{
+    if (!h || !sm_cycles || !ns)
+        return TCG_STATUS_INVALID_VALUE;
+    *sm_cycles = *ns = 0;
+    if (!h->d_clk)
+        return TCG_STATUS_SUCCESS;
+    unsigned long long v[2] = {0, 0};
+    if (cudaStreamSynchronize(h->stream) != cudaSuccess ||
+        cudaMemcpy(v, h->d_clk, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return TCG_STATUS_EXECUTION_FAILED;
+    }
+    *sm_cycles = v[0];
+    *ns = v[1];
+    return TCG_STATUS_SUCCESS;
+}
 
 tcgStatus_t tcg_set_kernel_options(tcgHandle_t h, int cta_group, int group_m)
 {

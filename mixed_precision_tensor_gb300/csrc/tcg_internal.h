@@ -110,6 +110,10 @@ struct GemmArgs {
     unsigned long long wait_limit_ns;
     int fault_inject;
     int c_bufs;                // 0 (beta == 0), 2 or 4: epilogue variant (see TileCfg)
+    // Clock probe (nullptr: off): every CTA adds the SM cycles (clock64) and nanoseconds
+    // (globaltimer) it ran for to clk[0] and clk[1], so clk[0] / clk[1] is the SM clock
+    // the kernel actually ran at.
+    unsigned long long *clk;
 };
 
 // Tile t -> (batch b, m-tile mt, n-tile nt) with grouped rasterisation.

@@ -194,6 +194,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kStageBytes = Cfg::kStageBytes;
     constexpr int kTileM = Cfg::kTileM;
 
+    unsigned long long clk0 = 0, ns0 = 0;
+    if (p.clk && threadIdx.x == 0) {
+        clk0 = clock64();
+        ns0 = globaltimer_ns();
+    }
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle atoms.
     const uint32_t raw_u32 = smem_u32(smem_raw);
@@ -632,6 +637,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_dealloc_pair(tmem_base, kTmemCols);
         else
             tmem_dealloc(tmem_base, kTmemCols);
+    }
+    if (p.clk && threadIdx.x == 0) {
+        atomicAdd(p.clk, static_cast<unsigned long long>(clock64()) - clk0);
+        atomicAdd(p.clk + 1, globaltimer_ns() - ns0);
     }
 }
 

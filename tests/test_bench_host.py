@@ -95,6 +95,12 @@ def test_nvml_sampling_against_a_fake_library():
     e = bench.at_clock_entry(bench_workload(), 1500.0, s, 152)
     assert e["peak_tflops"] == 152 * 8192 * 1500e6 / 1e12
     assert abs(e["frac"] - 1500.0 / e["peak_tflops"]) < 1e-12
+    assert e["clock_source"].startswith("nvml")
+    # the kernel's own clock measurement takes precedence over the NVML samples
+    e = bench.at_clock_entry(bench_workload("tf32_gemm_4096x4096x16384"), 900.0, s, 152,
+                             kernel_mhz=1800.0)
+    assert e["sm_mhz"] == 1800.0 and e["clock_source"].startswith("kernel")
+    assert e["peak_tflops"] == 152 * 4096 * 1800e6 / 1e12
 
 
 def _tree(tmp_path, sources, records):

@@ -192,3 +192,30 @@ def test_device_call_refuses_host_memory(cuda_device):
     torch.cuda.synchronize()
     assert torch.all(dC == 64.0) and torch.all(fC == 64.0)
     h.close()
+
+
+def test_clock_probe_reports_the_kernels_sm_clock(cuda_device):
+    """The clock probe sums every GEMM CTA's SM cycles and nanoseconds: the ratio is a
+    plausible SM clock, it counts only while on, and the results are unchanged."""
+    h = tcg.Handle()
+    A = torch.ones(1024, 1024, dtype=torch.float16, device="cuda")
+    B = torch.ones(1024, 1024, dtype=torch.float16, device="cuda")
+    C = torch.zeros(1024, 1024, device="cuda")
+    st, cyc, ns = tcg.tcg_read_clock_probe(h.h)
+    assert st == tcg.TCG_STATUS_SUCCESS and cyc == 0 and ns == 0       # never enabled
+    tcg.check(tcg.tcg_set_clock_probe(h.h, 1))
+    for _ in range(3):
+        tcg.gemm_rowmajor(h, A, B, C)
+    st, cyc, ns = tcg.tcg_read_clock_probe(h.h)
+    tcg.check(st)
+    assert cyc > 0 and ns > 0
+    ghz = cyc / ns
+    assert 0.3 < ghz < 2.5, ghz
+    tcg.check(tcg.tcg_set_clock_probe(h.h, 0))
+    tcg.gemm_rowmajor(h, A, B, C)
+    st, cyc2, ns2 = tcg.tcg_read_clock_probe(h.h)
+    assert (cyc2, ns2) == (cyc, ns)                                   # off: not counted
+    torch.cuda.synchronize()
+    assert torch.all(C == 1024.0)
+    tcg.check(tcg.tcg_get_device_error(h.h))
+    h.close()
