@@ -15,10 +15,12 @@ pytestmark = pytest.mark.gpu
 N, T = tcg.TCG_OP_N, tcg.TCG_OP_T
 
 CASES = [
-    # m, n, k, in, compute, out: a plain tile grid, a split-K shape, TF32 (workspace)
+    # m, n, k, in, compute, out: a plain tile grid, a split-K shape, TF32 and the
+    # three-product TF32 split (both round into the workspace first)
     (512, 768, 320, torch.float16, tcg.TCG_COMPUTE_32F, torch.float32),
     (256, 256, 16384, torch.bfloat16, tcg.TCG_COMPUTE_32F, torch.bfloat16),
     (384, 640, 1000, torch.float32, tcg.TCG_COMPUTE_32F_FAST_TF32, torch.float32),
+    (384, 640, 1000, torch.float32, tcg.TCG_COMPUTE_32F_3XTF32, torch.float32),
 ]
 
 

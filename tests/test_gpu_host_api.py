@@ -150,6 +150,7 @@ def test_device_call_refuses_host_memory(cuda_device):
     h = tcg.Handle()
     F16, F32 = tcg.TCG_R_16F, tcg.TCG_R_32F
     C32, TF32 = tcg.TCG_COMPUTE_32F, tcg.TCG_COMPUTE_32F_FAST_TF32
+    SPLIT3 = tcg.TCG_COMPUTE_32F_3XTF32
     INV = tcg.TCG_STATUS_INVALID_VALUE
     dA = torch.ones(64, 64, dtype=torch.float16, device="cuda")
     dB = torch.ones(64, 64, dtype=torch.float16, device="cuda")
@@ -173,14 +174,15 @@ def test_device_call_refuses_host_memory(cuda_device):
     s = torch.cuda.current_stream().cuda_stream
     assert tcg.tcg_gemm_tf32_noalloc(s, N, N, 64, 64, 64, 1.0, fA, 64, fA, 64, 0.0,
                                      torch.zeros(64, 64).pin_memory(), 64) == INV
-    # a workspace in pinned host memory is refused when a call would use it
+    # a workspace in pinned host memory is refused when a call would use it (the
+    # three-product TF32 split writes its rounded operand words there)
     hw = torch.empty(1 << 20, dtype=torch.uint8).pin_memory()
     base = (hw.data_ptr() + 255) // 256 * 256
     tcg.check(tcg.tcg_set_workspace(h.h, base, (1 << 20) - 256))
     before = tcg.tcg_launch_count(h.h)
     fC = torch.zeros(64, 64, device="cuda")
     assert tcg.tcg_gemm_ex(h.h, N, N, 64, 64, 64, 1.0, fA, F32, 64, fA, F32, 64, 0.0, fC, F32,
-                           64, TF32) == INV
+                           64, SPLIT3) == INV
     assert tcg.tcg_launch_count(h.h) == before
     tcg.check(tcg.tcg_set_workspace(h.h, None, 0))
     # device memory still works on the same handle

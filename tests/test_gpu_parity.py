@@ -562,22 +562,25 @@ def test_large_workload_sampled_integer(handle, name):
     _check_sampled(w, A, B, C, out, exact=True, count=64)
 
 
+@pytest.mark.parametrize("dtype", [torch.float16, torch.float32], ids=["f16", "tf32"])
 @pytest.mark.parametrize("cta_group", [1, 2])
-def test_timeout_is_reported_not_hung(cuda_device, cta_group):
+def test_timeout_is_reported_not_hung(cuda_device, cta_group, dtype):
     """A bounded wait that runs out (a stage nobody fills) ends the kernel with a
-    TIMEOUT status in the error word; the context stays usable afterwards."""
+    TIMEOUT status in the error word; the context stays usable afterwards.  With TF32
+    inputs the wait that runs out is the converter warps' (the raw stage never lands)."""
     h = tcg.Handle()
     tcg.check(tcg.tcg_set_kernel_options(h.h, cta_group, 0))
-    A = torch.ones(256, 256, dtype=torch.float16, device="cuda")
-    B = torch.ones(256, 256, dtype=torch.float16, device="cuda")
+    A = torch.ones(256, 256, dtype=dtype, device="cuda")
+    B = torch.ones(256, 256, dtype=dtype, device="cuda")
     C = torch.zeros(256, 256, device="cuda")
+    tf32 = dtype == torch.float32
     tcg.check(tcg.tcg_set_debug(h.h, 200_000_000, 1))          # 0.2 s, skip one load
-    tcg.gemm_rowmajor(h, A, B, C)
+    tcg.gemm_rowmajor(h, A, B, C, tf32=tf32)
     st = tcg.tcg_get_device_error(h.h)
     assert st == tcg.TCG_STATUS_TIMEOUT
     assert tcg.tcg_last_device_error_bits(h.h) != 0
     tcg.check(tcg.tcg_set_debug(h.h, 0, 0))
-    tcg.gemm_rowmajor(h, A, B, C)
+    tcg.gemm_rowmajor(h, A, B, C, tf32=tf32)
     assert tcg.tcg_get_device_error(h.h) == tcg.TCG_STATUS_SUCCESS
     torch.cuda.synchronize()
     assert torch.all(C == 256.0)
@@ -665,3 +668,52 @@ def test_tile_width_rule(cuda_device):
     tcg.check(tcg.tcg_set_kernel_options(h.h, 1, 0))
     assert width(256, 256, 256) == 256                 # single-CTA kernel: wide only
     h.close()
+
+
+def _tie_patterns(rng, n):
+    """FP32 values whose low 13 bits sit at, just below or just above the TF32 rounding
+    tie (0x1000), with an odd or even last kept bit, over finite exponents (subnormals
+    included); none rounds past the largest finite value."""
+    sign = rng.integers(0, 2, n).astype(np.uint32) << 31
+    expo = rng.integers(0, 254, n).astype(np.uint32) << 23          # 0: subnormal
+    keep = rng.integers(0, 1 << 10, n).astype(np.uint32) << 13       # kept mantissa bits
+    low = rng.choice(np.array([0x1000, 0x0FFF, 0x1001, 0x0000, 0x1FFF, 0x0001],
+                              dtype=np.uint32), n)
+    return (sign | expo | keep | low).view(np.float32)
+
+
+@pytest.mark.parametrize("transa,transb", [(N, N), (T, N), (N, T), (T, T)])
+def test_tf32_input_rounding_is_nearest_even(handle, transa, transb):
+    """FP32 inputs reach the tensor core rounded to TF32 to nearest, ties to even (not
+    cut): with the other operand an identity, D is the rounded input itself, bit for bit
+    against the oracle's TF32 rounding (pinned exhaustively on the CPU).  Ties with an
+    odd and an even last kept bit, values just below and above a tie, and subnormals;
+    both operands, every op combination, ragged M/N/K."""
+    rng = np.random.default_rng(77 + 2 * transa + transb)
+    m, k = 200, 72
+    dev = torch.device("cuda:0")
+    for side in ("A", "B"):
+        vals = _tie_patterns(rng, m * k).reshape(m, k)             # the operand's m x k values
+        eye = np.eye(k, dtype=np.float32)
+        if side == "A":                 # D (m x k) = vals (m x k) * I (k x k)
+            M, Nn, Aop, Bop = m, k, vals, eye
+        else:                           # D (k x m) = I (k x k) * vals^T (k x m)
+            M, Nn, Aop, Bop = k, m, eye, vals.T.copy()
+        Acol = Aop.T.copy() if transa == N else Aop.copy()          # column-major storage
+        Bcol = Bop.T.copy() if transb == N else Bop.copy()
+        lda = M if transa == N else k
+        ldb = k if transb == N else Nn
+        dA, dB = torch.from_numpy(Acol.reshape(-1)).to(dev), torch.from_numpy(Bcol.reshape(-1)).to(dev)
+        C = torch.zeros(Nn * M, device=dev)
+        tcg.check(tcg.tcg_gemm_ex(handle.h, transa, transb, M, Nn, k, 1.0, dA, tcg.TCG_R_32F, lda,
+                                  dB, tcg.TCG_R_32F, ldb, 0.0, C, tcg.TCG_R_32F, M,
+                                  tcg.TCG_COMPUTE_32F_FAST_TF32))
+        tcg.check(tcg.tcg_get_device_error(handle.h))
+        got = C.cpu().numpy().reshape(Nn, M).T                       # (M, Nn)
+        want = oracle.tf32_round_bits(vals.view(np.uint32)).view(np.float32)
+        if side == "B":
+            want = want.T
+        cut = (vals.view(np.uint32) & np.uint32(0xFFFFE000)).view(np.float32)
+        assert values_equal(got, want), f"operand {side}: not RNE-rounded"
+        # the data does tell nearest-even from a plain cut
+        assert not values_equal(cut if side == "A" else cut.T, want)
