@@ -450,14 +450,14 @@ int tile_n_for(tcgContext *h, int64_t m, int64_t n, int64_t k, int64_t batch, in
 // A K block (kDepth x 128 bytes of K for every row) keeps the tensor pipe 512 cycles per
 // 128-byte row busy on either kernel variant; ~1.8 GHz is taken for the tile time.
 TailPlan tail_for(tcgContext *h, int64_t m, int64_t n, int64_t k, int64_t batch, int es, int cg,
-                  bool fp32_out, const SplitPlan &split, int bn = kBN)
+                  bool fp32_out, const SplitPlan &split, int bn = kBN, double mmas_per_slice = 1.0)
 {
     const int64_t k_block = static_cast<int64_t>(kDepth) * (128 / es);
     const int nkb = static_cast<int>((k + k_block - 1) / k_block);
     const int64_t tiles = tiles_of(m, n, batch, cg, bn);
     if (!fp32_out || split.splits > 1 || h->split_k != 0 || bn != kBN)
         return TailPlan{tiles, 1, nkb};
-    const double tile_us = nkb * 512.0 * kDepth / 1.8e3;
+    const double tile_us = nkb * 512.0 * kDepth * mmas_per_slice / 1.8e3;
     return tail_plan(tiles, nkb, h->max_ctas[cg] / cg, tile_us, 4.0 * kBM * cg * kBN);
 }
 
@@ -526,11 +526,13 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
     const bool tf32 = p.compute == TCG_COMPUTE_32F_FAST_TF32 || split3;
     const int cg = h->cta_group;
     const int es_k = tf32 ? 4 : elem_size(p.Atype);
-    const int kind = tf32 ? kKindTF32 : (is_fp8(p.Atype) ? kKindF8 : kKindF16);
+    // The two-word split runs as one GEMM kernel with three products per K slice.
+    const int kind = split3 ? kKindTF32x3
+                            : (tf32 ? kKindTF32 : (is_fp8(p.Atype) ? kKindF8 : kKindF16));
     const int bn = tile_n_for(h, p.m, p.n, p.k, p.batch, es_k, cg, kind);
     const SplitPlan plan = plan_for(h, p.m, p.n, p.k, p.batch, es_k, cg, bn);
     const TailPlan tail = tail_for(h, p.m, p.n, p.k, p.batch, es_k, cg, p.Ctype == TCG_R_32F,
-                                   plan, bn);
+                                   plan, bn, split3 ? 3.0 : 1.0);
     const int64_t n_tiles_total = tiles_of(p.m, p.n, p.batch, cg, bn);
     const int64_t tail_tiles = tail.splits > 1 ? n_tiles_total - tail.full_tiles : 0;
     const size_t tf32_bytes = tf32 ? (split3 ? 2 : 1) * tf32_ws_bytes(p.m, p.n, p.k, p.batch) : 0;
@@ -610,8 +612,10 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
             return st;
     }
 
-    // One launch of the GEMM kernel: D = alpha * opA * opB + beta * C.
-    auto gemm_launch = [&](const void *opA, const void *opB, float beta) -> tcgStatus_t {
+    // One launch of the GEMM kernel: D = alpha * opA * opB + beta * C (with opA2 and opB2,
+    // the low words of the two-word split: D = alpha * (opA2 opB + opA opB2 + opA opB) + ...).
+    auto gemm_launch = [&](const void *opA, const void *opB, float beta, const void *opA2,
+                           const void *opB2) -> tcgStatus_t {
         GemmArgs a;
         std::memset(&a, 0, sizeof a);
         a.m = m; a.n = n; a.k = k; a.batch = batch;
@@ -674,11 +678,22 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
             return s2;
         a.a_bcast = abc ? 1 : 0;
         a.b_bcast = bbc ? 1 : 0;
+        CUtensorMap tmA2, tmB2;
+        if (opA2) {
+            int mode_lo = 0;
+            s2 = operand_map(h, opA2, at, a_kmajor, p.m, p.k, lda, sA, p.batch, kBM, a.k_row,
+                             &abc, &mode_lo, &tmA2);
+            if (s2 == TCG_STATUS_SUCCESS)
+                s2 = operand_map(h, opB2, at, b_kmajor, p.n, p.k, ldb, sB, p.batch, bn / cg,
+                                 a.k_row, &bbc, &mode_lo, &tmB2);
+            if (s2 != TCG_STATUS_SUCCESS)
+                return s2;
+        }
         const int64_t want = static_cast<int64_t>(a.total_tiles) * cg;
         const int grid = static_cast<int>(want < h->max_ctas[cg] ? want : h->max_ctas[cg]);
         cudaError_t e = launch_gemm(tmA, tmB, tmD, tmW, a,
                                     splitk ? static_cast<int>(kOutF32) : ok, cg, bn, grid,
-                                    h->stream);
+                                    h->stream, opA2 ? &tmA2 : nullptr, opB2 ? &tmB2 : nullptr);
         h->launches += 1;
         if (e == cudaSuccess && tail_tiles) {
             int64_t blocks = tail_tiles * (kBN / 16);  // 16 columns of a tail tile per block
@@ -701,16 +716,10 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
         return e == cudaSuccess ? TCG_STATUS_SUCCESS : TCG_STATUS_EXECUTION_FAILED;
     };
 
-    if (!split3)
-        return gemm_launch(Aop, Bop, p.beta);
-    // Three products, the small ones first, accumulated into D in FP32 ("NVIDIA Tensor
-    // Core混合精度计算原理与应用解析", section 5.1); lo_A * lo_B (<= 2^-22 relative) is dropped.
-    st = gemm_launch(Alo, Bop, p.beta);
-    if (st == TCG_STATUS_SUCCESS)
-        st = gemm_launch(Aop, Blo, 1.0f);
-    if (st == TCG_STATUS_SUCCESS)
-        st = gemm_launch(Aop, Bop, 1.0f);
-    return st;
+    // The split: three products per K slice, the small ones first, accumulated in one FP32
+    // accumulator ("NVIDIA Tensor Core混合精度计算原理与应用解析", section 5.1);
+    // lo_A * lo_B (<= 2^-22 relative) is dropped.
+    return gemm_launch(Aop, Bop, p.beta, split3 ? Alo : nullptr, split3 ? Blo : nullptr);
 }
 
 
@@ -1358,7 +1367,9 @@ tcgStatus_t tcg_gemm_tile_plan(tcgHandle_t h, int64_t m, int64_t n, int64_t k,
     const int cg = h->cta_group;
     const bool tf32 = compute == TCG_COMPUTE_32F_FAST_TF32 || compute == TCG_COMPUTE_32F_3XTF32;
     const int es = tf32 ? 4 : elem_size(Atype);
-    const int kind = tf32 ? kKindTF32 : (is_fp8(Atype) ? kKindF8 : kKindF16);
+    const bool split3 = compute == TCG_COMPUTE_32F_3XTF32;
+    const int kind = split3 ? kKindTF32x3
+                            : (tf32 ? kKindTF32 : (is_fp8(Atype) ? kKindF8 : kKindF16));
     const int bn = k > 0 ? tile_n_for(h, m, n, k, batch_count, es, cg, kind) : kBN;
     *tile_m = kBM * cg;
     *tile_n = bn;
@@ -1374,7 +1385,8 @@ tcgStatus_t tcg_gemm_tile_plan(tcgHandle_t h, int64_t m, int64_t n, int64_t k,
     if (tiles == 0 || k == 0)
         return TCG_STATUS_SUCCESS;
     const SplitPlan sp = plan_for(h, m, n, k, batch_count, es, cg, bn);
-    const TailPlan tp = tail_for(h, m, n, k, batch_count, es, cg, Ctype == TCG_R_32F, sp, bn);
+    const TailPlan tp = tail_for(h, m, n, k, batch_count, es, cg, Ctype == TCG_R_32F, sp, bn,
+                                 split3 ? 3.0 : 1.0);
     // tiles in raster order -> (b, mt, nt); entry b * mt_count * nt_count + mt * nt_count + nt
     for (int64_t t = 0; t < tiles; ++t) {
         int b, mt, nt;

@@ -70,8 +70,9 @@ enum OutKind { kOutF32 = 0, kOutF16 = 1, kOutBF16 = 2 };
 
 // MMA kind (operand formats): kind::f16 (FP16/BF16, K = 16 per instruction),
 // kind::tf32 (K = 8), kind::f8f6f4 with E4M3/E5M2 (K = 32).  Every kind reads 32 bytes
-// of K per instruction.
-enum MmaKind { kKindF16 = 0, kKindTF32 = 1, kKindF8 = 2 };
+// of K per instruction.  kKindTF32x3 is kind::tf32 on two words per operand (x = hi +
+// lo): four operand tiles per stage and three products per K slice into one accumulator.
+enum MmaKind { kKindF16 = 0, kKindTF32 = 1, kKindF8 = 2, kKindTF32x3 = 3 };
 
 // How an operand tile sits in global and shared memory (128-byte swizzle throughout).
 //   kK:   K contiguous.  3-D map {K, rows, batch}, box {one 128-byte row of K, rows};
@@ -217,9 +218,12 @@ inline SplitPlan split_plan(int64_t tiles, int num_k_blocks, int clusters, int f
 // tmW maps the tail partial sums (tile_m x 256 x slices FP32), used only when
 // a.tail_splits > 1 (any valid map otherwise).
 // bn: the tile width (kBN, or kBNNarrow where gemm_has_narrow says a variant exists).
+// tmA2 / tmB2: the low words of A and B for kKindTF32x3 (tmA / tmB for the high words);
+// nullptr for the other kinds.
 cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmD,
                         const CUtensorMap &tmW, const GemmArgs &a, int out_kind, int cta_group,
-                        int bn, int grid, cudaStream_t s);
+                        int bn, int grid, cudaStream_t s, const CUtensorMap *tmA2 = nullptr,
+                        const CUtensorMap *tmB2 = nullptr);
 // Whether a narrow-tile (kBNNarrow) variant of the GEMM kernel exists for this launch.
 bool gemm_has_narrow(int cta_group, int kind);
 // D (FP32) of the split tail tiles from their partial sums W (see tcg_tail_reduce_kernel).

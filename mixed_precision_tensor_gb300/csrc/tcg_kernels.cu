@@ -179,19 +179,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     tcg_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmD,
-                    const __grid_constant__ CUtensorMap tmW, const GemmArgs p)
+                    const __grid_constant__ CUtensorMap tmW,
+                    const __grid_constant__ CUtensorMap tmA2,
+                    const __grid_constant__ CUtensorMap tmB2, const GemmArgs p)
 {
     using Cfg = TileCfg<CG, CBUF, BN>;
     constexpr int kAccBufs = Cfg::kAccBufs;
     constexpr bool BETA = CBUF != 0;                          // C is read
-    constexpr int kStages = Cfg::kStages;
+    // Two-word TF32 (kKindTF32x3): a stage carries A's and B's high words, then their
+    // low words (tmA2, tmB2); each K slice takes three products, lo_A hi_B, hi_A lo_B and
+    // hi_A hi_B, into the one accumulator.
+    constexpr bool kX3 = KIND == kKindTF32x3;
+    constexpr int kOps = kX3 ? 2 : 1;                         // words per operand
+    constexpr int kStages = Cfg::kRingBytes / (kOps * Cfg::kStageBytes);
+    static_assert(kStages >= 2, "ring too small");
     constexpr int kRingBytes = Cfg::kRingBytes;
     constexpr int kEpiBufs = Cfg::kEpiBufs;
     constexpr int kEpiBytes = Cfg::kEpiBytes;
     constexpr int kBRows = Cfg::kBRows;
     constexpr int kAStage = Cfg::kAStage;
     constexpr int kBStage = Cfg::kBStage;
-    constexpr int kStageBytes = Cfg::kStageBytes;
+    constexpr int kStageBytes = kOps * Cfg::kStageBytes;     // all words of A and B
     constexpr int kTileM = Cfg::kTileM;
 
     unsigned long long clk0 = 0, ns0 = 0;
@@ -206,6 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *base_ptr = smem_raw + (base - raw_u32);
     const uint32_t a_smem = base;
     const uint32_t b_smem = base + kStages * kAStage;
+    const uint32_t a2_smem = b_smem + kStages * kBStage;    // low words (kX3)
+    const uint32_t b2_smem = a2_smem + kStages * kAStage;
     const uint32_t epi_smem = base + kRingBytes;
     uint8_t *epi_ptr = base_ptr + kRingBytes;
     SmemCtl *ctl = reinterpret_cast<SmemCtl *>(base_ptr + kRingBytes + kEpiBytes);
@@ -235,6 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB);
         tma_prefetch_map(&tmD);
+        if constexpr (kX3) {
+            tma_prefetch_map(&tmA2);
+            tma_prefetch_map(&tmB2);
+        }
         if (p.tail_splits > 1)
             tma_prefetch_map(&tmW);
     }
@@ -259,7 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The MMA kind is a template argument and every per-slice descriptor offset is
     // computed before the loop: the issuing thread's loop must stay branch-free and
     // short, as its instruction rate is what keeps the tensor core fed.
-    constexpr uint32_t kEsize = KIND == kKindTF32 ? 4u : (KIND == kKindF8 ? 1u : 2u);
+    constexpr bool kTf32 = KIND == kKindTF32 || kX3;
+    constexpr uint32_t kEsize = kTf32 ? 4u : (KIND == kKindF8 ? 1u : 2u);
     constexpr uint32_t kKmma = 32u / kEsize;                  // K per MMA instruction
     constexpr int kMmasPerRow = kRowBytes / 32;               // 4 MMAs per 128-byte K row
     constexpr int kMmasPerStage = kMmasPerRow * kDepth;       // 4
@@ -291,6 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // start-address field (bits 0-13), which cannot overflow in 227 KB of shared memory.
     const uint64_t a_desc0 = smem_desc_sw128(a_smem, a_lbo, a_sbo);
     const uint64_t b_desc0 = smem_desc_sw128(b_smem, b_lbo, b_sbo);
+    const uint64_t a2_desc0 = smem_desc_sw128(a2_smem, a_lbo, a_sbo);
+    const uint64_t b2_desc0 = smem_desc_sw128(b2_smem, b_lbo, b_sbo);
     uint32_t issued_mask = 0, issued_parity = 0;              // leader producer: loads per stage
 
     if (warp == 0) {
@@ -355,6 +372,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                         };
                         load(sa, &tmA, p.a_mode, std::integral_constant<int, kBM>{}, m0, za);
                         load(sb, &tmB, p.b_mode, std::integral_constant<int, kBRows>{}, n0, zb);
+                        if constexpr (kX3) {
+                            load(a2_smem + stage * kAStage, &tmA2, p.a_mode,
+                                 std::integral_constant<int, kBM>{}, m0, za);
+                            load(b2_smem + stage * kBStage, &tmB2, p.b_mode,
+                                 std::integral_constant<int, kBRows>{}, n0, zb);
+                        }
                     }
                     if (++stage == kStages) {
                         stage = 0;
@@ -396,7 +419,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t ad = ad_s + a_off[kk];
                         const uint64_t bd = bd_s + b_off[kk];
                         const uint32_t accum = (kb > kb_begin || kk > 0) ? 1u : 0u;
-                        if constexpr (CG == 2) {
+                        if constexpr (kX3) {
+                            // the two small products first, then hi_A hi_B
+                            const uint64_t ad2 = a2_desc0 +
+                                ((static_cast<uint32_t>(stage) * kAStage) >> 4) + a_off[kk];
+                            const uint64_t bd2 = b2_desc0 +
+                                ((static_cast<uint32_t>(stage) * kBStage) >> 4) + b_off[kk];
+                            if constexpr (CG == 2) {
+                                mma_tf32_pair(d_tmem, ad2, bd, p.idesc, accum);
+                                mma_tf32_pair(d_tmem, ad, bd2, p.idesc, 1u);
+                                mma_tf32_pair(d_tmem, ad, bd, p.idesc, 1u);
+                            } else {
+                                mma_tf32(d_tmem, ad2, bd, p.idesc, accum);
+                                mma_tf32(d_tmem, ad, bd2, p.idesc, 1u);
+                                mma_tf32(d_tmem, ad, bd, p.idesc, 1u);
+                            }
+                        } else if constexpr (CG == 2) {
                             if constexpr (KIND == kKindTF32)
                                 mma_tf32_pair(d_tmem, ad, bd, p.idesc, accum);
                             else if constexpr (KIND == kKindF8)
@@ -796,13 +834,16 @@ __global__ void __launch_bounds__(256) tcg_tf32_pack_kernel(const uint32_t *__re
 }
 
 typedef void (*GemmKernelFn)(const CUtensorMap, const CUtensorMap, const CUtensorMap,
-                             const CUtensorMap, const GemmArgs);
+                             const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                             const GemmArgs);
 
 template <int CG, int CBUF>
 static GemmKernelFn gemm_fn_cg(int out_kind, int kind)
 {
     if (kind == kKindTF32)   // TF32 inputs always produce FP32 output
         return tcg_gemm_kernel<kOutF32, CG, kKindTF32, CBUF, kBN>;
+    if (kind == kKindTF32x3)
+        return tcg_gemm_kernel<kOutF32, CG, kKindTF32x3, CBUF, kBN>;
     if (kind == kKindF8) {
         switch (out_kind) {
         case kOutF32: return tcg_gemm_kernel<kOutF32, CG, kKindF8, CBUF, kBN>;
@@ -1022,8 +1063,11 @@ cudaError_t launch_tf32_transpose_round(const void *in, int64_t ld, int64_t stri
 
 cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmD,
                         const CUtensorMap &tmW, const GemmArgs &a, int out_kind, int cta_group,
-                        int bn, int grid, cudaStream_t s)
+                        int bn, int grid, cudaStream_t s, const CUtensorMap *tmA2,
+                        const CUtensorMap *tmB2)
 {
+    if ((a.kind == kKindTF32x3) != (tmA2 != nullptr && tmB2 != nullptr))
+        return cudaErrorInvalidValue;
     if (bn != kBN && !(bn == kBNNarrow && gemm_has_narrow(cta_group, a.kind)))
         return cudaErrorInvalidValue;
     GemmKernelFn fn = gemm_fn(out_kind, cta_group, a.kind, a.c_bufs, bn);
@@ -1042,7 +1086,7 @@ cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, fn, tmA, tmB, tmD, tmW, a);
+    e = cudaLaunchKernelEx(&cfg, fn, tmA, tmB, tmD, tmW, tmA2 ? *tmA2 : tmA, tmB2 ? *tmB2 : tmB, a);
     if (e != cudaSuccess)
         return e;
     return cudaGetLastError();
