@@ -359,10 +359,13 @@ def _device_tensors(w, dev):
 def time_steps(step, stream, steps, warmup, flush, world, sampler, counter=None,
                before=None):
     """W untimed warm-up steps, then exactly K timed steps on ``stream`` bracketed by a
-    barrier and a device synchronisation.  Per-step CUDA events on the launching stream
-    (with an L2 flush before each step when ``flush`` is given); the clock record covers
-    the timed region; ``counter`` (the library's launch counter) is read around it.
-    Returns (per-step kernel ms, region ms, clocks, launches in the timed region)."""
+    barrier and a device synchronisation.  With ``flush`` (inputs that fit in L2) each
+    step is an L2 flush then the call, timed by its own pair of CUDA events; without, the
+    K calls run back to back between one pair of events (events between them would stop a
+    call from starting while the previous one drains), and the per-step time is the
+    region's over K.  The clock record covers the timed region; ``counter`` (the library's
+    launch counter) is read around it.  Returns (per-step kernel ms, region ms, clocks,
+    launches in the timed region)."""
     import torch
     with torch.cuda.stream(stream):
         for _ in range(max(3, warmup)):
@@ -382,16 +385,19 @@ def time_steps(step, stream, steps, warmup, flush, world, sampler, counter=None,
         for i in range(steps):
             if flush is not None:
                 flush.zero_()
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
+                starts[i].record(stream)
+                step()
+                ends[i].record(stream)
+            else:
+                step()
         g1.record(stream)
     torch.cuda.synchronize()
     t1 = time.perf_counter()
     launches = (counter() - n0) if counter else 0
     barrier(world)
-    kernel_ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / steps
     region_ms = g0.elapsed_time(g1)
+    kernel_ms = (sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / steps
+                 if flush is not None else region_ms / steps)
     clocks = sampler.region(t0, t1) if sampler is not None else None
     return kernel_ms, region_ms, clocks, launches
 

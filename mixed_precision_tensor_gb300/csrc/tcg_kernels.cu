@@ -269,6 +269,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
+    // Chained calls: the set-up above (barriers, TMEM, tensor-map prefetch) may overlap the
+    // end of the previous kernel on the stream; nothing below touches global memory before
+    // that kernel has completed and its writes are visible.
+    if (threadIdx.x == 0)
+        griddep_launch_dependents();
+    griddep_wait();
 
     // The MMA kind is a template argument and every per-slice descriptor offset is
     // computed before the loop: the issuing thread's loop must stay branch-free and
@@ -1075,7 +1081,7 @@ cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
@@ -1084,8 +1090,12 @@ cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
     attr[0].val.clusterDim.x = cta_group;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // Programmatic dependent launch: the kernel may start while the previous kernel on the
+    // stream finishes (it waits in griddepcontrol.wait before any global access).
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, fn, tmA, tmB, tmD, tmW, tmA2 ? *tmA2 : tmA, tmB2 ? *tmB2 : tmB, a);
     if (e != cudaSuccess)
         return e;

@@ -277,6 +277,21 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
+// ------------------------------------------- programmatic dependent launch
+// Let the next kernel on the stream (launched with programmatic stream serialization)
+// start its CTAs as this grid's CTAs exit.
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the grids this one depends on have completed and their memory operations
+// are visible (returns at once when there are none).
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---------------------------------------------------------- clusters / pairs
 __device__ __forceinline__ uint32_t cluster_ctarank()
 {
