@@ -341,11 +341,12 @@ tcgStatus_t tcg_split_k_plan(int64_t tiles, int num_k_blocks, int clusters, int 
                              int *splits, int *kb_per_split);
 
 /* Tail split (FP32 output, no split-K, automatic mode only): when the output tiles fill
- * whole waves of the GPU's SM pairs plus a partial one, the tiles after
- * (tiles / clusters - 1) full waves are cut into 2..4 K ranges whose FP32 partial sums
+ * whole waves of the GPU's SM pairs plus a partial one, the tiles of the partial wave
+ * (or of it and the wave before) are cut into 2..4 K ranges whose FP32 partial sums
  * land in tile-sized workspace slices and are added in range order by a second kernel,
  * which then applies alpha and beta -- so the last wave takes a fraction of a tile's time.
- * Chosen when the tensor time it saves is over twice the partial sums' round trip.
+ * Chosen when half the tensor time it is predicted to save (partial waves run at higher
+ * clocks) exceeds the reduction's cost (a launch plus its memory traffic).
  * tcg_tail_split_plan is the rule, pure host arithmetic: tiles, K blocks (128 bytes of K
  * each), tile slots (clusters), one tile's time in microseconds, one tile's FP32 bytes
  * -> the number of whole tiles, the ranges (1: no tail split) and K blocks per range.

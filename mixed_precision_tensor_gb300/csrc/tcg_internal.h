@@ -134,12 +134,17 @@ __host__ __device__ inline void raster(const GemmArgs &p, int t, int &b, int &mt
 
 
 // Tail split (FP32 output only): when the tiles fill whole waves of the SM pairs plus a
-// partial last wave, the last tiles (all but (tiles / clusters - 1) waves of them) are cut
-// into `splits` K ranges whose partial sums go to tile-sized FP32 slices, and
-// launch_tail_reduce adds them in range order and applies alpha and beta.  Chosen when
-// the estimated time saved on the tensor cores exceeds twice the partial-sum round trip
-// (write, read: 2 x tail tiles x splits x tile bytes at ~5 TB/s) plus a launch (~5 us);
-// tile_us is the time of one whole tile.
+// partial last wave, the tiles of that partial wave (or of it and the wave before) are
+// cut into `splits` K ranges whose partial sums go to tile-sized FP32 slices, and
+// launch_tail_reduce adds them in range order and applies alpha and beta.  Each
+// candidate (rest = tiles % clusters or that plus one wave; 2, 3 or 4 ranges) predicts
+// full / clusters + ceil(rest * splits / clusters) / splits tile times against the
+// unsplit ceil(tiles / clusters); only half of the predicted saving is counted (a partial
+// wave runs on fewer SMs, which clock higher under the power cap: measured on 8192^3
+// and TF32 4096 x 4096 x 16384 GEMMs).  The cost is a reduction launch (3 us) reading
+// the partial sums and C and writing D (rest * (splits + 2) tiles of bytes at ~4 TB/s).
+// The plan with the largest net saving is taken if it is positive; tile_us is the time
+// of one whole tile.
 struct TailPlan {
     int64_t full_tiles;        // tiles [0, full_tiles) whole
     int splits;                // 1: no tail split
@@ -152,23 +157,28 @@ inline TailPlan tail_plan(int64_t tiles, int num_k_blocks, int clusters, double 
     if (clusters <= 0 || tiles <= clusters || tiles % clusters == 0)
         return pl;
     const int64_t waves = (tiles + clusters - 1) / clusters;
-    const int64_t full = (tiles / clusters - 1) * clusters;
-    const int64_t rest = tiles - full;
-    double best = static_cast<double>(waves);
-    for (int s = 2; s <= 4; ++s) {
-        if (num_k_blocks < 2 * s)
+    double best = 0.0;
+    for (int c = 0; c < 2; ++c) {
+        const int64_t rest = tiles % clusters + c * static_cast<int64_t>(clusters);
+        if (rest >= tiles)
             break;
-        const int64_t tail_waves = (rest * s + clusters - 1) / clusters;
-        const double t = static_cast<double>(full / clusters) + static_cast<double>(tail_waves) / s;
-        const double saved_us = (static_cast<double>(waves) - t) * tile_us;
-        const double cost_us = 5.0 + 2.0 * static_cast<double>(rest * s) * tile_bytes / 5.0e6;
-        if (t < best && saved_us > 2.0 * cost_us) {
-            best = t;
-            pl.splits = s;
+        const int64_t full = tiles - rest;
+        for (int s = 2; s <= 4; ++s) {
+            if (num_k_blocks < 2 * s)
+                break;
+            const int64_t tail_waves = (rest * s + clusters - 1) / clusters;
+            const double t = static_cast<double>(full / clusters) +
+                             static_cast<double>(tail_waves) / s;
+            const double saved_us = 0.5 * (static_cast<double>(waves) - t) * tile_us;
+            const double cost_us = 3.0 + static_cast<double>(rest * (s + 2)) * tile_bytes / 4.0e6;
+            if (saved_us - cost_us > best) {
+                best = saved_us - cost_us;
+                pl.full_tiles = full;
+                pl.splits = s;
+            }
         }
     }
     if (pl.splits > 1) {
-        pl.full_tiles = full;
         pl.kb_per_split = (num_k_blocks + pl.splits - 1) / pl.splits;
         pl.splits = (num_k_blocks + pl.kb_per_split - 1) / pl.kb_per_split;
     }

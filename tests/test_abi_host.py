@@ -209,10 +209,13 @@ def test_host_buffer_calls_check_arguments_without_a_gpu():
 
 
 def test_tail_split_plan_rule():
-    # 256 tiles of 146 us (the TF32 4096 x 4096 x 16384 shape) on 76 tile slots: two full
-    # waves, the last 104 tiles in two K halves (3.5 tile times instead of 4)
+    # 256 tiles of 146 us (the TF32 4096 x 4096 x 16384 shape) on 76 tile slots: three full
+    # waves, the 28 tiles of the partial wave in two K halves (3.5 tile times instead of
+    # 4); splitting the last 104 tiles saves as much but reduces four times the partials
     st, full, s, kb = tcg.tcg_tail_split_plan(256, 256, 76, 256 * 1024 / 1.8e3, 262144.0)
-    assert (st, full, s, kb) == (0, 152, 2, 128)
+    assert (st, full, s, kb) == (0, 228, 2, 128)
+    # three times the tensor work per tile (the two-word split): the same plan
+    assert tcg.tcg_tail_split_plan(256, 256, 76, 3 * 256 * 1024 / 1.8e3, 262144.0)[1:3] == (228, 2)
     # 1024 tiles of 36 us (8192^3 FP16): the half tile saved does not pay for the partial sums
     assert tcg.tcg_tail_split_plan(1024, 64, 76, 64 * 1024 / 1.8e3, 262144.0)[1:] == (1024, 1, 64)
     # whole waves, or fewer tiles than slots: nothing to split

@@ -418,7 +418,8 @@ def test_split_k(cuda_device, m, n, k, in_t, out_t, alpha, beta, batch, forced):
 # ------------------------------------------------------------ tail split
 TAIL_CASES = [
     # row-major m x n x k, in, out, alpha, beta: 77 output tiles of the column-major call
-    # (1792 x 2816) on 76 SM pairs, long K -> the tiles are all cut in two K ranges
+    # (1792 x 2816) on 76 SM pairs, long K -> the one tile of the partial second wave (the
+    # corner tile, last in raster order) is cut in four K ranges
     (2816, 1792, 20480, "f16", "f32", 1.0, 0.0),
     (2816, 1792, 20480, "bf16", "f32", 0.5, 1.0),
 ]
