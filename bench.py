@@ -252,7 +252,9 @@ def cpu_baseline(w, A, B, C, budget_s=12.0):
     dt, fl = time_oracle(w, A, B, C, blocks, nthreads)
     return {"value": fl / dt / 1e12, "unit": UNIT, "cores": nthreads, "kind": "oracle",
             "sample": f"{len(blocks)} seeded 128x128 output tiles of the {w.m}x{w.n}x{w.k} "
-                      f"GEMM, full k each ({fl:.3e} FLOP in {dt:.2f} s)"}
+                      f"GEMM, full k each ({fl:.3e} FLOP in {dt:.2f} s)",
+            # the whole workload at the sampled rate (extrapolated, not measured)
+            "extrapolated_full_s": w.flops / (fl / dt)}
 
 
 # ------------------------------------------------------------------ main arms
@@ -566,12 +568,15 @@ def run_ours(args, w):
                 continue
             wk = wl.WORKLOADS[name]
             rec, tensors = measure(wk)
-            del tensors
             rec["config"] = {"m": wk.m, "n": wk.n, "k": wk.k, "batch": wk.batch,
                              "in": wk.in_type, "out": wk.out_type, "alpha": wk.alpha,
                              "beta": wk.beta, "seed": wk.seed,
                              "compute": wk.compute or "default"}
+            if rank == 0 and world == 1 and not args.no_cpu_baseline:
+                # the oracle on a small sample of this workload (~1.5 s of host time)
+                rec["cpu_baseline"] = cpu_baseline(wk, *tensors[3][:3], budget_s=1.5)
             side[name] = rec
+            del tensors
             torch.cuda.empty_cache()
         line["workloads"] = side
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
