@@ -252,7 +252,8 @@ def cpu_baseline(w, A, B, C, budget_s=12.0):
     dt, fl = time_oracle(w, A, B, C, blocks, nthreads)
     return {"value": fl / dt / 1e12, "unit": UNIT, "cores": nthreads, "kind": "oracle",
             "sample": f"{len(blocks)} seeded 128x128 output tiles of the {w.m}x{w.n}x{w.k} "
-                      f"GEMM, full k each ({fl:.3e} FLOP in {dt:.2f} s)",
+                      f"GEMM{' (batch entry 0 of %d)' % w.batch if w.batch > 1 else ''}, "
+                      f"full k each ({fl:.3e} FLOP in {dt:.2f} s)",
             # the whole workload at the sampled rate (extrapolated, not measured)
             "extrapolated_full_s": w.flops / (fl / dt)}
 
