@@ -450,6 +450,9 @@ def _device_inputs(w, A, B, C):
     dB = _t(B if w.batch > 1 else B[0]).to(dev)
     if w.in_type == "bf16":
         dA, dB = dA.view(torch.bfloat16), dB.view(torch.bfloat16)
+    if w.in_type in ("e4m3", "e5m2"):
+        f8 = torch.float8_e4m3fn if w.in_type == "e4m3" else torch.float8_e5m2
+        dA, dB = dA.view(f8), dB.view(f8)
     shape = (w.batch, w.m, w.n) if w.batch > 1 else (w.m, w.n)
     odt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.out_type]
     if C is not None:
@@ -718,3 +721,46 @@ def test_tf32_input_rounding_is_nearest_even(handle, transa, transb):
         assert values_equal(got, want), f"operand {side}: not RNE-rounded"
         # the data does tell nearest-even from a plain cut
         assert not values_equal(cut if side == "A" else cut.T, want)
+
+
+# ------------------------------------------------------------ extreme shapes
+EXTREME = [
+    # row-major m x n x k, batch, in, out (every leading dimension a multiple of 16 bytes):
+    # 100,000 tiny products (work units past 65535, ragged 8 x 8 tiles), one row of dot
+    # products of length 2^20 (one tile, K split in 64 ranges) and of 2^18 in TF32, a tall
+    # and skinny product (2^20 rows, 8 columns: 4096 tiles with ragged N), and a wide one
+    # (one row, 2^20 columns, FP8)
+    (8, 8, 8, 100_000, "f16", "f32"),
+    (1, 8, 1 << 20, 1, "bf16", "f32"),
+    (1 << 20, 8, 16, 1, "f16", "f16"),
+    (1, 1 << 20, 16, 1, "e4m3", "f32"),
+    (1, 8, 1 << 18, 1, "f32", "f32"),
+]
+
+
+@pytest.mark.timeout(900)
+@pytest.mark.parametrize("m,n,k,batch,in_t,out_t", EXTREME)
+def test_extreme_shapes_integer_exact(handle, m, n, k, batch, in_t, out_t):
+    """Shapes at the edges of the tile scheduler and the split plans, on integer inputs whose
+    sums are exact: the whole result equals numpy's int64 product (a library routine),
+    and sampled entries equal the exact oracle's."""
+    rng = np.random.default_rng(m * 7 + n * 3 + k + batch)
+    lo, hi = (-2, 3) if k <= 1 << 12 else (-1, 2)       # |sum| stays below 2^24 (and 2^11 for FP16 out)
+    A = rng.integers(lo, hi, (batch, m, k)).astype(np.float64)
+    B = rng.integers(lo, hi, (batch, k, n)).astype(np.float64)
+    want = np.einsum("bik,bkj->bij", A.astype(np.int64), B.astype(np.int64))
+    w = wl.custom(m, n, k, in_t, out_t, 1.0, 0.0, batch)
+    As = _to_storage(A.reshape(-1), in_t).reshape(batch, m, k)
+    Bs = _to_storage(B.reshape(-1), in_t).reshape(batch, k, n)
+    if in_t == "f16":
+        As, Bs = As.view(np.float16), Bs.view(np.float16)
+    out = _run_workload(handle, w, As, Bs, None)
+    got = decode_out(raw(np.ascontiguousarray(out)), out_t).reshape(batch, m, n)
+    assert np.array_equal(got, want.astype(np.float64)), "not the exact integer product"
+    # the exact oracle on a few entries (first and last batch entry, corner blocks)
+    for b in sorted({0, batch - 1}):
+        rows = (0, min(m, 64)) if m <= 128 else (m - 64, m)
+        cols = (0, min(n, 64))
+        D, _, _ = oracle_rowmajor(w, As, Bs, None, b=b, rows=rows, cols=cols)
+        ref = decode_out(raw(D), out_t)
+        assert values_equal(got[b, rows[0]:rows[1], cols[0]:cols[1]], ref)
