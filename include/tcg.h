@@ -49,7 +49,10 @@
  * pinned (cudaHostAlloc), managed or another device's memory is INVALID_VALUE with
  * nothing launched.  Host memory goes through the _host entry points.  All calls
  * are asynchronous on the handle's stream and return without a device
- * synchronisation (except tcg_get_device_error).  A handle is not thread-safe: use
+ * synchronisation (except tcg_get_device_error).  The GEMM kernel is launched with
+ * programmatic stream serialization: it may be resident before the previous kernel
+ * on the stream has finished, but it reads and writes no global memory until that
+ * kernel has completed, so stream order is kept.  A handle is not thread-safe: use
  * one per host thread.  C must not overlap A or
  * B.  The first GEMM call on a handle binds it to the current device and
  * allocates a 4-byte device error word; make that call before any stream
