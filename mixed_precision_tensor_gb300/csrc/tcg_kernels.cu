@@ -719,6 +719,7 @@ __global__ void __launch_bounds__(256) tcg_splitk_reduce_kernel(const float *__r
                                                                 float beta, void *D, int64_t ldc,
                                                                 int64_t strideC)
 {
+    griddep_wait();
     const int64_t slice = ldw * n;
     const int64_t cols = static_cast<int64_t>(batch) * n;
     for (int64_t bj = blockIdx.x; bj < cols; bj += gridDim.x) {
@@ -736,6 +737,7 @@ __global__ void __launch_bounds__(256) tcg_splitk_reduce_kernel(const float *__r
             store_out<OUT>(D, dcol + i, v);
         }
     }
+    griddep_launch_dependents();
 }
 
 // Tail reduction (FP32 output only): for each split tail tile r (tiles full_units + r),
@@ -749,6 +751,7 @@ __global__ void __launch_bounds__(256) tcg_tail_reduce_kernel(const float *__res
                                                               int tail_tiles, int tile_m,
                                                               const GemmArgs p)
 {
+    griddep_wait();
     constexpr int kGroups = kBN / kTailCols;
     const int64_t per_tile = static_cast<int64_t>(tile_m) * kBN;
     const int S = p.tail_splits;
@@ -784,6 +787,7 @@ __global__ void __launch_bounds__(256) tcg_tail_reduce_kernel(const float *__res
             }
         }
     }
+    griddep_launch_dependents();
 }
 
 // FP32 -> TF32, round to nearest, ties to even, kept in FP32 bits (low 13 bits zero).
@@ -957,6 +961,7 @@ __global__ void __launch_bounds__(256) tcg_tf32_round_kernel(const uint4 *__rest
                                                              int64_t ld_out4, int64_t stride_out4,
                                                              uint4 *__restrict__ out_lo)
 {
+    griddep_wait();
     for (int b = blockIdx.z; b < batch; b += gridDim.z)
         for (int c = blockIdx.y; c < cols; c += gridDim.y) {
             const uint4 *src = in + b * stride_in4 + static_cast<int64_t>(c) * ld4;
@@ -980,62 +985,92 @@ __global__ void __launch_bounds__(256) tcg_tf32_round_kernel(const uint4 *__rest
                 out[o + r] = v;
             }
         }
+    griddep_launch_dependents();
 }
 
 // M/N-major operand: element (r, p) (r < rows along M or N, p < k along K) at
 // in[b*stride_in + r + p*ld]; writes the K-major copy out[b*stride_out + p + r*ld_out],
-// rounded.  64 x 64 tiles through shared memory: every warp reads and writes whole
-// 128-byte runs; the 65-word row pitch keeps the transposed reads free of bank conflicts.
+// rounded, for p < round_up(k, 4) (zeros past k).  64 x 64 tiles through shared memory
+// with 16-byte global accesses on both sides: 16 threads read one K row's 64 elements
+// (four per thread) and 16 threads write one output row's 64; the 65-word row pitch
+// keeps both shared-memory phases at two-way bank conflicts at most.  ld, ld_out and the
+// strides are multiples of 4 elements and the pointers 16-byte aligned, so the four
+// elements read past `rows` stay inside the column's storage (ld >= round_up(rows, 4)).
 __global__ void __launch_bounds__(256) tcg_tf32_transpose_round_kernel(
     const uint32_t *__restrict__ in, int64_t ld, int64_t stride_in, int rows, int k, int batch,
     uint32_t *__restrict__ out, int64_t ld_out, int64_t stride_out, uint32_t *__restrict__ out_lo)
 {
-    __shared__ uint32_t tile[64][65];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __shared__ uint32_t tile[64][65];                 // [p][r]
+    griddep_wait();
+    const int c = threadIdx.x & 15, w = threadIdx.x >> 4;
     const int r_tiles = (rows + 63) / 64, p_tiles = (k + 63) / 64;
     for (int b = blockIdx.z; b < batch; b += gridDim.z)
         for (int pt = blockIdx.y; pt < p_tiles; pt += gridDim.y)
             for (int rt = blockIdx.x; rt < r_tiles; rt += gridDim.x) {
                 const int r0 = rt * 64, p0 = pt * 64;
                 const uint32_t *src = in + b * stride_in;
-                uint32_t *dst = out + b * stride_out;
                 __syncthreads();
-                for (int i = warp; i < 64; i += 8) {          // row p0 + i of the tile
-                    const int pp = p0 + i;
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int r = r0 + lane + 32 * h;
-                        tile[i][lane + 32 * h] =
-                            (pp < k && r < rows) ? src[r + static_cast<int64_t>(pp) * ld] : 0u;
-                    }
+                for (int j = 0; j < 4; ++j) {               // K rows p0 + w + 16 j
+                    const int pl = w + 16 * j, pp = p0 + pl, r = r0 + 4 * c;
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    if (pp < k && r < rows)
+                        v = *reinterpret_cast<const uint4 *>(src + r +
+                                                             static_cast<int64_t>(pp) * ld);
+                    tile[pl][4 * c] = v.x;
+                    tile[pl][4 * c + 1] = v.y;
+                    tile[pl][4 * c + 2] = v.z;
+                    tile[pl][4 * c + 3] = v.w;
                 }
                 __syncthreads();
-                for (int i = warp; i < 64; i += 8) {          // output row r0 + i
-                    const int r = r0 + i;
-                    if (r >= rows)
-                        continue;
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int pp = p0 + lane + 32 * h;
-                        if (pp < k) {
-                            const int64_t o = pp + static_cast<int64_t>(r) * ld_out;
-                            if (out_lo) {
-                                uint32_t hi, lo;
-                                tf32_split_bits(tile[lane + 32 * h][i], hi, lo);
-                                dst[o] = hi;
-                                out_lo[b * stride_out + o] = lo;
-                            } else {
-                                dst[o] = tf32_rne_bits(tile[lane + 32 * h][i]);
-                            }
-                        }
+                for (int j = 0; j < 4; ++j) {               // output rows r0 + w + 16 j
+                    const int rl = w + 16 * j, r = r0 + rl, pp = p0 + 4 * c;
+                    if (r >= rows || pp >= k)
+                        continue;
+                    const uint32_t x[4] = {tile[4 * c][rl], tile[4 * c + 1][rl],
+                                           tile[4 * c + 2][rl], tile[4 * c + 3][rl]};
+                    const int64_t o = b * stride_out + pp + static_cast<int64_t>(r) * ld_out;
+                    uint4 hi, lo;
+                    if (out_lo) {
+                        tf32_split_bits(x[0], hi.x, lo.x);
+                        tf32_split_bits(x[1], hi.y, lo.y);
+                        tf32_split_bits(x[2], hi.z, lo.z);
+                        tf32_split_bits(x[3], hi.w, lo.w);
+                        *reinterpret_cast<uint4 *>(out_lo + o) = lo;
+                    } else {
+                        hi = make_uint4(tf32_rne_bits(x[0]), tf32_rne_bits(x[1]),
+                                        tf32_rne_bits(x[2]), tf32_rne_bits(x[3]));
                     }
+                    *reinterpret_cast<uint4 *>(out + o) = hi;
                 }
             }
+    griddep_launch_dependents();
 }
 
 static inline unsigned clamp_grid(int64_t v, int64_t cap)
 {
     return static_cast<unsigned>(v < 1 ? 1 : (v > cap ? cap : v));
+}
+
+// Launch with programmatic stream serialization (the kernel waits in griddepcontrol.wait
+// before it reads anything and lets its own dependents launch at its end), so a chain
+// of the library's kernels on one stream hides each launch behind the previous kernel.
+template <typename... Params, typename... Args>
+static cudaError_t launch_chained(void (*kernel)(Params...), dim3 grid, dim3 block,
+                                  cudaStream_t s, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_tf32_round(const void *in, int64_t ld, int64_t stride_in, int64_t rows,
@@ -1045,12 +1080,11 @@ cudaError_t launch_tf32_round(const void *in, int64_t ld, int64_t stride_in, int
     const int64_t rows4 = (rows + 3) / 4;
     const dim3 g(clamp_grid((rows4 + 255) / 256, 1 << 16), clamp_grid(cols, 65535),
                  clamp_grid(batch, 65535));
-    tcg_tf32_round_kernel<<<g, 256, 0, s>>>(static_cast<const uint4 *>(in), ld / 4,
-                                            stride_in / 4, static_cast<int>(rows4),
-                                            static_cast<int>(cols), static_cast<int>(batch),
-                                            static_cast<uint4 *>(out), ld_out / 4,
-                                            stride_out / 4, static_cast<uint4 *>(out_lo));
-    return cudaGetLastError();
+    return launch_chained(tcg_tf32_round_kernel, g, dim3(256), s,
+                          static_cast<const uint4 *>(in), ld / 4, stride_in / 4,
+                          static_cast<int>(rows4), static_cast<int>(cols),
+                          static_cast<int>(batch), static_cast<uint4 *>(out), ld_out / 4,
+                          stride_out / 4, static_cast<uint4 *>(out_lo));
 }
 
 cudaError_t launch_tf32_transpose_round(const void *in, int64_t ld, int64_t stride_in,
@@ -1060,11 +1094,11 @@ cudaError_t launch_tf32_transpose_round(const void *in, int64_t ld, int64_t stri
 {
     const dim3 g(clamp_grid((rows + 63) / 64, (int64_t(1) << 31) - 1),
                  clamp_grid((k + 63) / 64, 65535), clamp_grid(batch, 65535));
-    tcg_tf32_transpose_round_kernel<<<g, 256, 0, s>>>(
-        static_cast<const uint32_t *>(in), ld, stride_in, static_cast<int>(rows),
-        static_cast<int>(k), static_cast<int>(batch), static_cast<uint32_t *>(out), ld_out,
-        stride_out, static_cast<uint32_t *>(out_lo));
-    return cudaGetLastError();
+    return launch_chained(tcg_tf32_transpose_round_kernel, g, dim3(256), s,
+                          static_cast<const uint32_t *>(in), ld, stride_in,
+                          static_cast<int>(rows), static_cast<int>(k), static_cast<int>(batch),
+                          static_cast<uint32_t *>(out), ld_out, stride_out,
+                          static_cast<uint32_t *>(out_lo));
 }
 
 cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CUtensorMap &tmD,
@@ -1117,28 +1151,18 @@ cudaError_t launch_splitk_reduce(const float *W, int64_t ldw, int splits, int m,
                                  float alpha, float beta, void *D, int64_t ldc, int64_t strideC,
                                  int out_kind, int grid, cudaStream_t s)
 {
-    switch (out_kind) {
-    case kOutF32:
-        tcg_splitk_reduce_kernel<kOutF32><<<grid, 256, 0, s>>>(W, ldw, splits, m, n, batch, alpha,
-                                                               beta, D, ldc, strideC);
-        break;
-    case kOutF16:
-        tcg_splitk_reduce_kernel<kOutF16><<<grid, 256, 0, s>>>(W, ldw, splits, m, n, batch, alpha,
-                                                               beta, D, ldc, strideC);
-        break;
-    default:
-        tcg_splitk_reduce_kernel<kOutBF16><<<grid, 256, 0, s>>>(W, ldw, splits, m, n, batch, alpha,
-                                                                beta, D, ldc, strideC);
-        break;
-    }
-    return cudaGetLastError();
+    auto fn = out_kind == kOutF32 ? tcg_splitk_reduce_kernel<kOutF32>
+            : (out_kind == kOutF16 ? tcg_splitk_reduce_kernel<kOutF16>
+                                   : tcg_splitk_reduce_kernel<kOutBF16>);
+    return launch_chained(fn, dim3(grid), dim3(256), s, W, ldw, splits, m, n, batch, alpha,
+                          beta, D, ldc, strideC);
 }
 
 cudaError_t launch_tail_reduce(const float *W, int tail_tiles, int tile_m, const GemmArgs &a,
                                int grid, cudaStream_t s)
 {
-    tcg_tail_reduce_kernel<<<grid, 256, 0, s>>>(W, tail_tiles, tile_m, a);
-    return cudaGetLastError();
+    return launch_chained(tcg_tail_reduce_kernel, dim3(grid), dim3(256), s, W, tail_tiles,
+                          tile_m, a);
 }
 
 cudaError_t launch_tf32_pack(const void *in, int64_t ld, int64_t stride_in, int in_kmajor,
