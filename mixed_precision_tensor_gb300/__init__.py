@@ -42,7 +42,8 @@ EXPORTS = ("tcg_create", "tcg_destroy", "tcg_set_stream", "tcg_set_workspace",
            "tcg_gemm_tf32_noalloc", "tcg_noalloc_device_error", "tcg_set_clock_probe",
            "tcg_read_clock_probe", "tcg_set_split_k", "tcg_split_k_plan",
            "tcg_gemm_split_k", "tcg_gemm_ex_host", "tcg_gemm_strided_batched_host",
-           "tcg_tail_split_plan", "tcg_gemm_tile_plan", "tcg_set_tile_n")
+           "tcg_tail_split_plan", "tcg_gemm_tile_plan", "tcg_set_tile_n",
+           "tcg_set_tf32_rounding")
 
 _lock = threading.Lock()
 _lib = None
@@ -113,6 +114,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.tcg_set_split_k.argtypes = [vp, ci]
         lib.tcg_set_tile_n.restype = st
         lib.tcg_set_tile_n.argtypes = [vp, ci]
+        lib.tcg_set_tf32_rounding.restype = st
+        lib.tcg_set_tf32_rounding.argtypes = [vp, ci]
         lib.tcg_split_k_plan.restype = st
         lib.tcg_split_k_plan.argtypes = [i64, ci, ci, ci, ctypes.POINTER(ci), ctypes.POINTER(ci)]
         lib.tcg_gemm_split_k.restype = st
@@ -234,6 +237,10 @@ def tcg_set_split_k(h: int, splits: int = 0) -> int:
 
 def tcg_set_tile_n(h: int, tile_n: int = 0) -> int:
     return load_library().tcg_set_tile_n(h, tile_n)
+
+
+def tcg_set_tf32_rounding(h: int, mode: int = 0) -> int:
+    return load_library().tcg_set_tf32_rounding(h, mode)
 
 
 def tcg_split_k_plan(tiles: int, num_k_blocks: int, clusters: int, forced: int = 0):

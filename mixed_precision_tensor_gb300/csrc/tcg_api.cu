@@ -73,6 +73,7 @@ struct tcgContext {
     int group_m = 0;           // 0: choose per problem
     int split_k = 0;           // 0: choose per problem, 1: never split, >= 2: that many ranges
     int tile_n = 0;            // 0: choose per problem, or kBN / kBNNarrow
+    int tf32_round = 0;        // TF32 rounding: 0 choose, 1 pre-pass kernels, 2 in the GEMM
     // Host-buffer calls: device copies of A, B, C (grown on demand) and two copy streams.
     void *stage_buf[3] = {nullptr, nullptr, nullptr};
     size_t stage_bytes[3] = {0, 0, 0};
@@ -403,6 +404,31 @@ size_t tf32_ws_bytes(int64_t m, int64_t n, int64_t k, int64_t batch)
     return a + b;
 }
 
+// In-kernel TF32 rounding (kKindTF32R): the rounded copies are cut into items of
+// kCvChunk K elements by one panel of tile rows (see GemmArgs::cv_*), with three
+// counters per item and panel in the workspace after the copies.
+constexpr int kCvChunk = 512;
+constexpr int64_t kMaxCvItems = int64_t(1) << 20;
+struct CvPlan {
+    int64_t items, panels;
+    int panels_a, panels_b, chunks;
+};
+CvPlan cv_plan(int64_t m, int64_t n, int64_t k, int64_t nba, int64_t nbb, int rows_a, int rows_b)
+{
+    CvPlan c;
+    const int64_t kp = (k + 3) / 4 * 4;
+    c.chunks = static_cast<int>((kp + kCvChunk - 1) / kCvChunk);
+    c.panels_a = static_cast<int>((m + rows_a - 1) / rows_a);
+    c.panels_b = static_cast<int>((n + rows_b - 1) / rows_b);
+    c.panels = nba * c.panels_a + nbb * c.panels_b;
+    c.items = c.panels * c.chunks;
+    return c;
+}
+size_t cv_ws_bytes(const CvPlan &c)
+{
+    return ((size_t)(2 * c.items + c.panels) * 4 + 255) / 256 * 256;
+}
+
 // Partial-sum workspace of a split-K call: batch * splits slices of round_up(m, 4) x n
 // FP32 values.
 size_t splitk_ws_bytes(int64_t m, int64_t n, int64_t batch, int splits)
@@ -540,12 +566,25 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
                                                 : (tail_tiles ? (size_t)(tail_tiles * tail.splits) *
                                                                     (size_t)(kBM * cg * kBN) * 4
                                                               : 0);
+    // TF32 rounding inside the GEMM kernel, or by the pre-pass kernels before it.
+    const int64_t nba0 = (p.batched ? p.strideA : 0) == 0 ? 1 : p.batch;
+    const int64_t nbb0 = (p.batched ? p.strideB : 0) == 0 ? 1 : p.batch;
+    const CvPlan cvp = cv_plan(p.m, p.n, p.k, nba0, nbb0, kBM * cg, bn);
+    // Rounding inside the GEMM kernel only when asked for (mode 2): on GB300 it loses to
+    // the pre-pass (4096 x 4096 x 16384: 808 against 697 us per call), because the tensor
+    // core fed at full rate leaves the SM's shared-memory/L1 data path almost no room for
+    // the rounding's loads and stores.
+    const bool fuse = tf32 && !split3 && h->tf32_round == 2 && cvp.items <= kMaxCvItems;
+    const size_t cv_bytes = fuse ? cv_ws_bytes(cvp) : 0;
     void *ws = nullptr;
-    if (tf32_bytes + splitk_bytes > 0) {
-        st = acquire_ws(h, tf32_bytes + splitk_bytes, &ws);
+    if (tf32_bytes + splitk_bytes + cv_bytes > 0) {
+        st = acquire_ws(h, tf32_bytes + splitk_bytes + cv_bytes, &ws);
         if (st != TCG_STATUS_SUCCESS)
             return st;
     }
+    uint32_t *cv_cnt = fuse ? reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) + tf32_bytes +
+                                                           splitk_bytes)
+                            : nullptr;
     float *W = splitk_bytes ? reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + tf32_bytes)
                             : nullptr;
     const int64_t ldw = (p.m + 3) / 4 * 4;
@@ -569,17 +608,23 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
         uint8_t *Bkl = split3 ? Bk + one : nullptr;
         // a batch stride of 0 (one operand shared by all batches) stays shared
         const int64_t nba = sA == 0 ? 1 : p.batch, nbb = sB == 0 ? 1 : p.batch;
-        cudaError_t e = a_kmajor
-            ? launch_tf32_round(p.A, p.lda, sA, p.k, p.m, nba, Ak, kp, p.m * kp, Akl, h->stream)
-            : launch_tf32_transpose_round(p.A, p.lda, sA, p.m, p.k, nba, Ak, kp, p.m * kp, Akl,
-                                          h->stream);
-        if (e == cudaSuccess)
-            e = b_kmajor
-                ? launch_tf32_round(p.B, p.ldb, sB, p.k, p.n, nbb, Bk, kp, p.n * kp, Bkl,
-                                    h->stream)
-                : launch_tf32_transpose_round(p.B, p.ldb, sB, p.n, p.k, nbb, Bk, kp, p.n * kp,
-                                              Bkl, h->stream);
-        h->launches += 2;
+        cudaError_t e;
+        if (fuse) {
+            // the GEMM kernel rounds the operands itself: only its counters start at zero
+            e = cudaMemsetAsync(cv_cnt, 0, cv_bytes, h->stream);
+        } else {
+            e = a_kmajor
+                ? launch_tf32_round(p.A, p.lda, sA, p.k, p.m, nba, Ak, kp, p.m * kp, Akl, h->stream)
+                : launch_tf32_transpose_round(p.A, p.lda, sA, p.m, p.k, nba, Ak, kp, p.m * kp, Akl,
+                                              h->stream);
+            if (e == cudaSuccess)
+                e = b_kmajor
+                    ? launch_tf32_round(p.B, p.ldb, sB, p.k, p.n, nbb, Bk, kp, p.n * kp, Bkl,
+                                        h->stream)
+                    : launch_tf32_transpose_round(p.B, p.ldb, sB, p.n, p.k, nbb, Bk, kp, p.n * kp,
+                                                  Bkl, h->stream);
+            h->launches += 2;
+        }
         if (e != cudaSuccess)
             return TCG_STATUS_EXECUTION_FAILED;
         Aop = Ak;
@@ -638,7 +683,41 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
             a.tail_kb_per_split = a.num_k_blocks;
         }
         a.group_m = h->group_m > 0 ? h->group_m : 8;
-        a.kind = kind;
+        a.kind = fuse ? kKindTF32R : kind;
+        if (fuse) {
+            const int64_t kp = (p.k + 3) / 4 * 4;
+            const bool src_kmajor[2] = {p.transa == TCG_OP_T, p.transb == TCG_OP_N};
+            const void *src[2] = {p.A, p.B};
+            const int64_t ld_src[2] = {p.lda, p.ldb};
+            const int64_t s_src[2] = {p.batched ? p.strideA : 0, p.batched ? p.strideB : 0};
+            void *dst[2] = {const_cast<void *>(Aop), const_cast<void *>(Bop)};
+            const int rows[2] = {m, n};
+            const int prow[2] = {kBM * cg, bn};
+            const int panels[2] = {cvp.panels_a, cvp.panels_b};
+            const int64_t nb[2] = {nba0, nbb0};
+            for (int x = 0; x < 2; ++x) {
+                a.cv_src[x] = src[x];
+                a.cv_dst[x] = dst[x];
+                a.cv_ld[x] = ld_src[x];
+                a.cv_stride[x] = s_src[x];
+                a.cv_dstride[x] = s_src[x] == 0 ? 0 : rows[x] * kp;
+                a.cv_kmajor[x] = src_kmajor[x] ? 1 : 0;
+                a.cv_rows[x] = rows[x];
+                a.cv_panel_rows[x] = prow[x];
+                a.cv_panels[x] = panels[x];
+                a.cv_subs[x] = (prow[x] / kCvRows) * (kCvChunk / kCvK);
+            }
+            a.cv_base[0] = 0;
+            a.cv_base[1] = static_cast<int>(nb[0] * panels[0] * cvp.chunks);
+            a.cv_pbase[0] = 0;
+            a.cv_pbase[1] = static_cast<int>(nb[0] * panels[0]);
+            a.cv_kp = kp;
+            a.cv_kc = kCvChunk;
+            a.cv_chunks = cvp.chunks;
+            a.cv_kb_per_chunk = kCvChunk / (kDepth * (128 / 4));
+            a.cv_items = static_cast<int>(cvp.items);
+            a.cv_cnt = cv_cnt;
+        }
         // operand format codes: kind::f16 F16 = 0, BF16 = 1; kind::tf32 TF32 = 2;
         // kind::f8f6f4 E4M3 = 0, E5M2 = 1
         const uint32_t fmt = tf32 ? 2u
@@ -1127,8 +1206,9 @@ tcgStatus_t tcg_gemm_workspace_size(tcgOp_t transa, tcgOp_t transb, int64_t m, i
         return TCG_STATUS_INVALID_VALUE;
     *bytes = 0;
     if (Atype == TCG_R_32F && k > 0) {
-        if (compute == TCG_COMPUTE_32F_FAST_TF32)
-            *bytes = tf32_ws_bytes(m, n, k, batch_count);
+        if (compute == TCG_COMPUTE_32F_FAST_TF32)   // copies + in-kernel rounding counters
+            *bytes = tf32_ws_bytes(m, n, k, batch_count) +
+                     cv_ws_bytes(cv_plan(m, n, k, batch_count, batch_count, kBM, kBNNarrow));
         else if (compute == TCG_COMPUTE_32F_3XTF32)
             *bytes = 2 * tf32_ws_bytes(m, n, k, batch_count);
     }
@@ -1325,6 +1405,14 @@ tcgStatus_t tcg_set_tile_n(tcgHandle_t h, int tile_n)
     if (!h || (tile_n != 0 && tile_n != kBN && tile_n != kBNNarrow))
         return TCG_STATUS_INVALID_VALUE;
     h->tile_n = tile_n;
+    return TCG_STATUS_SUCCESS;
+}
+
+tcgStatus_t tcg_set_tf32_rounding(tcgHandle_t h, int mode)
+{
+    if (!h || mode < 0 || mode > 2)
+        return TCG_STATUS_INVALID_VALUE;
+    h->tf32_round = mode;
     return TCG_STATUS_SUCCESS;
 }
 

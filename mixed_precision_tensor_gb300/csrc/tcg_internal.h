@@ -65,6 +65,7 @@ constexpr uint32_t kErrMmaFull = 2u;     // MMA waiting for operands
 constexpr uint32_t kErrMmaAcc = 4u;      // MMA waiting for a free accumulator
 constexpr uint32_t kErrEpilogue = 8u;    // epilogue waiting for a finished accumulator
 constexpr uint32_t kErrDrain = 16u;      // end-of-kernel drain
+constexpr uint32_t kErrConvert = 32u;    // producer waiting for in-kernel TF32 rounding
 
 enum OutKind { kOutF32 = 0, kOutF16 = 1, kOutBF16 = 2 };
 
@@ -72,7 +73,9 @@ enum OutKind { kOutF32 = 0, kOutF16 = 1, kOutBF16 = 2 };
 // kind::tf32 (K = 8), kind::f8f6f4 with E4M3/E5M2 (K = 32).  Every kind reads 32 bytes
 // of K per instruction.  kKindTF32x3 is kind::tf32 on two words per operand (x = hi +
 // lo): four operand tiles per stage and three products per K slice into one accumulator.
-enum MmaKind { kKindF16 = 0, kKindTF32 = 1, kKindF8 = 2, kKindTF32x3 = 3 };
+// kKindTF32R is kind::tf32 with the TF32 rounding done inside the GEMM kernel (see the
+// cv_* arguments) instead of by the separate pre-pass kernels.
+enum MmaKind { kKindF16 = 0, kKindTF32 = 1, kKindF8 = 2, kKindTF32x3 = 3, kKindTF32R = 4 };
 
 // How an operand tile sits in global and shared memory (128-byte swizzle throughout).
 //   kK:   K contiguous.  3-D map {K, rows, batch}, box {one 128-byte row of K, rows};
@@ -115,7 +118,35 @@ struct GemmArgs {
     // (globaltimer) it ran for to clk[0] and clk[1], so clk[0] / clk[1] is the SM clock
     // the kernel actually ran at.
     unsigned long long *clk;
+    // TF32 rounding inside the GEMM kernel (kKindTF32R).  Index 0 is op(A), 1 is op(B).
+    // The kernel writes the same rounded K-major copies the pre-pass would (element (r, q)
+    // of batch entry b at cv_dst[x] + b * cv_dstride[x] + r * cv_kp + q), from the raw
+    // FP32 operand (element (r, q) at cv_src[x] + b * cv_stride[x] + (cv_kmajor[x] ?
+    // q + r * cv_ld[x] : r + q * cv_ld[x])).  The copies are cut into items: (operand,
+    // batch entry, panel of cv_panel_rows[x] rows -- the tile rows of that operand --, chunk
+    // of cv_kc K elements), item index cv_base[x] + (b * cv_panels[x] + panel) * cv_chunks
+    // + chunk; and each item into cv_subs[x] sub-units of kCvRows rows x kCvK elements of
+    // K.  cv_cnt holds three arrays of counters, zeroed before the launch: sub-units
+    // claimed per item [cv_items], sub-units done per item [cv_items], and sub-units done
+    // per panel [cv_panels_total] (panel index cv_pbase[x] + b * cv_panels[x] + panel).
+    const void *cv_src[2];
+    void *cv_dst[2];
+    int64_t cv_ld[2], cv_stride[2], cv_dstride[2];
+    int64_t cv_kp;
+    int cv_kmajor[2];
+    int cv_rows[2];
+    int cv_panel_rows[2];
+    int cv_panels[2];
+    int cv_subs[2];
+    int cv_base[2], cv_pbase[2];
+    int cv_kc, cv_chunks, cv_kb_per_chunk;
+    int cv_items;
+    uint32_t *cv_cnt;
 };
+
+// Sub-unit of the in-kernel TF32 rounding: 64 rows x 128 K elements (32 KiB of FP32).
+constexpr int kCvRows = 64;
+constexpr int kCvK = 128;
 
 // Tile t -> (batch b, m-tile mt, n-tile nt) with grouped rasterisation.
 __host__ __device__ inline void raster(const GemmArgs &p, int t, int &b, int &mt, int &nt)

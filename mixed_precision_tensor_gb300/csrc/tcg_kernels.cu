@@ -56,6 +56,7 @@ struct SmemCtl {
     uint64_t drain;
     uint32_t tmem_base;
     volatile int abort_flag;
+    volatile int cv_slot[2];           // epilogue half: the sub-unit its leader claimed
 };
 static_assert(sizeof(SmemCtl) <= kBarrierBytes, "barrier area too small");
 
@@ -125,6 +126,218 @@ __device__ __forceinline__ UnitInfo unit_info(const GemmArgs &p, int u)
     return w;
 }
 
+// FP32 -> TF32, round to nearest, ties to even, kept in FP32 bits (low 13 bits zero).
+// Inf passes through; NaN becomes a quiet NaN of the same sign (its payload could sit
+// entirely in the 13 dropped bits).  A carry out of the mantissa moves to the next
+// binade, and values past the largest TF32 number become Inf, as RNE requires.
+__device__ __forceinline__ uint32_t tf32_rne_bits(uint32_t u)
+{
+    if ((u & 0x7F800000u) == 0x7F800000u)
+        return (u & 0x007FFFFFu) ? ((u & 0x80000000u) | 0x7FC00000u) : u;
+    return (u + 0x0FFFu + ((u >> 13) & 1u)) & 0xFFFFE000u;
+}
+
+// ------------------------------------------ TF32 rounding inside the GEMM kernel
+// kKindTF32R: the GEMM kernel writes the rounded K-major copies of op(A) and op(B) itself
+// while it multiplies, instead of two pre-pass kernels running before it.  The copies
+// are cut into items (operand, batch entry, panel of tile rows, chunk of K) and the
+// items into sub-units of kCvRows x kCvK elements (GemmArgs cv_*).  The epilogue warps,
+// idle while an accumulator fills, claim sub-units through a per-item counter, in the
+// order in which their own pair's work units will need them, round them and count them
+// done; the producer waits for an item's count before it loads the item's stages.  Each
+// element is rounded once, so the extra traffic is one read and one write of each
+// operand, spread over the GEMM, where the pre-pass kernels ran alone before it.
+// Nothing inside a sub-unit waits, so a claimed sub-unit always completes, and every
+// item a pair needs lies on its own walk: the producers' waits end whether or not the
+// other CTAs are resident.
+
+struct CvItem {
+    int x, b, panel, chunk;
+};
+__device__ __forceinline__ CvItem cv_item(const GemmArgs &p, int item)
+{
+    CvItem it;
+    it.x = item >= p.cv_base[1] ? 1 : 0;
+    const int rem = item - p.cv_base[it.x];
+    const int bp = rem / p.cv_chunks;
+    it.chunk = rem - bp * p.cv_chunks;
+    it.b = bp / p.cv_panels[it.x];
+    it.panel = bp - it.b * p.cv_panels[it.x];
+    return it;
+}
+
+// Round sub-unit s of an item with the 128 threads of an epilogue half (tid = 0..127,
+// named barrier bar_id); tile: 16 KiB of the half's staging buffer.  Sub-unit s covers
+// rows r0 .. r0 + 63 of the panel and K elements q0 .. q0 + 127 of the chunk.
+//   K-major source: 32 threads per row (16 bytes each), 16 rows per thread, read and
+//     written along K.
+//   M/N-major source: two 64 x 64 transposes through shared memory, 16 threads per
+//     64-element row on both sides (16-byte global accesses).  The tile has no padding
+//     column: element (K row kr, row r) sits at word kr * 64 + (r ^ 2 (kr >> 2)), which
+//     keeps the 16-byte writes and the 4-byte column reads free of bank conflicts.
+// As in the pre-pass kernels, rows past the operand are skipped, K past k reads zeros
+// (M/N-major) and each 16-byte group that starts before round_up(k, 4) is written.
+// mid() runs once every load is issued: the half's leader uses it to overlap its
+// bookkeeping (the previous sub-unit's done count, the next claim) with the loads.
+template <typename Mid>
+__device__ __forceinline__ void cv_convert(const GemmArgs &p, int item, int s, int tid,
+                                           uint32_t *tile, uint32_t bar_id, Mid &&mid)
+{
+    const CvItem it = cv_item(p, item);
+    const int x = it.x;
+    const int rg = p.cv_panel_rows[x] / kCvRows;
+    const int r0 = it.panel * p.cv_panel_rows[x] + (s % rg) * kCvRows;
+    const int64_t q0 = static_cast<int64_t>(it.chunk) * p.cv_kc + (s / rg) * kCvK;
+    const int rows = p.cv_rows[x];
+    const int64_t kp = p.cv_kp, ld = p.cv_ld[x];
+    const uint32_t *src = static_cast<const uint32_t *>(p.cv_src[x]) + it.b * p.cv_stride[x];
+    uint32_t *dst = static_cast<uint32_t *>(p.cv_dst[x]) + it.b * p.cv_dstride[x];
+    if (p.cv_kmajor[x]) {
+        const int j = tid & 31, rr = tid >> 5;
+        const int64_t q = q0 + 4 * j;
+        uint4 v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int r = r0 + rr + 4 * i;
+            v[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (r < rows && q < kp)
+                v[i] = __ldg(reinterpret_cast<const uint4 *>(src + q + static_cast<int64_t>(r) * ld));
+        }
+        mid();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int r = r0 + rr + 4 * i;
+            if (r < rows && q < kp) {
+                const uint4 o = make_uint4(tf32_rne_bits(v[i].x), tf32_rne_bits(v[i].y),
+                                           tf32_rne_bits(v[i].z), tf32_rne_bits(v[i].w));
+                *reinterpret_cast<uint4 *>(dst + q + static_cast<int64_t>(r) * kp) = o;
+            }
+        }
+        return;
+    }
+    const int k = p.k;
+    const int c = tid & 15, w = tid >> 4;
+    uint4 v[2][8];
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {           // K rows q0 + 64 t + w + 8 j, rows r0 + 4c ..
+            const int64_t q = q0 + 64 * t + w + 8 * j;
+            const int r = r0 + 4 * c;
+            v[t][j] = make_uint4(0u, 0u, 0u, 0u);
+            if (q < k && r < rows)
+                v[t][j] = __ldg(reinterpret_cast<const uint4 *>(src + r + q * ld));
+        }
+    mid();
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        named_barrier_sync(bar_id, 128);         // the tile's previous readers are done
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int kr = w + 8 * j;
+            const uint32_t f = static_cast<uint32_t>(kr >> 2) << 1;
+            // words 4c .. 4c + 3 of K row kr go to 4 (c ^ (f >> 2)) + (i ^ (f & 2))
+            const uint4 u = v[t][j];
+            const uint4 o = (f & 2u) ? make_uint4(u.z, u.w, u.x, u.y) : u;
+            *reinterpret_cast<uint4 *>(tile + kr * 64 + 4 * (c ^ static_cast<int>(f >> 2))) = o;
+        }
+        named_barrier_sync(bar_id, 128);
+        const int64_t q = q0 + 64 * t + 4 * c;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {             // output rows r0 + w + 8 j
+            const int rl = w + 8 * j, r = r0 + rl;
+            if (r >= rows || q >= k)
+                continue;
+            const int sw = rl ^ (2 * c);
+            const uint4 o = make_uint4(tf32_rne_bits(tile[(4 * c) * 64 + sw]),
+                                       tf32_rne_bits(tile[(4 * c + 1) * 64 + sw]),
+                                       tf32_rne_bits(tile[(4 * c + 2) * 64 + sw]),
+                                       tf32_rne_bits(tile[(4 * c + 3) * 64 + sw]));
+            *reinterpret_cast<uint4 *>(dst + q + static_cast<int64_t>(r) * kp) = o;
+        }
+    }
+}
+
+// The producer's wait for items ia and ib (their sub-units done), bounded like every
+// wait of the kernel; then this thread's TMA loads see the rounded values.
+template <int CG>
+__device__ __forceinline__ bool cv_wait(const GemmArgs &p, SmemCtl *ctl, int ia, int ib)
+{
+    const uint32_t *done = p.cv_cnt + p.cv_items;
+    const uint32_t ta = static_cast<uint32_t>(p.cv_subs[0]);
+    const uint32_t tb = static_cast<uint32_t>(p.cv_subs[1]);
+    if (ld_relaxed_gpu(done + ia) < ta || ld_relaxed_gpu(done + ib) < tb) {
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_relaxed_gpu(done + ia) < ta || ld_relaxed_gpu(done + ib) < tb) {
+            if (ctl->abort_flag)
+                return false;
+            if (globaltimer_ns() - t0 > p.wait_limit_ns) {
+                raise_abort<CG>(ctl, p, kErrConvert);
+                return false;
+            }
+        }
+    }
+    fence_acq_rel_gpu();
+    fence_proxy_async_global();
+    return true;
+}
+
+// Count sub-units of `item` done (the half's leader, after a barrier that follows every
+// thread's writes of it): the fence makes those writes visible at GPU scope before the
+// counts (the barrier-then-fence release pattern).
+__device__ __forceinline__ void cv_report(const GemmArgs &p, int item)
+{
+    const CvItem ci = cv_item(p, item);
+    __threadfence();
+    atomicAdd(p.cv_cnt + p.cv_items + item, 1u);
+    atomicAdd(p.cv_cnt + 2 * p.cv_items + p.cv_pbase[ci.x] + ci.b * p.cv_panels[ci.x] + ci.panel,
+              1u);
+}
+
+// An epilogue half's walk over the items its pair's work units need, in the order they
+// need them: unit by unit (t = cluster_id, + num_clusters, ...), chunk by chunk, A then
+// B.  claim() returns item * 64 + sub-unit of the next sub-unit it won, or -1 once the
+// walk is over.  Only the half's leader walks.
+struct CvWalk {
+    int t, c, c_end, x, ia, ib;
+
+    __device__ __forceinline__ void start(const GemmArgs &p, int unit)
+    {
+        t = unit;
+        x = 0;
+        if (t >= p.total_tiles)
+            return;
+        const UnitInfo w = unit_info(p, t);
+        const int kstage = kDepth * (kRowBytes / 4);            // K elements per stage
+        c = (w.kb0 * kstage) / p.cv_kc;
+        c_end = (w.kb1 * kstage + p.cv_kc - 1) / p.cv_kc;
+        ia = p.cv_base[0] + ((p.a_bcast ? 0 : w.b) * p.cv_panels[0] + w.mt) * p.cv_chunks;
+        ib = p.cv_base[1] + ((p.b_bcast ? 0 : w.b) * p.cv_panels[1] + w.nt) * p.cv_chunks;
+    }
+
+    __device__ __forceinline__ int claim(const GemmArgs &p, int num_clusters)
+    {
+        uint32_t *claimed = p.cv_cnt;
+        while (t < p.total_tiles) {
+            const int item = (x == 0 ? ia : ib) + c;
+            const uint32_t subs = static_cast<uint32_t>(p.cv_subs[x]);
+            if (ld_relaxed_gpu(claimed + item) < subs) {
+                const uint32_t s = atomicAdd(claimed + item, 1u);
+                if (s < subs)
+                    return item * 64 + static_cast<int>(s);
+            }
+            if (x == 0) {
+                x = 1;
+            } else if (++c < c_end) {
+                x = 0;
+            } else {
+                start(p, t + num_clusters);
+            }
+        }
+        return -1;
+    }
+};
+
 template <int OUT>
 __device__ __forceinline__ void store_out(void *D, int64_t idx, float v)
 {
@@ -190,6 +403,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // low words (tmA2, tmB2); each K slice takes three products, lo_A hi_B, hi_A lo_B and
     // hi_A hi_B, into the one accumulator.
     constexpr bool kX3 = KIND == kKindTF32x3;
+    // In-kernel TF32 rounding (kKindTF32R): the epilogue warps round the operands into
+    // their K-major copies between accumulators and the producer waits for each item.
+    constexpr bool kFuse = KIND == kKindTF32R;
     constexpr int kOps = kX3 ? 2 : 1;                         // words per operand
     constexpr int kStages = Cfg::kRingBytes / (kOps * Cfg::kStageBytes);
     static_assert(kStages >= 2, "ring too small");
@@ -279,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The MMA kind is a template argument and every per-slice descriptor offset is
     // computed before the loop: the issuing thread's loop must stay branch-free and
     // short, as its instruction rate is what keeps the tensor core fed.
-    constexpr bool kTf32 = KIND == kKindTF32 || kX3;
+    constexpr bool kTf32 = KIND == kKindTF32 || kX3 || kFuse;
     constexpr uint32_t kEsize = kTf32 ? 4u : (KIND == kKindF8 ? 1u : 2u);
     constexpr uint32_t kKmma = 32u / kEsize;                  // K per MMA instruction
     constexpr int kMmasPerRow = kRowBytes / 32;               // 4 MMAs per 128-byte K row
@@ -329,7 +545,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int m0 = w.mt * kTileM + static_cast<int>(rank) * kBM;
                 const int n0 = w.nt * BN + static_cast<int>(rank) * kBRows;
                 const int za = p.a_bcast ? 0 : w.b, zb = p.b_bcast ? 0 : w.b;
+                // In-kernel rounding: the unit's items (A and B, chunk 0 of the panel); when
+                // both panels are done already, the unit needs no further waits.
+                int cv_ia = 0, cv_ib = 0;
+                bool cv_ready = true;
+                if constexpr (kFuse) {
+                    cv_ia = p.cv_base[0] + (za * p.cv_panels[0] + w.mt) * p.cv_chunks;
+                    cv_ib = p.cv_base[1] + (zb * p.cv_panels[1] + w.nt) * p.cv_chunks;
+                    const uint32_t *pdone = p.cv_cnt + 2 * p.cv_items;
+                    const int pa = p.cv_pbase[0] + za * p.cv_panels[0] + w.mt;
+                    const int pb = p.cv_pbase[1] + zb * p.cv_panels[1] + w.nt;
+                    cv_ready = ld_relaxed_gpu(pdone + pa) >=
+                                   static_cast<uint32_t>(p.cv_subs[0] * p.cv_chunks) &&
+                               ld_relaxed_gpu(pdone + pb) >=
+                                   static_cast<uint32_t>(p.cv_subs[1] * p.cv_chunks);
+                    if (cv_ready) {
+                        fence_acq_rel_gpu();
+                        fence_proxy_async_global();
+                    }
+                }
                 for (int kb = kb_begin; kb < kb_end; ++kb) {
+                    if constexpr (kFuse) {
+                        if (!cv_ready && (kb == kb_begin || kb % p.cv_kb_per_chunk == 0)) {
+                            const int c = kb / p.cv_kb_per_chunk;
+                            if (!cv_wait<CG>(p, ctl, cv_ia + c, cv_ib + c)) {
+                                ok = false;
+                                break;
+                            }
+                        }
+                    }
                     const uint32_t fb_local = smem_u32(&ctl->full[stage]);
                     const uint32_t fb = (CG == 2) ? mapa_shared(fb_local, 0) : fb_local;
                     if (!wait_bounded<CG>(smem_u32(&ctl->empty[stage]), phase ^ 1u, ctl, p,
@@ -441,14 +685,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 mma_tf32(d_tmem, ad, bd, p.idesc, 1u);
                             }
                         } else if constexpr (CG == 2) {
-                            if constexpr (KIND == kKindTF32)
+                            if constexpr (KIND == kKindTF32 || kFuse)
                                 mma_tf32_pair(d_tmem, ad, bd, p.idesc, accum);
                             else if constexpr (KIND == kKindF8)
                                 mma_f8_pair(d_tmem, ad, bd, p.idesc, accum);
                             else
                                 mma_f16_pair(d_tmem, ad, bd, p.idesc, accum);
                         } else {
-                            if constexpr (KIND == kKindTF32)
+                            if constexpr (KIND == kKindTF32 || kFuse)
                                 mma_tf32(d_tmem, ad, bd, p.idesc, accum);
                             else if constexpr (KIND == kKindF8)
                                 mma_f8(d_tmem, ad, bd, p.idesc, accum);
@@ -544,20 +788,84 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             issued = gg + 1;
         };
-        if (BETA && half_leader)
+        // With in-kernel TF32 rounding the staging buffers also serve the rounding's
+        // transposes between tiles, so C loads stay within a tile (issued once its
+        // accumulator is ready) instead of running ahead across tile boundaries.
+        if (BETA && !kFuse && half_leader)
             for (uint32_t gg = 0; gg < static_cast<uint32_t>(kAhead); ++gg)
                 load_c_chunk(gg);
         uint32_t g = 0;                                         // chunks done by this half
         int it = 0;
+        CvWalk walk{};                                          // the half leader's walk
+        bool cv_more = kFuse;
+        if constexpr (kFuse) {
+            if (half_leader)
+                walk.start(p, cluster_id);
+        }
         for (int t = cluster_id; t < p.total_tiles; t += num_clusters, ++it) {
             const int acc = it % kAccBufs;
             const uint32_t acc_phase = (it / kAccBufs) & 1;
+            if constexpr (kFuse) {
+                // Round sub-units until this tile's accumulator is ready or the walk is
+                // over.  The leader decides (test the barrier, else claim) and tells the
+                // half through the shared slot; a sub-unit is counted done once every
+                // thread's writes are fenced.
+                // The leader's bookkeeping runs while the sub-unit's loads are in flight:
+                // the previous sub-unit's done count (`unreported`) and the claim of the
+                // next one (`pending`, which must be converted before anything else).
+                if (cv_more) {
+                    const uint32_t acc_bar = smem_u32(&ctl->acc_full[acc]);
+                    uint32_t *tile = reinterpret_cast<uint32_t *>(stage0_ptr);
+                    if (half_leader)
+                        bulk_wait_group_read<0>();              // no store reads the staging
+                    int pending = -3;                           // leader: nothing claimed
+                    int unreported = -1;                        // leader: item not yet counted
+                    for (;;) {
+                        if (half_leader) {
+                            int code = pending;
+                            if (code == -3)
+                                code = mbar_test_wait(acc_bar, acc_phase)
+                                           ? -2                 // the accumulator is ready
+                                           : (ctl->abort_flag ? -1 : walk.claim(p, num_clusters));
+                            ctl->cv_slot[half] = code;
+                            pending = -3;
+                        }
+                        named_barrier_sync(bar_id, 128);
+                        const int code = ctl->cv_slot[half];
+                        if (code < 0) {
+                            cv_more = code == -2;
+                            break;
+                        }
+                        cv_convert(p, code >> 6, code & 63, rl, tile, bar_id, [&] {
+                            if (half_leader) {
+                                if (unreported >= 0)
+                                    cv_report(p, unreported);
+                                unreported = -1;
+                                if (!mbar_test_wait(acc_bar, acc_phase))
+                                    pending = ctl->abort_flag ? -1 : walk.claim(p, num_clusters);
+                            }
+                        });
+                        fence_proxy_async_shared();
+                        named_barrier_sync(bar_id, 128);
+                        if (half_leader)
+                            unreported = code >> 6;
+                    }
+                    if (half_leader && unreported >= 0)
+                        cv_report(p, unreported);
+                }
+            }
             bool ok = wait_bounded<CG>(smem_u32(&ctl->acc_full[acc]), acc_phase, ctl, p,
                                        kErrEpilogue);
             if (named_barrier_or(bar_id, 128, !ok || ctl->abort_flag))
                 break;
             tc_fence_after();
             const UnitInfo wt = unit_info(p, t);
+            const uint32_t g_end = g + static_cast<uint32_t>(kChunks);
+            if constexpr (kFuse && BETA) {
+                if (half_leader)
+                    for (uint32_t gg = g; gg < g + static_cast<uint32_t>(kAhead) && gg < g_end; ++gg)
+                        load_c_chunk(gg);
+            }
             bool aborted = false;
 #pragma unroll 1
             for (int c = 0; c < kChunks; ++c, ++g) {
@@ -635,8 +943,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // The buffer of chunk g + 1 (no C) or g + kAhead (C) was last stored
                     // from by chunk g + 1 - kEpiBufs: allow only this chunk's store pending.
                     bulk_wait_group_read<1>();
-                    if constexpr (BETA)
-                        load_c_chunk(g + kAhead);
+                    if constexpr (BETA) {
+                        if (!kFuse || g + kAhead < g_end)
+                            load_c_chunk(g + kAhead);
+                    }
                 }
                 named_barrier_sync(bar_id, 128);               // the next buffer is free
             }
@@ -790,17 +1100,6 @@ __global__ void __launch_bounds__(256) tcg_tail_reduce_kernel(const float *__res
     griddep_launch_dependents();
 }
 
-// FP32 -> TF32, round to nearest, ties to even, kept in FP32 bits (low 13 bits zero).
-// Inf passes through; NaN becomes a quiet NaN of the same sign (its payload could sit
-// entirely in the 13 dropped bits).  A carry out of the mantissa moves to the next
-// binade, and values past the largest TF32 number become Inf, as RNE requires.
-__device__ __forceinline__ uint32_t tf32_rne_bits(uint32_t u)
-{
-    if ((u & 0x7F800000u) == 0x7F800000u)
-        return (u & 0x007FFFFFu) ? ((u & 0x80000000u) | 0x7FC00000u) : u;
-    return (u + 0x0FFFu + ((u >> 13) & 1u)) & 0xFFFFE000u;
-}
-
 // out[b][r][p] = tf32(op element (r, p)) with rows r < rows (the M or N extent) and K
 // contiguous (ld_out elements per row).  The input element (r, p) sits at
 // in[b*stride_in + p + r*ld] (K-major) or in[b*stride_in + r + p*ld] (M/N-major).
@@ -854,6 +1153,8 @@ static GemmKernelFn gemm_fn_cg(int out_kind, int kind)
         return tcg_gemm_kernel<kOutF32, CG, kKindTF32, CBUF, kBN>;
     if (kind == kKindTF32x3)
         return tcg_gemm_kernel<kOutF32, CG, kKindTF32x3, CBUF, kBN>;
+    if (kind == kKindTF32R)
+        return tcg_gemm_kernel<kOutF32, CG, kKindTF32R, CBUF, kBN>;
     if (kind == kKindF8) {
         switch (out_kind) {
         case kOutF32: return tcg_gemm_kernel<kOutF32, CG, kKindF8, CBUF, kBN>;

@@ -136,8 +136,11 @@ def test_workspace_size_query(lib):
     assert tcg.tcg_gemm_workspace_size(N, N, 64, 64, 64, F16, C32) == 0
     ws = tcg.tcg_gemm_workspace_size(N, N, 100, 50, 30, F32, TF32)
     kp = 32
-    assert ws >= (100 + 50) * kp * 4
-    assert tcg.tcg_gemm_workspace_size(N, N, 100, 50, 30, F32, SPLIT3) == 2 * ws
+    copies = (100 + 50) * kp * 4             # the rounded K-major copies (256-byte multiples)
+    # plus the counters of the in-kernel rounding: (2 items + 1 panel) x 4 bytes per
+    # operand, in one 256-byte block
+    assert ws == copies + 256
+    assert tcg.tcg_gemm_workspace_size(N, N, 100, 50, 30, F32, SPLIT3) == 2 * copies
     assert tcg.tcg_set_workspace(tcg.tcg_create(), 0x1000 + 16, 1024) == INV   # not 256-aligned
 
 
