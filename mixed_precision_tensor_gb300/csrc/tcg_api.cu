@@ -757,6 +757,13 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
             return s2;
         a.a_bcast = abc ? 1 : 0;
         a.b_bcast = bbc ? 1 : 0;
+        // An operand whose rows meet a single tile along the other dimension, and that no
+        // other batch entry shares, is read exactly once (e.g. a batch of one-tile
+        // products): its loads need not stay in L2.  Measured on GB300, 512 batched
+        // 256^3 FP16 products, back-to-back calls: 58.3 -> 51.1 us (C and D then stay in
+        // L2); with L2 flushed between calls 59.4 us either way.
+        a.a_once = (!abc && a.num_n_tiles == 1) ? 1 : 0;
+        a.b_once = (!bbc && a.num_m_tiles == 1) ? 1 : 0;
         CUtensorMap tmA2, tmB2;
         if (opA2) {
             int mode_lo = 0;

@@ -103,6 +103,7 @@ struct GemmArgs {
     int group_m;               // tile rasterisation: group of m-tiles walked together
     int a_mode, b_mode;        // OperandMode of A and B
     int a_bcast, b_bcast;      // batch stride 0: always batch coordinate 0
+    int a_once, b_once;        // every element read by one tile only: L2 evict_first loads
     int kind;                  // MmaKind
     int k_row;                 // K elements per 128-byte row: 64, 32 (TF32), 128 (FP8)
     uint32_t idesc;            // tcgen05 instruction descriptor
