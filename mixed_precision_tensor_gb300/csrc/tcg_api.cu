@@ -377,7 +377,8 @@ tcgStatus_t operand_map(tcgContext *h, const void *ptr, tcgDataType_t t, bool km
 // Map of D (= C) for the epilogue: {m, n, batch}, box {128 rows, chunk columns, 1}, no
 // swizzle; TMA loads of C zero-fill and TMA stores of D clip outside the matrix.
 tcgStatus_t output_map(tcgContext *h, void *C, tcgDataType_t t, int64_t m, int64_t n,
-                       int64_t ldc, int64_t strideC, int64_t batch, CUtensorMap *out)
+                       int64_t ldc, int64_t strideC, int64_t batch, CUtensorMap *out,
+                       int c_bufs = 0)
 {
     const int es = elem_size(t);
     const uint64_t ldb = static_cast<uint64_t>(ldc) * es;
@@ -387,7 +388,8 @@ tcgStatus_t output_map(tcgContext *h, void *C, tcgDataType_t t, int64_t m, int64
     const uint64_t dims[3] = {static_cast<uint64_t>(m), static_cast<uint64_t>(n),
                               static_cast<uint64_t>(batch < 1 ? 1 : batch)};
     const uint64_t str[2] = {ldb, bstride};
-    const uint32_t box[3] = {static_cast<uint32_t>(kBM), static_cast<uint32_t>(epi_cols(es)), 1};
+    const uint32_t box[3] = {static_cast<uint32_t>(kBM),
+                             static_cast<uint32_t>(epi_cols(es, c_bufs)), 1};
     return get_map(h, C, t, 3, dims, str, box, out, false);
 }
 
@@ -642,9 +644,14 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
     const bool splitk = plan.splits > 1;
     // The GEMM kernel writes D -- or, split, the FP32 partial sums (slice b * splits + s).
     CUtensorMap tmD;
+    // Four C buffers (one operand stage less; 16 KiB chunks for 16-bit outputs) when the
+    // epilogue's C/D traffic outweighs the main loop: K bytes per row <= 1024 x D's element
+    // size.  Split, the kernel writes raw partial sums (beta 0).
+    const int c_bufs = (splitk || p.beta == 0.0f) ? 0
+                     : (cg == 2 && k * es_k <= 1024 * elem_size(p.Ctype) ? 4 : 2);
     st = splitk ? output_map(h, W, TCG_R_32F, p.m, p.n, ldw, ldw * p.n, p.batch * plan.splits,
                              &tmD)
-                : output_map(h, p.C, p.Ctype, p.m, p.n, p.ldc, strideC, p.batch, &tmD);
+                : output_map(h, p.C, p.Ctype, p.m, p.n, p.ldc, strideC, p.batch, &tmD, c_bufs);
     if (st != TCG_STATUS_SUCCESS)
         return st;
     // Split tail tiles write their partial sums to tile-sized FP32 slices of W.
@@ -733,10 +740,7 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
         // partial-sum slices and the reduction applies alpha and beta.
         a.alpha = splitk ? 1.0f : p.alpha;
         a.beta = splitk ? 0.0f : beta;
-        // Four C buffers (one operand stage less) when the epilogue's C/D traffic
-        // outweighs the main loop: K bytes per row <= 1024 x D's element size.
-        a.c_bufs = a.beta == 0.0f ? 0
-                 : (cg == 2 && k * es <= 1024 * elem_size(p.Ctype) ? 4 : 2);
+        a.c_bufs = a.beta == 0.0f ? 0 : c_bufs;
         a.C = splitk ? static_cast<const void *>(W) : p.C;
         a.D = splitk ? static_cast<void *>(W) : p.C;
         a.ldc = splitk ? ldw : p.ldc;

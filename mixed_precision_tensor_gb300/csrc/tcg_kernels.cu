@@ -416,7 +416,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tmA2,
                     const __grid_constant__ CUtensorMap tmB2, const GemmArgs p)
 {
-    using Cfg = TileCfg<CG, CBUF, BN>;
+    constexpr int kOutB = OUT == kOutF32 ? 4 : 2;
+    constexpr int kChunkB = epi_chunk_bytes(kOutB, CBUF);   // bytes of one epilogue chunk
+    using Cfg = TileCfg<CG, CBUF, BN, kChunkB>;
     constexpr int kAccBufs = Cfg::kAccBufs;
     constexpr bool BETA = CBUF != 0;                          // C is read
     // Two-word TF32 (kKindTF32x3): a stage carries A's and B's high words, then their
@@ -788,7 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // tiles form one sequence g = 0, 1, ... per half; with beta != 0 the C loads run
         // kEpiBufs - 1 chunks ahead of it (across tile boundaries).
         constexpr int kOutBytes = OUT == kOutF32 ? 4 : 2;
-        constexpr int kCols = epi_cols(kOutBytes);             // 16 (FP32) or 32 (16-bit)
+        constexpr int kCols = epi_cols(kOutBytes, CBUF);       // 16 (FP32), 32 or 64 (16-bit)
         constexpr int kChunks = (BN / 2) / kCols;              // per half per tile
         constexpr int kAhead = BETA ? kEpiBufs - 1 : 0;        // C loads in flight
         const int q = warp & 3;
@@ -797,8 +799,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t bar_id = 1u + static_cast<uint32_t>(half);
         const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t acc_empty_local = smem_u32(&ctl->acc_empty[0]);
-        const uint32_t stage0 = epi_smem + static_cast<uint32_t>(half * kEpiBufs * kEpiChunkBytes);
-        uint8_t *stage0_ptr = epi_ptr + half * kEpiBufs * kEpiChunkBytes;
+        const uint32_t stage0 = epi_smem + static_cast<uint32_t>(half * kEpiBufs * kChunkB);
+        uint8_t *stage0_ptr = epi_ptr + half * kEpiBufs * kChunkB;
         const int rl = q * 32 + lane;                           // row within the CTA's 128
 
         // Origin (first row, first column, slice) of chunk c of this half in work unit w.
@@ -833,8 +835,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t buf = gg % kEpiBufs;
             const uint32_t bar = smem_u32(&ctl->c_full[half][buf]);
             if (!tail && x < p.m && y < p.n) {
-                mbar_arrive_expect_tx(bar, kEpiChunkBytes);
-                tma_load_3d(stage0 + buf * kEpiChunkBytes, &tmD, bar, x, y, z);
+                mbar_arrive_expect_tx(bar, kChunkB);
+                tma_load_3d(stage0 + buf * kChunkB, &tmD, bar, x, y, z);
             } else {
                 mbar_arrive(bar);       // nothing of this chunk is in the matrix
             }
@@ -922,7 +924,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
             for (int c = 0; c < kChunks; ++c, ++g) {
                 const uint32_t buf = g % kEpiBufs;
-                uint8_t *sbuf = stage0_ptr + buf * kEpiChunkBytes;
+                uint8_t *sbuf = stage0_ptr + buf * kChunkB;
                 if constexpr (BETA) {
                     ok = wait_bounded<CG>(smem_u32(&ctl->c_full[half][buf]),
                                           (g / kEpiBufs) & 1u, ctl, p, kErrEpilogue);
@@ -935,10 +937,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t taddr = tmem_base + lane_off +
                                        static_cast<uint32_t>(acc * BN + half * (BN / 2) + c * kCols);
                 uint32_t v[kCols];
-                if constexpr (kCols == 16)
+                if constexpr (kCols == 16) {
                     tmem_ld_32x32b_x16(taddr, v);
-                else
-                    tmem_ld_32x32b_x32(taddr, v);
+                } else {
+#pragma unroll
+                    for (int h = 0; h < kCols / 32; ++h)
+                        tmem_ld_32x32b_x32(taddr + 32 * h,
+                                           *reinterpret_cast<uint32_t (*)[32]>(v + 32 * h));
+                }
                 tmem_ld_wait();
                 if (c == kChunks - 1) {
                     // This warp has read its part of the accumulator: report to the MMA CTA.
@@ -994,9 +1000,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 named_barrier_sync(bar_id, 128);               // the block is complete
                 if (half_leader) {
                     if (tail_unit)
-                        tma_store_3d(&tmW, stage0 + buf * kEpiChunkBytes, cx, cy, cz);
+                        tma_store_3d(&tmW, stage0 + buf * kChunkB, cx, cy, cz);
                     else if (!thread_store && cx < p.m && cy < p.n)
-                        tma_store_3d(&tmD, stage0 + buf * kEpiChunkBytes, cx, cy, cz);
+                        tma_store_3d(&tmD, stage0 + buf * kChunkB, cx, cy, cz);
                     bulk_commit_group();
                     // The buffer of chunk g + 1 (no C) or g + kAhead (C) was last stored
                     // from by chunk g + 1 - kEpiBufs: allow only this chunk's store pending.
