@@ -659,7 +659,7 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
     CUtensorMap tmW = tmD;
     if (tail_tiles) {
         st = output_map(h, W, TCG_R_32F, tile_m, kBN, tile_m, (int64_t)tile_m * kBN,
-                        tail_tiles * tail.splits, &tmW);
+                        tail_tiles * tail.splits, &tmW, c_bufs);
         if (st != TCG_STATUS_SUCCESS)
             return st;
     }
@@ -1749,7 +1749,7 @@ extern "C" tcgStatus_t tcg_gemm_tf32_noalloc(void *stream, tcgOp_t transa, tcgOp
     if (st != TCG_STATUS_SUCCESS)
         return st;
     CUtensorMap tmD;
-    st = output_map(&ctx, C, TCG_R_32F, m, n, ldc, 0, 1, &tmD);
+    st = output_map(&ctx, C, TCG_R_32F, m, n, ldc, 0, 1, &tmD, a.c_bufs);
     if (st != TCG_STATUS_SUCCESS)
         return st;
     const int64_t want = static_cast<int64_t>(a.total_tiles) * cg;

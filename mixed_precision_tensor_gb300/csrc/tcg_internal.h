@@ -26,7 +26,7 @@ constexpr int kThreads = 32 * (2 + kEpiWarps);     // producer, MMA, 8 epilogue 
 // Shared memory: operand ring + epilogue staging = kDataBytes.  Epilogue staging: each
 // half of the epilogue (4 warps, 128 rows) owns CBUF buffers (2 when C is not read) of
 // one 128-row chunk of D (16 FP32 or 32 16-bit columns: 8 KiB; in the CBUF = 4 variant
-// with a 16-bit output, three buffers of 64 columns, 16 KiB -- see epi_chunk_bytes),
+// three buffers of 32 FP32 or 64 16-bit columns, 16 KiB -- see epi_chunk_bytes),
 // loaded with C by TMA (buffers - 1) chunks ahead when beta != 0 and written back by TMA.
 // Four buffers (and a shorter ring) pay off when
 // the epilogue's C/D traffic outweighs the main loop: K bytes per operand row <= 1024 x
@@ -35,15 +35,18 @@ constexpr int kDataBytes = 224 * 1024;
 constexpr int kEpiChunkBytes = 8 * 1024;
 constexpr int kBarrierBytes = 512;
 constexpr int kSmemBytes = kDataBytes + kBarrierBytes + 1024;  // + alignment slack
-// Bytes and columns of one epilogue chunk.  16-bit outputs in the CBUF = 4 variant (short
-// K: the epilogue's C/D traffic outweighs the main loop) stage 16 KiB chunks -- half the
-// chunks per tile, so half the per-chunk barriers, proxy fences and TMA operations
-// (measured on GB300, 512 batched 256^3 FP16 products, beta = 0.5, back to back: 51.8 ->
-// 49.0 us with four such buffers; 16 KiB chunks in every variant slowed a 4096^3 FP16 ->
-// FP16 product, beta = 1, from 94 to 99 us through its shorter ring).
+// Bytes and columns of one epilogue chunk.  The CBUF = 4 variant (short K: the epilogue's
+// C/D traffic outweighs the main loop) stages 16 KiB chunks, 64 16-bit or 32 FP32 columns
+// -- half the chunks per tile, so half the per-chunk barriers, proxy fences and TMA
+// operations (measured on GB300: 512 batched 256^3 FP16 products, beta = 0.5, back to
+// back, 51.8 -> 49.0 us with four such buffers; the 256^3 FP16 -> FP32 product, beta = 1,
+// 14.3 -> 13.6-13.9 us; 16 KiB chunks in every variant slowed a 4096^3 FP16 -> FP16
+// product, beta = 1, from 94 to 99 us through its shorter ring).  Every tensor map of D
+// (or of the tail partial sums) that such a kernel stores through has a box this wide.
 __host__ __device__ constexpr int epi_chunk_bytes(int out_bytes, int c_bufs)
 {
-    return (out_bytes == 2 && c_bufs == 4) ? 2 * kEpiChunkBytes : kEpiChunkBytes;
+    (void)out_bytes;
+    return c_bufs == 4 ? 2 * kEpiChunkBytes : kEpiChunkBytes;
 }
 __host__ __device__ constexpr int epi_cols(int out_bytes, int c_bufs)
 {
@@ -60,7 +63,7 @@ __host__ __device__ constexpr int epi_cols(int out_bytes, int c_bufs)
 // operands use a 4-D view that brings a tile's chunks in one box (OperandMode kMN4).
 template <int CG, int CBUF, int BN = kBN, int CHUNK = kEpiChunkBytes>
 struct TileCfg {
-    // CBUF 4 with 16 KiB chunks (16-bit output) keeps three of them, so that the ring
+    // CBUF 4 with its 16 KiB chunks keeps three of them, so that the ring
     // holds a whole K = 256 tile (four stages): batched 256^3 FP16, back to back 49.0 ->
     // 47-48 us, L2 flushed 59.4 -> 57.3 us.
     static constexpr int kEpiBufs = CBUF ? ((CBUF == 4 && CHUNK > kEpiChunkBytes) ? 3 : CBUF) : 2;
