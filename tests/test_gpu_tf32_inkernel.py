@@ -207,3 +207,32 @@ def test_inkernel_timeout_is_reported_not_hung(cuda_device):
     torch.cuda.synchronize()
     assert torch.all(C == 1024.0)
     h.close()
+
+
+def _random_tf32_cases(count=40, seed=20261203):
+    """Seeded random TF32 configurations for the in-kernel rounding: shapes up to a few
+    hundred with ragged edges and K across several 512-element chunks, op combinations,
+    alpha, beta, batches and leading-dimension padding."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(count):
+        m, n = (int(x) for x in rng.integers(1, 420, 2))
+        k = int(rng.integers(1, 2600))
+        transa, transb = (int(x) for x in rng.integers(0, 2, 2))
+        alpha = float(rng.choice([1.0, 0.5, -2.0]))
+        beta = float(rng.choice([0.0, 1.0, 0.25]))
+        batch = int(rng.choice([1, 1, 3]))
+        extra_ld = int(rng.integers(0, 2))
+        cases.append((i, m, n, k, transa, transb, alpha, beta, batch, extra_ld))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_tf32_cases(), ids=lambda c: f"cfg{c[0]}")
+def test_inkernel_random_configurations(inkernel, case):
+    """Within the bound of the exact oracle and bit-exact against the block-FMA model, with
+    the guard bands and the ldc padding untouched."""
+    i, m, n, k, transa, transb, alpha, beta, batch, extra_ld = case
+    res, guards = run_colmajor(inkernel, transa, transb, m, n, k, alpha, beta, "f32", "f32",
+                               seed=7000 + i, dist="uniform", extra_ld=extra_ld, batch=batch)
+    assert guards, "guard band or ldc padding written"
+    _assert_results(res, k, alpha, beta, "f32", exact=False)
