@@ -29,14 +29,21 @@ def _code(dt):
             torch.float32: tcg.TCG_R_32F}[dt]
 
 
-@pytest.mark.parametrize("m,n,k,in_dt,compute,out_dt", CASES)
-def test_graph_replay_matches_eager(cuda_device, m, n, k, in_dt, compute, out_dt):
+# (case, TF32 rounding mode): every case with the default rounding, and the TF32 case also
+# through the in-kernel rounding option, whose counters a memset node zeroes before each
+# GEMM launch
+GRAPH_CASES = [c + (0,) for c in CASES] + [CASES[2] + (2,)]
+
+
+@pytest.mark.parametrize("m,n,k,in_dt,compute,out_dt,tf32_rounding", GRAPH_CASES)
+def test_graph_replay_matches_eager(cuda_device, m, n, k, in_dt, compute, out_dt, tf32_rounding):
     gen = torch.Generator(device="cpu").manual_seed(m + n + k)
     A = (torch.rand(k, m, generator=gen) * 2 - 1).to(in_dt).cuda()       # column-major m x k
     B = (torch.rand(n, k, generator=gen) * 2 - 1).to(in_dt).cuda()       # column-major k x n
     C0 = (torch.rand(n, m, generator=gen) * 2 - 1).to(out_dt).cuda()     # column-major m x n
     stream = torch.cuda.Stream()
     h = tcg.Handle(stream)
+    tcg.check(tcg.tcg_set_tf32_rounding(h.h, tf32_rounding))
 
     def chain(C):
         # three dependent calls: D = A B + 0.5 D, D is C
