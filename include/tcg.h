@@ -322,20 +322,24 @@ tcgStatus_t tcg_set_kernel_options(tcgHandle_t h, int cta_group, int group_m);
  * other values. */
 tcgStatus_t tcg_set_tile_n(tcgHandle_t h, int tile_n);
 
-/* Where TCG_COMPUTE_32F_FAST_TF32 calls round op(A) and op(B) to TF32 (nearest even;
+/* Where TCG_COMPUTE_32F_FAST_TF32 and TCG_COMPUTE_32F_3XTF32 calls round op(A) and op(B)
+ * to TF32 (nearest even; the two-word split also writes x - hi, rounded, as a low word;
  * "CUDA Handbook, 17.5 Tensor Cores": FP32 inputs are rounded to TF32 on the way into the
  * tensor core).  Either way the rounded values land in the same K-major workspace copies
  * and the result is the same bit for bit; only the schedule differs:
- *   0, 1  (0 is the default) two pre-pass kernels round both operands, then the GEMM
- *      kernel reads the copies;
+ *   1  two pre-pass kernels round both operands, then the GEMM kernel reads the copies;
  *   2  the GEMM kernel rounds them itself: its epilogue warps, idle while an accumulator
  *      fills, round 64 x 128 blocks of the copies in the order the tiles need them, and
  *      the loads of a K range wait until its blocks are done, so the rounding's HBM
- *      traffic overlaps the multiplication instead of preceding it.  Slower on GB300
- *      (4096 x 4096 x 16384: 808 against 697 us per call): a tensor core fed at full rate
- *      leaves the SM's shared-memory/L1 data path too little room for the rounding.
- * The two-word split (TCG_COMPUTE_32F_3XTF32) always uses the pre-pass.  Workspace:
- * mode 2 needs a few counters more (tcg_gemm_workspace_size includes them).
+ *      traffic overlaps the multiplication instead of preceding it.  Slower for TF32 on
+ *      GB300 (4096 x 4096 x 16384: 808 against 697 us per call): a tensor core fed at full
+ *      rate leaves the SM's shared-memory/L1 data path too little room for the rounding.
+ *   0  (default) 1 for TF32; for the two-word split (TCG_COMPUTE_32F_3XTF32, whose three
+ *      products per stage leave the data path more room) 2 when K is not split and
+ *      k >= 8192, else 1 (GB300: 4096 x 4096 x 16384 +2.2%, 8192^3 +1.6%; shorter or
+ *      split K lose).
+ * In mode 2 the split's GEMM kernel writes both words.  Workspace: mode 2 needs a few
+ * counters more (tcg_gemm_workspace_size includes them).
  * INVALID_VALUE: NULL h, other values. */
 tcgStatus_t tcg_set_tf32_rounding(tcgHandle_t h, int mode);
 

@@ -572,11 +572,16 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
     const int64_t nba0 = (p.batched ? p.strideA : 0) == 0 ? 1 : p.batch;
     const int64_t nbb0 = (p.batched ? p.strideB : 0) == 0 ? 1 : p.batch;
     const CvPlan cvp = cv_plan(p.m, p.n, p.k, nba0, nbb0, kBM * cg, bn);
-    // Rounding inside the GEMM kernel only when asked for (mode 2): on GB300 it loses to
-    // the pre-pass (4096 x 4096 x 16384: 808 against 697 us per call), because the tensor
-    // core fed at full rate leaves the SM's shared-memory/L1 data path almost no room for
-    // the rounding's loads and stores.
-    const bool fuse = tf32 && !split3 && h->tf32_round == 2 && cvp.items <= kMaxCvItems;
+    // Rounding inside the GEMM kernel: always in mode 2, never in mode 1; by default only
+    // for the two-word split with unsplit K of at least 8192.  Plain TF32 loses with it
+    // (4096 x 4096 x 16384: 808 against 697 us per call): a tensor core fed at full rate
+    // leaves the SM's shared-memory/L1 data path almost no room for the rounding's loads
+    // and stores.  The split's three products per stage leave more, and it gains there
+    // (GB300, same-box A/B: 4096 x 4096 x 16384 +2.2%, 8192^3 +1.6%, 2048 x 2048 x 8192
+    // +1.0%; but 4096^3 -0.6% and 1024 x 1024 x 16384, split K, -19%).
+    const bool fuse_auto = split3 && plan.splits == 1 && p.k >= 8192;
+    const bool fuse = tf32 && cvp.items <= kMaxCvItems &&
+                      (h->tf32_round == 2 || (h->tf32_round == 0 && fuse_auto));
     const size_t cv_bytes = fuse ? cv_ws_bytes(cvp) : 0;
     void *ws = nullptr;
     if (tf32_bytes + splitk_bytes + cv_bytes > 0) {
@@ -690,7 +695,7 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
             a.tail_kb_per_split = a.num_k_blocks;
         }
         a.group_m = h->group_m > 0 ? h->group_m : 8;
-        a.kind = fuse ? kKindTF32R : kind;
+        a.kind = fuse ? (split3 ? kKindTF32x3R : kKindTF32R) : kind;
         if (fuse) {
             const int64_t kp = (p.k + 3) / 4 * 4;
             const bool src_kmajor[2] = {p.transa == TCG_OP_T, p.transb == TCG_OP_N};
@@ -698,6 +703,7 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
             const int64_t ld_src[2] = {p.lda, p.ldb};
             const int64_t s_src[2] = {p.batched ? p.strideA : 0, p.batched ? p.strideB : 0};
             void *dst[2] = {const_cast<void *>(Aop), const_cast<void *>(Bop)};
+            void *dst_lo[2] = {const_cast<void *>(Alo), const_cast<void *>(Blo)};
             const int rows[2] = {m, n};
             const int prow[2] = {kBM * cg, bn};
             const int panels[2] = {cvp.panels_a, cvp.panels_b};
@@ -705,6 +711,7 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
             for (int x = 0; x < 2; ++x) {
                 a.cv_src[x] = src[x];
                 a.cv_dst[x] = dst[x];
+                a.cv_dst_lo[x] = dst_lo[x];
                 a.cv_ld[x] = ld_src[x];
                 a.cv_stride[x] = s_src[x];
                 a.cv_dstride[x] = s_src[x] == 0 ? 0 : rows[x] * kp;
@@ -1221,7 +1228,8 @@ tcgStatus_t tcg_gemm_workspace_size(tcgOp_t transa, tcgOp_t transb, int64_t m, i
             *bytes = tf32_ws_bytes(m, n, k, batch_count) +
                      cv_ws_bytes(cv_plan(m, n, k, batch_count, batch_count, kBM, kBNNarrow));
         else if (compute == TCG_COMPUTE_32F_3XTF32)
-            *bytes = 2 * tf32_ws_bytes(m, n, k, batch_count);
+            *bytes = 2 * tf32_ws_bytes(m, n, k, batch_count) +
+                     cv_ws_bytes(cv_plan(m, n, k, batch_count, batch_count, kBM, kBNNarrow));
     }
     // Split-K partial sums, as a handle with default options would split on the current
     // device (its SM count; at most kMaxSplits slices).

@@ -92,9 +92,12 @@ enum OutKind { kOutF32 = 0, kOutF16 = 1, kOutBF16 = 2 };
 // kind::tf32 (K = 8), kind::f8f6f4 with E4M3/E5M2 (K = 32).  Every kind reads 32 bytes
 // of K per instruction.  kKindTF32x3 is kind::tf32 on two words per operand (x = hi +
 // lo): four operand tiles per stage and three products per K slice into one accumulator.
-// kKindTF32R is kind::tf32 with the TF32 rounding done inside the GEMM kernel (see the
-// cv_* arguments) instead of by the separate pre-pass kernels.
-enum MmaKind { kKindF16 = 0, kKindTF32 = 1, kKindF8 = 2, kKindTF32x3 = 3, kKindTF32R = 4 };
+// kKindTF32R / kKindTF32x3R are kKindTF32 / kKindTF32x3 with the TF32 rounding (the
+// two-word split) done inside the GEMM kernel (see the cv_* arguments) instead of by the
+// separate pre-pass kernels.
+enum MmaKind {
+    kKindF16 = 0, kKindTF32 = 1, kKindF8 = 2, kKindTF32x3 = 3, kKindTF32R = 4, kKindTF32x3R = 5
+};
 
 // How an operand tile sits in global and shared memory (128-byte swizzle throughout).
 //   kK:   K contiguous.  3-D map {K, rows, batch}, box {one 128-byte row of K, rows};
@@ -151,6 +154,7 @@ struct GemmArgs {
     // per panel [cv_panels_total] (panel index cv_pbase[x] + b * cv_panels[x] + panel).
     const void *cv_src[2];
     void *cv_dst[2];
+    void *cv_dst_lo[2];        // two-word split: the low words, in the same layout
     int64_t cv_ld[2], cv_stride[2], cv_dstride[2];
     int64_t cv_kp;
     int cv_kmajor[2];

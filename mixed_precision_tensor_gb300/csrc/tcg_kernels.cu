@@ -137,6 +137,24 @@ __device__ __forceinline__ uint32_t tf32_rne_bits(uint32_t u)
     return (u + 0x0FFFu + ((u >> 13) & 1u)) & 0xFFFFE000u;
 }
 
+// Two-word TF32 split of an FP32 value ("NVIDIA Tensor Core混合精度计算原理与应用解析",
+// section 5.1: represent each operand by pieces the tensor core multiplies exactly):
+// hi = RNE_tf32(x), lo = RNE_tf32(x - hi).  x - hi is exact in FP32 (hi is within a
+// factor of two of x), so x = hi + lo up to 2^-22 |x|.  Inf and NaN keep hi = x, lo = 0;
+// a finite x that rounds past the largest TF32 value is truncated instead, so hi stays
+// finite and lo carries the rest.
+__device__ __forceinline__ void tf32_split_bits(uint32_t u, uint32_t &hi, uint32_t &lo)
+{
+    hi = tf32_rne_bits(u);
+    if ((u & 0x7F800000u) == 0x7F800000u) {
+        lo = 0u;
+        return;
+    }
+    if ((hi & 0x7F800000u) == 0x7F800000u)
+        hi = u & 0xFFFFE000u;
+    lo = tf32_rne_bits(__float_as_uint(__uint_as_float(u) - __uint_as_float(hi)));
+}
+
 // ------------------------------------------ TF32 rounding inside the GEMM kernel
 // kKindTF32R: the GEMM kernel writes the rounded K-major copies of op(A) and op(B) itself
 // while it multiplies, instead of two pre-pass kernels running before it.  The copies
@@ -179,7 +197,7 @@ __device__ __forceinline__ CvItem cv_item(const GemmArgs &p, int item)
 // (M/N-major) and each 16-byte group that starts before round_up(k, 4) is written.
 // mid() runs once every load is issued: the half's leader uses it to overlap its
 // bookkeeping (the previous sub-unit's done count, the next claim) with the loads.
-template <typename Mid>
+template <bool kSplit, typename Mid>
 __device__ __forceinline__ void cv_convert(const GemmArgs &p, int item, int s, int tid,
                                            uint32_t *tile, uint32_t bar_id, Mid &&mid)
 {
@@ -192,6 +210,23 @@ __device__ __forceinline__ void cv_convert(const GemmArgs &p, int item, int s, i
     const int64_t kp = p.cv_kp, ld = p.cv_ld[x];
     const uint32_t *src = static_cast<const uint32_t *>(p.cv_src[x]) + it.b * p.cv_stride[x];
     uint32_t *dst = static_cast<uint32_t *>(p.cv_dst[x]) + it.b * p.cv_dstride[x];
+    uint32_t *dst_lo = kSplit ? static_cast<uint32_t *>(p.cv_dst_lo[x]) + it.b * p.cv_dstride[x]
+                              : nullptr;
+    // RNE to TF32, or (two-word split) the high word with the low word written beside it
+    auto put = [&](int64_t off, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+        if constexpr (kSplit) {
+            uint4 hi, lo;
+            tf32_split_bits(a, hi.x, lo.x);
+            tf32_split_bits(b, hi.y, lo.y);
+            tf32_split_bits(c, hi.z, lo.z);
+            tf32_split_bits(d, hi.w, lo.w);
+            *reinterpret_cast<uint4 *>(dst + off) = hi;
+            *reinterpret_cast<uint4 *>(dst_lo + off) = lo;
+        } else {
+            *reinterpret_cast<uint4 *>(dst + off) =
+                make_uint4(tf32_rne_bits(a), tf32_rne_bits(b), tf32_rne_bits(c), tf32_rne_bits(d));
+        }
+    };
     if (p.cv_kmajor[x]) {
         const int j = tid & 31, rr = tid >> 5;
         const int64_t q = q0 + 4 * j;
@@ -207,11 +242,8 @@ __device__ __forceinline__ void cv_convert(const GemmArgs &p, int item, int s, i
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const int r = r0 + rr + 4 * i;
-            if (r < rows && q < kp) {
-                const uint4 o = make_uint4(tf32_rne_bits(v[i].x), tf32_rne_bits(v[i].y),
-                                           tf32_rne_bits(v[i].z), tf32_rne_bits(v[i].w));
-                *reinterpret_cast<uint4 *>(dst + q + static_cast<int64_t>(r) * kp) = o;
-            }
+            if (r < rows && q < kp)
+                put(q + static_cast<int64_t>(r) * kp, v[i].x, v[i].y, v[i].z, v[i].w);
         }
         return;
     }
@@ -249,11 +281,9 @@ __device__ __forceinline__ void cv_convert(const GemmArgs &p, int item, int s, i
             if (r >= rows || q >= k)
                 continue;
             const int sw = rl ^ (2 * c);
-            const uint4 o = make_uint4(tf32_rne_bits(tile[(4 * c) * 64 + sw]),
-                                       tf32_rne_bits(tile[(4 * c + 1) * 64 + sw]),
-                                       tf32_rne_bits(tile[(4 * c + 2) * 64 + sw]),
-                                       tf32_rne_bits(tile[(4 * c + 3) * 64 + sw]));
-            *reinterpret_cast<uint4 *>(dst + q + static_cast<int64_t>(r) * kp) = o;
+            put(q + static_cast<int64_t>(r) * kp, tile[(4 * c) * 64 + sw],
+                tile[(4 * c + 1) * 64 + sw], tile[(4 * c + 2) * 64 + sw],
+                tile[(4 * c + 3) * 64 + sw]);
         }
     }
 }
@@ -424,10 +454,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Two-word TF32 (kKindTF32x3): a stage carries A's and B's high words, then their
     // low words (tmA2, tmB2); each K slice takes three products, lo_A hi_B, hi_A lo_B and
     // hi_A hi_B, into the one accumulator.
-    constexpr bool kX3 = KIND == kKindTF32x3;
+    constexpr bool kX3 = KIND == kKindTF32x3 || KIND == kKindTF32x3R;
     // In-kernel TF32 rounding (kKindTF32R): the epilogue warps round the operands into
     // their K-major copies between accumulators and the producer waits for each item.
-    constexpr bool kFuse = KIND == kKindTF32R;
+    constexpr bool kFuse = KIND == kKindTF32R || KIND == kKindTF32x3R;
     constexpr int kOps = kX3 ? 2 : 1;                         // words per operand
     constexpr int kStages = Cfg::kRingBytes / (kOps * Cfg::kStageBytes);
     static_assert(kStages >= 2, "ring too small");
@@ -890,7 +920,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             cv_more = code == -2;
                             break;
                         }
-                        cv_convert(p, code >> 6, code & 63, rl, tile, bar_id, [&] {
+                        cv_convert<kX3>(p, code >> 6, code & 63, rl, tile, bar_id, [&] {
                             if (half_leader) {
                                 if (unreported >= 0)
                                     cv_report(p, unreported);
@@ -1219,6 +1249,8 @@ static GemmKernelFn gemm_fn_cg(int out_kind, int kind)
         return tcg_gemm_kernel<kOutF32, CG, kKindTF32x3, CBUF, kBN>;
     if (kind == kKindTF32R)
         return tcg_gemm_kernel<kOutF32, CG, kKindTF32R, CBUF, kBN>;
+    if (kind == kKindTF32x3R)
+        return tcg_gemm_kernel<kOutF32, CG, kKindTF32x3R, CBUF, kBN>;
     if (kind == kKindF8) {
         switch (out_kind) {
         case kOutF32: return tcg_gemm_kernel<kOutF32, CG, kKindF8, CBUF, kBN>;
@@ -1294,24 +1326,6 @@ int gemm_max_resident_ctas(int cta_group, int num_sms)
         return num_sms / cta_group * cta_group;
     }
     return clusters * cta_group;
-}
-
-// Two-word TF32 split of an FP32 value ("NVIDIA Tensor Core混合精度计算原理与应用解析",
-// section 5.1: represent each operand by pieces the tensor core multiplies exactly):
-// hi = RNE_tf32(x), lo = RNE_tf32(x - hi).  x - hi is exact in FP32 (hi is within a
-// factor of two of x), so x = hi + lo up to 2^-22 |x|.  Inf and NaN keep hi = x, lo = 0;
-// a finite x that rounds past the largest TF32 value is truncated instead, so hi stays
-// finite and lo carries the rest.
-__device__ __forceinline__ void tf32_split_bits(uint32_t u, uint32_t &hi, uint32_t &lo)
-{
-    hi = tf32_rne_bits(u);
-    if ((u & 0x7F800000u) == 0x7F800000u) {
-        lo = 0u;
-        return;
-    }
-    if ((hi & 0x7F800000u) == 0x7F800000u)
-        hi = u & 0xFFFFE000u;
-    lo = tf32_rne_bits(__float_as_uint(__uint_as_float(u) - __uint_as_float(hi)));
 }
 
 // K-major operand (K contiguous, `ld` elements per row of op, `rows` = K, `cols` = M or
@@ -1471,7 +1485,8 @@ cudaError_t launch_gemm(const CUtensorMap &tmA, const CUtensorMap &tmB, const CU
                         int bn, int grid, cudaStream_t s, const CUtensorMap *tmA2,
                         const CUtensorMap *tmB2)
 {
-    if ((a.kind == kKindTF32x3) != (tmA2 != nullptr && tmB2 != nullptr))
+    const bool two_words = a.kind == kKindTF32x3 || a.kind == kKindTF32x3R;
+    if (two_words != (tmA2 != nullptr && tmB2 != nullptr))
         return cudaErrorInvalidValue;
     if (bn != kBN && !(bn == kBNNarrow && gemm_has_narrow(cta_group, a.kind)))
         return cudaErrorInvalidValue;

@@ -236,3 +236,77 @@ def test_inkernel_random_configurations(inkernel, case):
                                seed=7000 + i, dist="uniform", extra_ld=extra_ld, batch=batch)
     assert guards, "guard band or ldc padding written"
     _assert_results(res, k, alpha, beta, "f32", exact=False)
+
+
+# ------------------------------------------------------- the two-word split (3xTF32)
+def _split3_call(h, transa, transb, m, n, k, A, B, C, batch=1, alpha=1.0, beta=0.0):
+    lda = m if transa == N else k
+    ldb = k if transb == N else n
+    a_cols = k if transa == N else m
+    b_cols = n if transb == N else k
+    tcg.check(tcg.tcg_gemm_strided_batched(
+        h.h, transa, transb, m, n, k, alpha, A, tcg.TCG_R_32F, lda, lda * a_cols, B,
+        tcg.TCG_R_32F, ldb, ldb * b_cols, beta, C, tcg.TCG_R_32F, m, m * n, batch,
+        tcg.TCG_COMPUTE_32F_3XTF32), "gemm")
+    tcg.check(tcg.tcg_get_device_error(h.h), "device error")
+
+
+@pytest.mark.parametrize("transa,transb", [(N, N), (T, N), (N, T), (T, T)])
+def test_split3_inkernel_matches_prepass_bit_for_bit(cuda_device, transa, transb):
+    """The two-word split with both words written by the GEMM kernel: D equals the
+    pre-pass path's bit for bit (same high and low words, same three products per K
+    slice), over more than one wave of tiles, several K chunks and a batch."""
+    m, n, k, batch = 1300, 1800, 3000, 2                      # 6 x 8 tiles per entry
+    rng = np.random.default_rng(41 + transa * 2 + transb)
+    dev = torch.device("cuda:0")
+    A = torch.from_numpy(rng.standard_normal(batch * m * k).astype(np.float32)).to(dev)
+    B = torch.from_numpy(rng.standard_normal(batch * k * n).astype(np.float32)).to(dev)
+    C0 = torch.from_numpy(rng.standard_normal(batch * m * n).astype(np.float32)).to(dev)
+    outs = []
+    for mode in (PREPASS, INKERNEL):
+        h = _handle(2, mode)
+        C = C0.clone()
+        _split3_call(h, transa, transb, m, n, k, A, B, C, batch, 0.75, -0.5)
+        outs.append(C.cpu().numpy().view(np.uint32))
+        h.close()
+    assert np.array_equal(outs[0], outs[1]), "in-kernel split differs from the pre-pass"
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 1, 1), (129, 255, 1100), (300, 520, 2049)])
+def test_split3_inkernel_within_fp32_bound(inkernel, m, n, k):
+    """Against the oracle's exact product of the FP32 inputs: within
+    (k + 8)*2^-23*(|alpha||A||B| + |beta||C|), as for the pre-pass split; integer data
+    exact."""
+    res, guards = run_colmajor(inkernel, N, T, m, n, k, 0.75, -0.5, "f32", "f32",
+                               seed=61 * m + n + k, dist="uniform", split3=True)
+    assert guards
+    got, D, R, AB, cdec, _ = res[0]
+    bound = (k + 8) * 2.0 ** -23 * (0.75 * AB + 0.5 * np.abs(cdec))
+    err = np.abs(got.astype(np.float64) - R)
+    assert np.all(err <= bound), f"worst {np.max(err / np.maximum(bound, 1e-300))}"
+    res, guards = run_colmajor(inkernel, T, N, m, n, k, 1.0, 0.5, "f32", "f32", seed=7 + k,
+                               dist="integer", batch=2, split3=True)
+    assert guards
+    for got, D, R, AB, cdec, _ in res:
+        assert values_equal(got.astype(np.float64), R)
+
+
+def test_split3_default_mode_rounds_in_the_kernel_for_long_k(cuda_device):
+    """By default the two-word split with unsplit K >= 8192 rounds inside the GEMM kernel;
+    its D equals the pre-pass path's bit for bit (48 tiles, no K split)."""
+    m, n, k = 1536, 2048, 8192
+    rng = np.random.default_rng(17)
+    dev = torch.device("cuda:0")
+    A = torch.from_numpy(rng.standard_normal(m * k).astype(np.float32)).to(dev)
+    B = torch.from_numpy(rng.standard_normal(k * n).astype(np.float32)).to(dev)
+    outs, launches = [], []
+    for mode in (PREPASS, 0):
+        h = _handle(2, mode)
+        C = torch.zeros(m * n, device=dev)
+        before = tcg.tcg_launch_count(h.h)
+        _split3_call(h, N, N, m, n, k, A, B, C)
+        launches.append(tcg.tcg_launch_count(h.h) - before)
+        outs.append(C.cpu().numpy().view(np.uint32))
+        h.close()
+    assert np.array_equal(outs[0], outs[1])
+    assert launches[1] < launches[0], launches      # no pre-pass launches by default
