@@ -409,7 +409,7 @@ size_t tf32_ws_bytes(int64_t m, int64_t n, int64_t k, int64_t batch)
 // In-kernel TF32 rounding (kKindTF32R): the rounded copies are cut into items of
 // kCvChunk K elements by one panel of tile rows (see GemmArgs::cv_*), with three
 // counters per item and panel in the workspace after the copies.
-constexpr int kCvChunk = 512;
+constexpr int kCvChunk = 1024;
 constexpr int64_t kMaxCvItems = int64_t(1) << 20;
 struct CvPlan {
     int64_t items, panels;

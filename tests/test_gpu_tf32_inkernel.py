@@ -7,7 +7,7 @@ those of the pre-pass path, so the result must be the same bit for bit -- and it
 checked the same way: bit-exact against the exact oracle on integer inputs, within the
 error bound of "NVIDIA Tensor Core混合精度计算原理与应用解析" section 2.3 on random ones,
 bit-exact against the block-FMA model (oracle.MODEL), and bit-identical to the pre-pass
-path (mode 1).  Shapes span several K chunks (512 elements) with ragged ends, every op
+path (mode 1).  Shapes span several K chunks (1024 elements) with ragged ends, every op
 combination (K-major sources rounded in place order, M/N-major ones transposed), both
 kernel variants, beta != 0 (the epilogue's C loads then stay within a tile), batches
 with a shared operand, split-K and tail-split work units.
@@ -211,7 +211,7 @@ def test_inkernel_timeout_is_reported_not_hung(cuda_device):
 
 def _random_tf32_cases(count=40, seed=20261203):
     """Seeded random TF32 configurations for the in-kernel rounding: shapes up to a few
-    hundred with ragged edges and K across several 512-element chunks, op combinations,
+    hundred with ragged edges and K across up to three 1024-element chunks, op combinations,
     alpha, beta, batches and leading-dimension padding."""
     rng = np.random.default_rng(seed)
     cases = []
