@@ -332,7 +332,7 @@ tcgStatus_t tcg_set_tile_n(tcgHandle_t h, int tile_n);
  *      fills, round 64 x 128 blocks of the copies in the order the tiles need them, and
  *      the loads of a K range wait until its blocks are done, so the rounding's HBM
  *      traffic overlaps the multiplication instead of preceding it.  Slower for TF32 on
- *      GB300 (4096 x 4096 x 16384: 808 against 697 us per call): a tensor core fed at full
+ *      GB300 (4096 x 4096 x 16384: 781 against 702 us per call): a tensor core fed at full
  *      rate leaves the SM's shared-memory/L1 data path too little room for the rounding.
  *   0  (default) 1 for TF32; for the two-word split (TCG_COMPUTE_32F_3XTF32, whose three
  *      products per stage leave the data path more room) 2 when K is not split and

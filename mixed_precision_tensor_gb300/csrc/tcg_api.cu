@@ -574,7 +574,7 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
     const CvPlan cvp = cv_plan(p.m, p.n, p.k, nba0, nbb0, kBM * cg, bn);
     // Rounding inside the GEMM kernel: always in mode 2, never in mode 1; by default only
     // for the two-word split with unsplit K of at least 8192.  Plain TF32 loses with it
-    // (4096 x 4096 x 16384: 808 against 697 us per call): a tensor core fed at full rate
+    // (4096 x 4096 x 16384: 781 against 702 us per call): a tensor core fed at full rate
     // leaves the SM's shared-memory/L1 data path almost no room for the rounding's loads
     // and stores.  The split's three products per stage leave more, and it gains there
     // (GB300, same-box A/B: 4096 x 4096 x 16384 +2.2%, 8192^3 +1.6%, 2048 x 2048 x 8192
