@@ -336,8 +336,8 @@ tcgStatus_t tcg_set_tile_n(tcgHandle_t h, int tile_n);
  *      rate leaves the SM's shared-memory/L1 data path too little room for the rounding.
  *   0  (default) 1 for TF32; for the two-word split (TCG_COMPUTE_32F_3XTF32, whose three
  *      products per stage leave the data path more room) 2 when K is not split and
- *      k >= 8192, else 1 (GB300: 4096 x 4096 x 16384 +2.2%, 8192^3 +1.6%; shorter or
- *      split K lose).
+ *      k >= 6144, else 1 (GB300: 4096 x 4096 x 16384 +4%, 2048 x 2048 x 8192 +3%,
+ *      4096 x 4096 x 6144 +2%; k = 4096 even, shorter or split K lose).
  * In mode 2 the split's GEMM kernel writes both words.  Workspace: mode 2 needs a few
  * counters more (tcg_gemm_workspace_size includes them).
  * INVALID_VALUE: NULL h, other values. */

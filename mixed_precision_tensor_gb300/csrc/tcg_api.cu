@@ -573,13 +573,15 @@ tcgStatus_t run(tcgContext *h, const Problem &p)
     const int64_t nbb0 = (p.batched ? p.strideB : 0) == 0 ? 1 : p.batch;
     const CvPlan cvp = cv_plan(p.m, p.n, p.k, nba0, nbb0, kBM * cg, bn);
     // Rounding inside the GEMM kernel: always in mode 2, never in mode 1; by default only
-    // for the two-word split with unsplit K of at least 8192.  Plain TF32 loses with it
+    // for the two-word split with unsplit K of at least 6144.  Plain TF32 loses with it
     // (4096 x 4096 x 16384: 781 against 702 us per call): a tensor core fed at full rate
     // leaves the SM's shared-memory/L1 data path almost no room for the rounding's loads
     // and stores.  The split's three products per stage leave more, and it gains there
-    // (GB300, same-box A/B: 4096 x 4096 x 16384 +2.2%, 8192^3 +1.6%, 2048 x 2048 x 8192
-    // +1.0%; but 4096^3 -0.6% and 1024 x 1024 x 16384, split K, -19%).
-    const bool fuse_auto = split3 && plan.splits == 1 && p.k >= 8192;
+    // (GB300, same-box A/B with 1024-element items: 2048 x 2048 x 8192 +3.3%, 4096 x 4096
+    // x 6144 +2.4%, 4096^3 and 8192 x 8192 x 4096 even, 4096 x 8192 x 2048 -0.9%; with
+    // 512-element items 4096 x 4096 x 16384 +2.2% and 8192^3 +1.6%, then 2.1% and 0.7% more
+    // with 1024; 1024 x 1024 x 16384, split K, -19%).
+    const bool fuse_auto = split3 && plan.splits == 1 && p.k >= 6144;
     const bool fuse = tf32 && cvp.items <= kMaxCvItems &&
                       (h->tf32_round == 2 || (h->tf32_round == 0 && fuse_auto));
     const size_t cv_bytes = fuse ? cv_ws_bytes(cvp) : 0;

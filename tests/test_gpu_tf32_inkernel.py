@@ -292,7 +292,7 @@ def test_split3_inkernel_within_fp32_bound(inkernel, m, n, k):
 
 
 def test_split3_default_mode_rounds_in_the_kernel_for_long_k(cuda_device):
-    """By default the two-word split with unsplit K >= 8192 rounds inside the GEMM kernel;
+    """By default the two-word split with unsplit K >= 6144 rounds inside the GEMM kernel;
     its D equals the pre-pass path's bit for bit (48 tiles, no K split)."""
     m, n, k = 1536, 2048, 8192
     rng = np.random.default_rng(17)
